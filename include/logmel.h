@@ -1,0 +1,212 @@
+/*
+ * logmel.h -- C ABI of liblogmel.so, the GB300 (sm_103a) log-mel front end.
+ *
+ * Two operations:
+ *
+ *  1. lm_log_mel_from_stft: Whisper's log-mel spectrogram from a complex
+ *     STFT, as defined by the KBench task spec "audio_mel_spectrogram_fused.py"
+ *     (its reference function and the per-clip definition in its spec text):
+ *         mag[b,f,k]      = re^2 + im^2                      (power)
+ *         mel[b,f,n]      = sum_k mag[b,f,k] * mel_filters[n,k]
+ *         log_spec[b,f,n] = log10(max(mel[b,f,n], 1e-10))
+ *         hi[b]           = max over (f, n) of log_spec[b,f,n]  (per clip)
+ *         out[b,f,n]      = (max(log_spec[b,f,n], hi[b] - 8) + 4) / 4
+ *     All arithmetic is f32 (the spec's precision section rules out bf16,
+ *     fp16 and fp8 anywhere on this path).
+ *
+ *  2. lm_mel_spectrogram: waveform -> mel spectrogram, the torchaudio-style
+ *     MelSpectrogram described on the "flashmel" PyPI page (usage section and
+ *     argument list): framing with center padding, periodic Hann window,
+ *     one-sided real FFT, |X|^power, triangular mel filterbank (HTK or Slaney
+ *     scale), f32 or int16 input (int16 scaled by 1/32768), f32 or f16
+ *     output, laid out [B, n_mels, n_frames].  Optionally followed by the same
+ *     log10 / per-clip clamp / rescale as operation 1.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must point to memory of the current
+ *    CUDA device; the caller owns all buffers.  Inputs are read-only.
+ *  - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *    stream); results are ready once the stream reaches that point.
+ *  - Nothing is allocated on the compute path: scratch comes from the
+ *    caller's `workspace`, sized by the matching *_workspace_size call.
+ *  - Errors are returned as lm_status, never by aborting or trapping.
+ *    Argument errors are detected on the host before anything is enqueued.
+ *    LM_ERR_CUDA means a CUDA runtime call failed; lm_last_cuda_error()
+ *    returns its code (per host thread).
+ *  - Kernels bound every wait they perform.  A wait that runs out (which
+ *    correct use never triggers) sets a device error word in the workspace
+ *    instead of hanging; lm_workspace_error() reads it.
+ */
+#ifndef LOGMEL_H_
+#define LOGMEL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *lm_stream_t;
+
+typedef enum lm_status {
+  LM_OK = 0,
+  LM_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size */
+  LM_ERR_UNSUPPORTED = 2,   /* a valid request this library does not implement */
+  LM_ERR_MISALIGNED = 3,    /* a pointer lacks the stated alignment */
+  LM_ERR_CUDA = 4,          /* a CUDA runtime call failed, see lm_last_cuda_error */
+  LM_ERR_OUT_OF_MEMORY = 5, /* plan creation could not allocate its tables */
+  LM_ERR_DEVICE_FAULT = 6,  /* a kernel reported a bounded wait that ran out */
+  LM_ERR_WORKSPACE = 7      /* workspace null or smaller than required */
+} lm_status;
+
+typedef enum lm_dtype { LM_F32 = 0, LM_I16 = 1, LM_F16 = 2 } lm_dtype;
+
+typedef enum lm_pad_mode {
+  LM_PAD_REFLECT = 0,   /* mirror about the edge sample, edge not repeated */
+  LM_PAD_CONSTANT = 1,  /* zeros */
+  LM_PAD_REPLICATE = 2, /* repeat the edge sample */
+  LM_PAD_CIRCULAR = 3   /* wrap around */
+} lm_pad_mode;
+
+typedef enum lm_mel_scale { LM_MEL_HTK = 0, LM_MEL_SLANEY = 1 } lm_mel_scale;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char *lm_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call made by this host thread
+ * inside the library (0 if none). */
+int lm_last_cuda_error(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int lm_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* 1. log-mel from a complex STFT                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace lm_log_mel_from_stft needs for B clips. */
+lm_status lm_log_mel_from_stft_workspace_size(int64_t B, size_t *bytes);
+
+/*
+ * Whisper log-mel from a complex STFT (KBench "audio_mel_spectrogram_fused"
+ * spec: reference function, per-clip definition and I/O contract).
+ *
+ *   stft        device, [B][F][NF] complex64 = interleaved (re, im) f32
+ *               pairs, contiguous, 16-byte aligned.            (read-only)
+ *   mel_filters device, [NM][NF] f32 row-major, 4-byte aligned; any dense
+ *               matrix (only the span between the first and the last
+ *               nonzero of each row is read).                  (read-only)
+ *   out         device, [B][F][NM] f32, 4-byte aligned; must not overlap
+ *               the inputs.
+ *   B, F        clips and frames per clip (B, F >= 0; F may be ragged).
+ *   NF, NM      bins per frame (1..8193) and mel bands (1..512).
+ *   workspace   device, >= lm_log_mel_from_stft_workspace_size(B) bytes,
+ *               4-byte aligned; its contents are overwritten.
+ *
+ * Errors: LM_ERR_INVALID_ARG (null pointer with B*F > 0, negative sizes),
+ * LM_ERR_UNSUPPORTED (NF or NM out of range), LM_ERR_MISALIGNED,
+ * LM_ERR_WORKSPACE, LM_ERR_CUDA.  B == 0 or F == 0 returns LM_OK and
+ * enqueues nothing.  Concurrent calls must use distinct workspaces.
+ */
+lm_status lm_log_mel_from_stft(const void *stft, const float *mel_filters, float *out, int64_t B,
+                               int64_t F, int32_t NF, int32_t NM, void *workspace,
+                               size_t workspace_bytes, lm_stream_t stream);
+
+/* How lm_log_mel_from_stft will run a problem of this shape on the current
+ * device (pure host-side planning; no work is enqueued).  Fields:
+ *   resident       1 = single cooperative launch that keeps each tile's log
+ *                  values on chip until its clip maximum is known and writes
+ *                  the output once; 0 = two launches (log values, then the
+ *                  in-place floor/rescale pass).
+ *   kernels        kernel launches per call (1 or 2; plus one memset of the
+ *                  workspace header and clip counters).
+ *   grid           CTAs of the main kernel (persistent, at most one per SM).
+ *   frames_per_tile, stages, lag: tile height, shared-memory ring depth, and
+ *                  how many tiles each thread holds back before writing.
+ *   smem_bytes     dynamic shared memory per CTA. */
+typedef struct lm_stft_launch_info {
+  int32_t resident;
+  int32_t kernels;
+  int32_t grid;
+  int32_t frames_per_tile;
+  int32_t stages;
+  int32_t lag;
+  int64_t smem_bytes;
+} lm_stft_launch_info;
+
+lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                        lm_stft_launch_info *info);
+
+/* Synchronises `stream`, then reads the device error word of a workspace
+ * used by lm_log_mel_from_stft or lm_mel_spectrogram.  *device_error = 0
+ * means no kernel reported a problem.  Returns LM_ERR_DEVICE_FAULT when it
+ * is nonzero. */
+lm_status lm_workspace_error(const void *workspace, size_t workspace_bytes, uint32_t *device_error,
+                             lm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* 2. waveform -> mel spectrogram                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Parameters of a mel spectrogram, named as torchaudio's MelSpectrogram
+ * arguments listed on the flashmel page (window is always periodic Hann,
+ * onesided always true). */
+typedef struct lm_mel_params {
+  int32_t sample_rate; /* Hz, > 0 */
+  int32_t n_fft;       /* 400, or a power of two in [64, 16384] */
+  int32_t win_length;  /* 0 = n_fft; otherwise 1..n_fft, window centred in the frame */
+  int32_t hop_length;  /* > 0 */
+  int32_t n_mels;      /* 1..256 */
+  float f_min;         /* Hz, >= 0 */
+  float f_max;         /* Hz, > f_min; <= 0 means sample_rate / 2 */
+  int32_t pad;         /* extra zero padding on both sides before framing, >= 0 */
+  int32_t center;      /* 1: pad n_fft/2 on both sides with pad_mode */
+  int32_t pad_mode;    /* lm_pad_mode */
+  float power;         /* 1 (magnitude) or 2 (power) */
+  int32_t normalized;  /* 1: scale the window by 1/sqrt(sum w^2) */
+  int32_t mel_scale;   /* lm_mel_scale */
+  int32_t slaney_norm; /* 1: each triangle scaled to unit area */
+  int32_t log_mel;     /* 1: log10(max(x,1e-10)), per-clip clamp at max-8, (x+4)/4 */
+} lm_mel_params;
+
+typedef struct lm_mel_plan lm_mel_plan;
+
+/* Validates `params`, builds the window, filterbank and FFT tables on the
+ * host in double and uploads them (rounded to f32) to the current device.
+ * Errors: LM_ERR_INVALID_ARG, LM_ERR_UNSUPPORTED, LM_ERR_OUT_OF_MEMORY,
+ * LM_ERR_CUDA.  The plan is immutable and may be shared by streams. */
+lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan **plan);
+
+/* Frees the plan's device tables (synchronises the device first). */
+lm_status lm_mel_plan_destroy(lm_mel_plan *plan);
+
+/* Number of output frames for a signal of T samples. */
+lm_status lm_mel_n_frames(const lm_mel_plan *plan, int64_t T, int64_t *n_frames);
+
+/* Bytes of device workspace lm_mel_spectrogram needs for B clips. */
+lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, size_t *bytes);
+
+/*
+ * Mel spectrogram of B waveforms (flashmel page, usage and "how it works").
+ *
+ *   wave      device, [B][T] f32 (in_dtype LM_F32) or int16 (LM_I16, scaled
+ *             by 1/32768), contiguous, 4-byte aligned.          (read-only)
+ *   out       device, [B][n_mels][n_frames] f32 (LM_F32) or f16 (LM_F16),
+ *             4-byte aligned.  log_mel plans require LM_F32.
+ *   workspace device, >= lm_mel_workspace_size(plan, B) bytes.
+ *
+ * Errors: LM_ERR_INVALID_ARG (null pointers, T too short for reflect
+ * padding, n_frames < 1), LM_ERR_UNSUPPORTED (dtype combination),
+ * LM_ERR_MISALIGNED, LM_ERR_WORKSPACE, LM_ERR_CUDA.
+ */
+lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wave, int32_t in_dtype, int64_t B,
+                             int64_t T, void *out, int32_t out_dtype, void *workspace,
+                             size_t workspace_bytes, lm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOGMEL_H_ */

@@ -1,0 +1,56 @@
+// internal.h -- declarations shared by the library's translation units.
+// Not part of the public C ABI (that is include/logmel.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "logmel.h"
+
+namespace lm {
+
+// Per-device facts the launchers need, queried once per device.
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
+};
+
+// Fills `info` for the current device.  Returns LM_ERR_CUDA on failure.
+lm_status current_device_info(DeviceInfo *info);
+
+// Records a failed CUDA call for lm_last_cuda_error() and maps it to a status.
+lm_status cuda_fail(cudaError_t e);
+
+// Checks the result of a CUDA call; on failure records it and returns LM_ERR_CUDA.
+#define LM_CUDA_TRY(expr)                               \
+  do {                                                  \
+    cudaError_t lm_e_ = (expr);                         \
+    if (lm_e_ != cudaSuccess) return ::lm::cuda_fail(lm_e_); \
+  } while (0)
+
+// Sets a kernel's dynamic shared memory limit once per (kernel, device).
+lm_status ensure_smem_attribute(const void *kernel, int bytes);
+
+// Every workspace starts with a 16-byte header whose first u32 is the
+// device error word (bit flags set by kernels whose bounded waits ran out).
+constexpr size_t kWorkspaceHeaderBytes = 16;
+
+// Reads an environment override once; returns `fallback` when unset.
+const char *env_or(const char *name, const char *fallback);
+
+// --- log_mel_from_stft -----------------------------------------------------
+
+// Workspace: header, clip_key[B], clip_done[B] (u32 each).
+size_t stft_workspace_bytes(int64_t B);
+
+// Validated launch; arguments as in lm_log_mel_from_stft.
+lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
+                          int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+lm_status stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM, lm_stft_launch_info *info);
+
+}  // namespace lm

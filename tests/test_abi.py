@@ -1,0 +1,94 @@
+"""The C-ABI library builds, loads and exports what include/logmel.h declares,
+and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import pathlib
+import re
+import subprocess
+
+import pytest
+
+ROOT = pathlib.Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "logmel.h"
+
+
+@pytest.fixture(scope="module")
+def L():
+    from log_mel_spectrogram_gb300 import build, _native
+    build.build()
+    return _native.lib()
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("lm_log_mel_from_stft", "lm_log_mel_from_stft_workspace_size", "lm_mel_plan_create",
+                 "lm_mel_spectrogram", "lm_mel_plan_destroy", "lm_workspace_error", "lm_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    from log_mel_spectrogram_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", str(build.LIB)], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        getattr(L, n)  # resolvable through ctypes too
+
+
+def test_library_is_built_for_sm_103a():
+    from log_mel_spectrogram_gb300 import build
+    assert any("compute_103a,code=sm_103a" in a for a in build.ARCH)
+
+
+def test_status_strings(L):
+    for code in range(0, 9):
+        s = L.lm_status_string(code)
+        assert s and isinstance(s, bytes)
+    assert L.lm_status_string(0) == b"LM_OK"
+    assert L.lm_version() >= 100
+
+
+def test_workspace_size(L):
+    n = ctypes.c_size_t()
+    assert L.lm_log_mel_from_stft_workspace_size(256, ctypes.byref(n)) == 0
+    assert n.value >= 16 + 2 * 4 * 256 and n.value % 256 == 0
+    assert L.lm_log_mel_from_stft_workspace_size(-1, ctypes.byref(n)) == 1
+
+
+def _call(L, stft=0x10000, filt=0x20000, out=0x30000000, B=2, F=3, NF=201, NM=80, ws=0x40000, ws_bytes=4096):
+    return L.lm_log_mel_from_stft(stft, filt, out, B, F, NF, NM, ws, ws_bytes, None)
+
+
+def test_argument_validation_needs_no_gpu(L):
+    # Every one of these is rejected before any CUDA call (the pointers are
+    # never dereferenced), so they run on a machine without a GPU.
+    assert _call(L, B=-1) == 1
+    assert _call(L, F=-5) == 1
+    assert _call(L, NF=0) == 1
+    assert _call(L, NM=0) == 1
+    assert _call(L, NM=513) == 2
+    assert _call(L, NF=9000) == 2
+    assert _call(L, stft=0) == 1
+    assert _call(L, ws=0) == 7
+    assert _call(L, stft=0x10008) == 3      # complex64 source must be 16-byte aligned
+    assert _call(L, out=0x30000002) == 3
+    assert _call(L, ws_bytes=8) == 7
+    assert _call(L, out=0x10000 + 64) == 1  # output overlapping the input
+    assert _call(L, B=0) == 0               # nothing to do
+    assert _call(L, F=0) == 0
+
+
+def test_mel_plan_validation(L):
+    from log_mel_spectrogram_gb300 import _native
+    plan = ctypes.c_void_p()
+    assert L.lm_mel_plan_create(None, ctypes.byref(plan)) == 1
+    p = _native.MelParams(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, center=1,
+                          power=2.0)
+    assert L.lm_mel_plan_create(ctypes.byref(p), None) == 1

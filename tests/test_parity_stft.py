@@ -1,0 +1,143 @@
+"""GPU parity of log_mel_from_stft against the CPU oracle.
+
+Gate (elementwise): |gpu - oracle| <= 1e-4 + 1e-4 |oracle|, the f32
+tolerance the log-mel front end is specified at; the KBench spec's
+relative-Frobenius gate (1e-4) is checked too.  Inputs come from the seeded
+generators in workloads.py and are identical on both sides.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import __graft_entry__
+    __graft_entry__.build()
+    import log_mel_spectrogram_gb300
+    return log_mel_spectrogram_gb300
+
+
+def _compare(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} outside tolerance; max err {err.max():.3g} "
+                           f"at {np.unravel_index(np.argmax(err), err.shape)}")
+    fro = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert fro <= 1e-4
+    return err.max()
+
+
+def _run(lm, oracle_mod, stft, W, check_ws=True):
+    dev = torch.device("cuda")
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(stft.shape[0]), dtype=torch.uint8, device=dev)
+    out = lm.log_mel_from_stft(stft.to(dev), W.to(dev), workspace=ws)
+    if check_ws:
+        assert lm.workspace_error(ws) == 0
+    got = out.cpu().numpy()
+    ref = oracle_mod.log_mel_from_stft(stft.numpy(), W.numpy())
+    return got, ref
+
+
+@pytest.mark.parametrize("w", workloads.STFT_WORKLOADS[:2], ids=lambda w: w.name)
+def test_small_workloads(lm, oracle_mod, w):
+    stft, W = workloads.stft_workload_inputs(w)
+    _compare(*_run(lm, oracle_mod, stft, W))
+
+
+@pytest.mark.parametrize("shape", workloads.STFT_CORRECTNESS_SHAPES, ids=str)
+def test_correctness_shapes(lm, oracle_mod, shape):
+    B, F, NF, NM = shape
+    stft, W = workloads.stft_inputs(B, F, NF, NM, seed=B * 1000 + F)
+    _compare(*_run(lm, oracle_mod, stft, W))
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 201, 80), (3, 1, 201, 128), (2, 5, 1, 1), (1, 7, 3, 2), (4, 33, 64, 40),
+                                   (3, 17, 401, 80), (5, 9, 129, 512), (2, 50, 2049, 128), (9, 3, 7, 300)],
+                         ids=str)
+def test_edge_shapes(lm, oracle_mod, shape):
+    # F = 1, NF = 1, NM = 1, even NF (every tile aligned), odd B*F*NF (the
+    # tensor ends 8 bytes past a 16-byte boundary), NM up to 512, big NF.
+    B, F, NF, NM = shape
+    stft, W = workloads.stft_inputs(B, F, NF, NM, seed=11 + B + F + NF)
+    _compare(*_run(lm, oracle_mod, stft, W))
+
+
+def test_silent_clip_and_floor(lm, oracle_mod):
+    stft, W = workloads.stft_inputs(3, 200, 201, 128, seed=5)
+    stft[1] = 0                      # silent clip: every output -1.5
+    stft[2, 100:] *= 1e-6            # 120 dB drop: the floor is active
+    got, ref = _run(lm, oracle_mod, stft, W)
+    _compare(got, ref)
+    assert np.all(got[1] == np.float32(-1.5))
+    assert np.isclose(got[2].min(), got[2].max() - 2.0, atol=1e-5)
+
+
+def test_zero_and_wide_filter_rows(lm, oracle_mod):
+    # rows with no support (mel = 0 -> -10), and rows wider than the
+    # register taps (the dense tail path): a random dense nonnegative matrix.
+    stft, W = workloads.stft_inputs(2, 90, 201, 64, seed=8)
+    W = W.clone()
+    W[3] = 0
+    W[10] = 0
+    _compare(*_run(lm, oracle_mod, stft, W))
+    Wd = torch.rand(64, 201, generator=torch.Generator().manual_seed(3))
+    _compare(*_run(lm, oracle_mod, stft, Wd))
+    Ww = workloads.triangle_filters(401, 10)  # ~80-bin triangles
+    s2, _ = workloads.stft_inputs(2, 40, 401, 10, seed=9)
+    _compare(*_run(lm, oracle_mod, s2, Ww))
+
+
+@pytest.mark.parametrize("variant", ["resident", "twopass"])
+def test_variants_agree(lm, oracle_mod, variant, monkeypatch):
+    monkeypatch.setenv("LOGMEL_K1_VARIANT", variant)
+    stft, W = workloads.stft_inputs(6, 777, 201, 128, seed=21)
+    _compare(*_run(lm, oracle_mod, stft, W))
+
+
+def test_deterministic_and_stream_aware(lm):
+    stft, W = workloads.stft_inputs(4, 500, 201, 80, seed=2, device="cuda")
+    a = lm.log_mel_from_stft(stft, W)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = lm.log_mel_from_stft(stft, W)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_empty_batch(lm):
+    stft = torch.zeros(0, 10, 201, dtype=torch.complex64, device="cuda")
+    W = torch.ones(80, 201, device="cuda")
+    assert lm.log_mel_from_stft(stft, W).shape == (0, 10, 80)
+    stft = torch.zeros(2, 0, 201, dtype=torch.complex64, device="cuda")
+    assert lm.log_mel_from_stft(stft, W).shape == (2, 0, 80)
+
+
+def test_full_size_headline_sampled(lm, oracle_mod):
+    # B=256, F=3000, NF=201, NM=128, launched exactly as the benchmark does.
+    # The oracle recomputes three whole clips; every clip is checked for the
+    # 80 dB window property.
+    w = workloads.WHISPER_STFT_B256
+    stft, W = workloads.stft_workload_inputs(w, device="cuda")
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B), dtype=torch.uint8, device="cuda")
+    out = lm.log_mel_from_stft(stft, W, workspace=ws)
+    assert lm.workspace_error(ws) == 0
+    for b in (0, 131, 255):
+        ref = oracle_mod.log_mel_from_stft(stft[b:b + 1].cpu().numpy(), W.cpu().numpy())
+        _compare(out[b:b + 1].cpu().numpy(), ref)
+    mx = out.amax(dim=(1, 2))
+    mn = out.amin(dim=(1, 2))
+    assert torch.all(mn >= mx - 2.0 - 1e-5)
+    assert torch.isfinite(out).all()
