@@ -179,9 +179,12 @@ def run_ours(args, world, rank, local):
     import log_mel_spectrogram_gb300 as lm
 
     w = workloads.WHISPER_STFT_B256
+    if args.batch and args.batch != w.B:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch, name=w.name.replace(f"b{w.B}_", f"b{args.batch}_"))
     stft, W = workloads.stft_workload_inputs(w, device=dev)
     out = torch.empty((w.B, w.F, w.NM), dtype=torch.float32, device=dev)
-    ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B, w.F, w.NF, w.NM), dtype=torch.uint8, device=dev)
     info = lm.describe_log_mel_from_stft(w.B, w.F, w.NF, w.NM)
     stream = torch.cuda.current_stream(dev)
 
@@ -223,34 +226,36 @@ def run_ours(args, world, rank, local):
     value = world * w.B * args.steps / (total_ms / 1e3)
 
     # end to end: pinned host input -> device -> library call -> host result
-    e2e_steps = max(1, min(args.steps, 5))
-    stft_h = torch.empty(stft.shape, dtype=stft.dtype, pin_memory=True)
-    stft_h.copy_(stft)
-    W_h = W.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    d_stft = torch.empty_like(stft)
-    d_W = torch.empty_like(W)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        d_stft.copy_(stft_h, non_blocking=True)
-        d_W.copy_(W_h, non_blocking=True)
-        lm.log_mel_from_stft(d_stft, d_W, out=out, workspace=ws)
-        out_h.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * w.B * e2e_steps / (e2e_ms / 1e3)
-    del d_stft
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 5))
+    e2e_value = None
+    if e2e_steps:
+        stft_h = torch.empty(stft.shape, dtype=stft.dtype, pin_memory=True)
+        stft_h.copy_(stft)
+        W_h = W.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        d_stft = torch.empty_like(stft)
+        d_W = torch.empty_like(W)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            d_stft.copy_(stft_h, non_blocking=True)
+            d_W.copy_(W_h, non_blocking=True)
+            lm.log_mel_from_stft(d_stft, d_W, out=out, workspace=ws)
+            out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e_value = world * w.B * e2e_steps / (e2e_ms / 1e3)
+        del d_stft, stft_h, out_h
 
     peak, peak_kind = _peaks()
     mean_launch_s = statistics.mean(launch_ms) / 1e3
@@ -336,6 +341,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--reference-clips", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs on smaller cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -86,8 +86,10 @@ int lm_version(void);
 /* 1. log-mel from a complex STFT                                           */
 /* ------------------------------------------------------------------------ */
 
-/* Bytes of device workspace lm_log_mel_from_stft needs for B clips. */
-lm_status lm_log_mel_from_stft_workspace_size(int64_t B, size_t *bytes);
+/* Bytes of device workspace lm_log_mel_from_stft needs for this shape
+ * (a header, one u32 per clip and one u32 per tile of frames).  Host-only. */
+lm_status lm_log_mel_from_stft_workspace_size(int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                              size_t *bytes);
 
 /*
  * Whisper log-mel from a complex STFT (KBench "audio_mel_spectrogram_fused"
@@ -102,7 +104,7 @@ lm_status lm_log_mel_from_stft_workspace_size(int64_t B, size_t *bytes);
  *               the inputs.
  *   B, F        clips and frames per clip (B, F >= 0; F may be ragged).
  *   NF, NM      bins per frame (1..8193) and mel bands (1..512).
- *   workspace   device, >= lm_log_mel_from_stft_workspace_size(B) bytes,
+ *   workspace   device, >= lm_log_mel_from_stft_workspace_size(B, F, NF, NM) bytes,
  *               4-byte aligned; its contents are overwritten.
  *
  * Errors: LM_ERR_INVALID_ARG (null pointer with B*F > 0, negative sizes),

@@ -42,9 +42,10 @@ def _require_cuda(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
-def log_mel_from_stft_workspace_size(B: int) -> int:
+def log_mel_from_stft_workspace_size(B: int, F: int, NF: int, NM: int) -> int:
     n = ctypes.c_size_t()
-    _native.check(_native.lib().lm_log_mel_from_stft_workspace_size(int(B), ctypes.byref(n)),
+    _native.check(_native.lib().lm_log_mel_from_stft_workspace_size(int(B), int(F), int(NF), int(NM),
+                                                                    ctypes.byref(n)),
                   "lm_log_mel_from_stft_workspace_size")
     return int(n.value)
 
@@ -64,7 +65,7 @@ def log_mel_from_stft(stft: torch.Tensor, mel_filters: torch.Tensor, out: torch.
         out = torch.empty((B, F, NM), dtype=torch.float32, device=stft.device)
     elif out.shape != (B, F, NM) or out.dtype != torch.float32 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [B, F, NM] float32 tensor")
-    ws_bytes = log_mel_from_stft_workspace_size(B)
+    ws_bytes = log_mel_from_stft_workspace_size(B, F, NF, NM)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=stft.device)
     elif workspace.numel() * workspace.element_size() < ws_bytes:

@@ -66,7 +66,7 @@ def lib() -> ctypes.CDLL:
         L.lm_status_string.restype = ctypes.c_char_p
         L.lm_last_cuda_error.restype = ctypes.c_int
         L.lm_version.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
+        L.lm_log_mel_from_stft_workspace_size.argtypes = [i64, i64, i32, i32, ctypes.POINTER(sz)]
         L.lm_log_mel_from_stft_workspace_size.restype = ctypes.c_int
         L.lm_log_mel_from_stft.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, sz, vp]
         L.lm_log_mel_from_stft.restype = ctypes.c_int

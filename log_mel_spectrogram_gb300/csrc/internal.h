@@ -43,8 +43,8 @@ const char *env_or(const char *name, const char *fallback);
 
 // --- log_mel_from_stft -----------------------------------------------------
 
-// Workspace: header, clip_key[B], clip_done[B] (u32 each).
-size_t stft_workspace_bytes(int64_t B);
+// Workspace bytes of lm_log_mel_from_stft for this shape.
+size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM);
 
 // Validated launch; arguments as in lm_log_mel_from_stft.
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,

@@ -50,9 +50,11 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kMonitorWarp = kConsumerWarps + 1;
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
-constexpr int kSlots = 16;       // ring of per-step tile-max and clip-max slots
+constexpr int kPublisherWarp = kConsumerWarps + 1;
+constexpr int kResolverWarp = kConsumerWarps + 2;
+constexpr int kThreads = (kConsumerWarps + 3) * 32;
+constexpr int kLag = 8;          // resident mode: steps a tile's log values stay in registers
+constexpr int kSlots = 32;       // ring of per-step tile-max and clip-max slots (> 2 kLag)
 constexpr int kMaxStages = 8;
 constexpr int kRegTaps = 8;      // filter taps held in registers per band
 constexpr int kMaxBands = 512;   // = kConsumers: one band per consumer thread
@@ -64,8 +66,8 @@ struct StftArgs {
   const float *filters;
   float *out;
   uint32_t *err;
-  uint32_t *clip_key;   // [B] order-preserving key of the clip's max log value
-  uint32_t *clip_done;  // [B] tiles of the clip already published
+  uint32_t *clip_key;   // [B] two-pass mode: order-preserving key of the clip's max log value
+  uint32_t *tile_key;   // [n_tiles] resident mode: key of each tile's max, 0 = not yet published
   int64_t B, F;
   int32_t NF, NM;
   int32_t FG;              // frame groups: active consumer threads = FG * NM
@@ -76,6 +78,7 @@ struct StftArgs {
   int32_t grid_r;          // gridDim.x % tiles_per_clip
   int32_t n_stages;
   uint32_t stage_stride;   // bytes per stage, multiple of 128
+  uint32_t aux_offset;     // shared-memory offset of SmemAux (after the stages and the ring)
   uint64_t total_bytes;    // B * F * NF * 8
 };
 
@@ -90,6 +93,7 @@ struct SmemAux {
   int32_t band_width[kMaxBands];
   int32_t max_width;
   int32_t abort_flag;
+  int64_t published;  // resident mode: steps whose tile maximum is in global memory
 };
 
 // Walks this CTA's tiles: clip index b and tile index within the clip.
@@ -148,10 +152,105 @@ __device__ __forceinline__ float rescale(float ls, float floor_v) {
   return fmaf(fmaxf(ls, floor_v), 0.25f, 1.0f);
 }
 
-template <int FPT, int L, bool kResident>
+// Per-thread constants of a consumer: its mel band, frame group and the
+// band's support with the first kRegTaps weights in registers.
+struct Band {
+  int n, fg;
+  bool active;
+  int st, wd;
+  float w[kRegTaps];
+  const float *wrow;
+};
+
+// Consumer main loop.  W = number of register taps used (4 or 8), or 0 for
+// bands wider than kRegTaps (tail weights read through L1).
+template <int FPT, int W, bool kResident>
+__device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, SmemAux &aux, float *ring,
+                                        int64_t my_tiles, const Band &c, int lane) {
+  volatile int *abort_flag = &aux.abort_flag;
+  const int S = a.n_stages;
+  const int64_t fstep = static_cast<int64_t>(a.FG) * a.NF;  // complex values between a thread's frames
+  const int ostep = a.FG * a.NM;                           // outputs between a thread's frames
+  const int slot_stride = a.TF * a.NM;
+  TileIter cit, sit;
+  cit.init(blockIdx.x, a.tiles_per_clip);
+  sit.init(blockIdx.x, a.tiles_per_clip);
+  int s = 0, slot = 0, sslot = 0;
+  uint32_t ph = 0;
+
+  // Final values of step q: (max(ls, hi - 8) + 4) / 4 from this thread's own ring entries.
+  auto store_final = [&](int64_t q) {
+    mbar_wait(&aux.hi_bar[q & (kSlots - 1)], static_cast<uint32_t>((q / kSlots) & 1), abort_flag, a.err);
+    const float floor_v = aux.hi_val[q & (kSlots - 1)] - 8.0f;
+    const int nf = sit.frames(a);
+    const float *r = ring + sslot * slot_stride + c.fg * a.NM + c.n;
+    float *o = a.out + sit.first_frame(a) * a.NM + c.fg * a.NM + c.n;
+#pragma unroll
+    for (int j = 0; j < FPT; ++j) {
+      if (c.active && c.fg + j * a.FG < nf) __stcs(o, rescale(*r, floor_v));
+      r += ostep;
+      o += ostep;
+    }
+    sit.next(a);
+    if (++sslot == kLag + 1) sslot = 0;
+  };
+
+  for (int64_t k = 0; k < my_tiles; ++k) {
+    mbar_wait(&aux.full[s], ph, abort_flag, a.err);
+    const int64_t frame0 = cit.first_frame(a);
+    const int nf = cit.frames(a);
+    const float2 *fr = reinterpret_cast<const float2 *>(smem + static_cast<size_t>(s) * a.stage_stride +
+                                                        (((frame0 * a.NF) & 1) ? 8 : 0)) +
+                       c.st + static_cast<int64_t>(c.fg) * a.NF;
+    float *dst = kResident ? ring + slot * slot_stride + c.fg * a.NM + c.n
+                           : a.out + frame0 * a.NM + c.fg * a.NM + c.n;
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < FPT; ++j) {
+      if (c.active && c.fg + j * a.FG < nf) {
+        float acc;
+        if constexpr (W > 0) {
+          acc = band_sum<W>(fr, c.wd, c.w);
+        } else {
+          acc = band_sum_wide(fr, c.wd, c.w, c.wrow);
+        }
+        const float v = __log10f(fmaxf(acc, 1e-10f));
+        lmax = fmaxf(lmax, v);
+        *dst = v;
+      }
+      fr += fstep;
+      dst += ostep;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&aux.empty[s]);
+    lmax = warp_max(lmax);
+
+    if constexpr (kResident) {
+      const int r = static_cast<int>(k & (kSlots - 1));
+      if (lane == 0) {
+        atomicMax(&aux.tmax_key[r], float_to_ordered(lmax));
+        mbar_arrive(&aux.tmax_bar[r]);
+      }
+      if (k >= kLag) store_final(k - kLag);
+      if (++slot == kLag + 1) slot = 0;
+    } else {
+      if (lane == 0) atomicMax(a.clip_key + cit.b, float_to_ordered(lmax));
+    }
+    cit.next(a);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  if constexpr (kResident) {
+    for (int64_t q = my_tiles > kLag ? my_tiles - kLag : 0; q < my_tiles; ++q) store_final(q);
+  }
+}
+
+template <int FPT, bool kResident>
 __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  SmemAux &aux = *reinterpret_cast<SmemAux *>(smem + static_cast<size_t>(a.n_stages) * a.stage_stride);
+  SmemAux &aux = *reinterpret_cast<SmemAux *>(smem + a.aux_offset);
   volatile int *abort_flag = &aux.abort_flag;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -171,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
     }
     aux.max_width = 0;
     aux.abort_flag = 0;
+    aux.published = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -211,45 +311,94 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
     return;
   }
 
-  if (warp == kMonitorWarp) {
-    // ------------- monitor: publish tile maxima, resolve clip maxima -------------
+  if (warp == kPublisherWarp) {
+    // ---- publisher: one store per tile of the tile's maximum key ----
     if (!kResident || lane != 0) return;
-    TileIter pub, res;
-    pub.init(blockIdx.x, a.tiles_per_clip);
-    res.init(blockIdx.x, a.tiles_per_clip);
     volatile uint32_t *tkey = aux.tmax_key;
-    int64_t q = 0;  // next step whose clip maximum the consumers will need
-    auto resolve = [&](int64_t step) {
-      const uint32_t *done = a.clip_done + res.b;
-      uint64_t t0 = 0;
-      while (ld_acquire_gpu(done) < static_cast<uint32_t>(a.tiles_per_clip)) {
-        if (*abort_flag) break;
-        __nanosleep(32);
-        const uint64_t now = global_timer_ns();
-        if (t0 == 0) {
-          t0 = now;
-        } else if (now - t0 > kWaitTimeoutNs) {
-          *abort_flag = 1;
-          atomicOr(a.err, kErrClipTimeout);
-          break;
-        }
-      }
-      aux.hi_val[step & (kSlots - 1)] = ordered_to_float(ld_relaxed_gpu(a.clip_key + res.b));
-      mbar_arrive(&aux.hi_bar[step & (kSlots - 1)]);
-      res.next(a);
-    };
+    volatile int64_t *published = &aux.published;
     for (int64_t k = 0; k < my_tiles; ++k) {
       const int r = static_cast<int>(k & (kSlots - 1));
       mbar_wait(&aux.tmax_bar[r], static_cast<uint32_t>((k / kSlots) & 1), abort_flag, a.err);
       const uint32_t key = tkey[r];
       tkey[r] = 0u;
-      atomicMax(a.clip_key + pub.b, key);
-      __threadfence();
-      red_add_release_gpu(a.clip_done + pub.b, 1u);
-      pub.next(a);
-      if (k + 1 - L >= 0) resolve(q++);
+      st_relaxed_gpu(a.tile_key + blockIdx.x + k * G, key);
+      *published = k + 1;
     }
-    for (; q < my_tiles; ++q) resolve(q);
+    return;
+  }
+
+  if (warp == kResolverWarp) {
+    // ---- resolver: clip maximum once every tile of the clip is published ----
+    // The slots of a clip are contiguous (tiles are numbered clip-major), so
+    // one warp-wide load pass reads them all; a zero slot means a tile of the
+    // clip is still in flight on some CTA.  Before handing over the maximum
+    // for step q the resolver waits until this CTA has published step q: that
+    // both covers this CTA's own tile and guarantees the consumers have taken
+    // the slot's previous value (step q - kSlots), so an mbarrier phase is
+    // never completed twice ahead of its waiters.
+    if (!kResident) return;
+    volatile int64_t *published = &aux.published;
+    TileIter res;
+    res.init(blockIdx.x, a.tiles_per_clip);
+    int64_t cached_b = -1;
+    float cached_hi = 0.f;
+    bool gave_up = false;
+    for (int64_t q = 0; q < my_tiles; ++q) {
+      uint64_t t0 = 0;
+      while (!gave_up && *published <= q) {
+        int stop = 0;
+        if (lane == 0) {
+          const uint64_t now = global_timer_ns();
+          if (t0 == 0) t0 = now;
+          if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            atomicOr(a.err, kErrClipTimeout);
+          }
+          stop = *abort_flag;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) gave_up = true;
+        else __nanosleep(32);
+      }
+      if (res.b != cached_b && !gave_up) {
+        const uint32_t *slots = a.tile_key + res.b * a.tiles_per_clip;
+        uint32_t m = 0;
+        t0 = 0;
+        for (;;) {
+          bool ok = true;
+          m = 0;
+#pragma unroll 4
+          for (int i = lane; i < a.tiles_per_clip; i += 32) {
+            const uint32_t v = ld_relaxed_gpu(slots + i);
+            ok = ok && (v != 0u);
+            m = max(m, v);
+          }
+          if (__all_sync(0xffffffffu, ok)) break;
+          int stop = 0;
+          if (lane == 0) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
+              *abort_flag = 1;
+              atomicOr(a.err, kErrClipTimeout);
+            }
+            stop = *abort_flag;
+          }
+          if (__shfl_sync(0xffffffffu, stop, 0)) {
+            gave_up = true;
+            break;
+          }
+          __nanosleep(128);
+        }
+        cached_b = res.b;
+        cached_hi = ordered_to_float(__reduce_max_sync(0xffffffffu, m));
+      }
+      if (lane == 0) {
+        aux.hi_val[q & (kSlots - 1)] = cached_hi;
+        mbar_arrive(&aux.hi_bar[q & (kSlots - 1)]);
+      }
+      __syncwarp();
+      res.next(a);
+    }
     return;
   }
 
@@ -276,110 +425,23 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 
-  const int ct = threadIdx.x;
-  const int n = ct % a.NM;
-  const int fg = ct / a.NM;
-  const bool active = fg < a.FG;
-  int st = 0, wd = 0;
-  float w[kRegTaps];
-  if (active) {
-    st = aux.band_start[n];
-    wd = aux.band_width[n];
-  }
-  const float *wrow = a.filters + static_cast<int64_t>(n) * a.NF + st;
+  Band band;
+  band.n = threadIdx.x % a.NM;
+  band.fg = threadIdx.x / a.NM;
+  band.active = band.fg < a.FG;
+  band.st = band.active ? aux.band_start[band.n] : 0;
+  band.wd = band.active ? aux.band_width[band.n] : 0;
+  band.wrow = a.filters + static_cast<int64_t>(band.n) * a.NF + band.st;
 #pragma unroll
-  for (int t = 0; t < kRegTaps; ++t) w[t] = (t < wd) ? __ldg(wrow + t) : 0.f;
+  for (int t = 0; t < kRegTaps; ++t) band.w[t] = (t < band.wd) ? __ldg(band.wrow + t) : 0.f;
+  float *ring = reinterpret_cast<float *>(smem + static_cast<size_t>(a.n_stages) * a.stage_stride);
   const int maxw = aux.max_width;
-
-  float ring[L + 1][FPT];
-  TileIter cit, sit;
-  cit.init(blockIdx.x, a.tiles_per_clip);
-  sit.init(blockIdx.x, a.tiles_per_clip);
-  int s = 0;
-  uint32_t ph = 0;
-
-  auto store_final = [&](const float (&v)[FPT], float floor_v) {
-    const int nf = sit.frames(a);
-    float *o = a.out + sit.first_frame(a) * a.NM + n;
-#pragma unroll
-    for (int j = 0; j < FPT; ++j) {
-      const int f = fg + j * a.FG;
-      if (active && f < nf) __stcs(o + static_cast<int64_t>(f) * a.NM, rescale(v[j], floor_v));
-    }
-    sit.next(a);
-  };
-
-  for (int64_t k = 0; k < my_tiles; ++k) {
-    mbar_wait(&aux.full[s], ph, abort_flag, a.err);
-    const int64_t frame0 = cit.first_frame(a);
-    const int nf = cit.frames(a);
-    const unsigned char *tile = smem + static_cast<size_t>(s) * a.stage_stride +
-                                (((frame0 * a.NF) & 1) ? 8 : 0);
-    const float2 *fr0 = reinterpret_cast<const float2 *>(tile) + st;
-    float lmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < FPT; ++j) {
-      const int f = fg + j * a.FG;
-      float v = -INFINITY;
-      if (active && f < nf) {
-        const float2 *fr = fr0 + static_cast<int64_t>(f) * a.NF;
-        float acc;
-        if (maxw <= 4)
-          acc = band_sum<4>(fr, wd, w);
-        else if (maxw <= kRegTaps)
-          acc = band_sum<kRegTaps>(fr, wd, w);
-        else
-          acc = band_sum_wide(fr, wd, w, wrow);
-        v = log10f(fmaxf(acc, 1e-10f));
-        lmax = fmaxf(lmax, v);
-      }
-      ring[0][j] = v;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&aux.empty[s]);
-    lmax = warp_max(lmax);
-
-    if constexpr (kResident) {
-      const int r = static_cast<int>(k & (kSlots - 1));
-      if (lane == 0) {
-        atomicMax(&aux.tmax_key[r], float_to_ordered(lmax));
-        mbar_arrive(&aux.tmax_bar[r]);
-      }
-      if (k >= L) {
-        const int64_t q = k - L;
-        mbar_wait(&aux.hi_bar[q & (kSlots - 1)], static_cast<uint32_t>((q / kSlots) & 1), abort_flag, a.err);
-        store_final(ring[L], aux.hi_val[q & (kSlots - 1)] - 8.0f);
-      }
-#pragma unroll
-      for (int d = L; d >= 1; --d)
-#pragma unroll
-        for (int j = 0; j < FPT; ++j) ring[d][j] = ring[d - 1][j];
-    } else {
-      if (lane == 0) atomicMax(a.clip_key + cit.b, float_to_ordered(lmax));
-      float *o = a.out + frame0 * a.NM + n;
-#pragma unroll
-      for (int j = 0; j < FPT; ++j) {
-        const int f = fg + j * a.FG;
-        if (active && f < nf) o[static_cast<int64_t>(f) * a.NM] = ring[0][j];
-      }
-    }
-    cit.next(a);
-    if (++s == S) {
-      s = 0;
-      ph ^= 1u;
-    }
-  }
-
-  if constexpr (kResident) {
-#pragma unroll
-    for (int d = L; d >= 1; --d) {
-      const int64_t q = my_tiles - d;
-      if (q >= 0) {
-        mbar_wait(&aux.hi_bar[q & (kSlots - 1)], static_cast<uint32_t>((q / kSlots) & 1), abort_flag, a.err);
-        store_final(ring[d], aux.hi_val[q & (kSlots - 1)] - 8.0f);
-      }
-    }
-  }
+  if (maxw <= 4)
+    consume<FPT, 4, kResident>(a, smem, aux, ring, my_tiles, band, lane);
+  else if (maxw <= kRegTaps)
+    consume<FPT, kRegTaps, kResident>(a, smem, aux, ring, my_tiles, band, lane);
+  else
+    consume<FPT, 0, kResident>(a, smem, aux, ring, my_tiles, band, lane);
 }
 
 // Two-pass epilogue: out = (max(out, hi[b] - 8) + 4) / 4 in place.
@@ -409,48 +471,60 @@ __global__ void logmel_clamp_kernel(float *out, const uint32_t *clip_key, int64_
 using KernelFn = void (*)(StftArgs);
 
 template <int FPT>
-KernelFn pick_l(int L, bool resident) {
-  if (!resident) return stft_logmel_kernel<FPT, 1, false>;
-  return L <= 4 ? stft_logmel_kernel<FPT, 4, true> : stft_logmel_kernel<FPT, 8, true>;
+KernelFn pick_variant(bool resident) {
+  return resident ? stft_logmel_kernel<FPT, true> : stft_logmel_kernel<FPT, false>;
 }
 
-KernelFn pick_kernel(int fpt, int L, bool resident) {
+KernelFn pick_kernel(int fpt, bool resident) {
   switch (fpt) {
-    case 1: return pick_l<1>(L, resident);
-    case 2: return pick_l<2>(L, resident);
-    case 4: return pick_l<4>(L, resident);
-    default: return pick_l<8>(L, resident);
+    case 1: return pick_variant<1>(resident);
+    case 2: return pick_variant<2>(resident);
+    case 4: return pick_variant<4>(resident);
+    default: return pick_variant<8>(resident);
   }
 }
 
 struct TilePlan {
   int FG, FPT, TF, S;
   uint32_t stride;
+  int64_t ring_bytes;
+  uint32_t aux_offset;
   size_t smem;
 };
 
-TilePlan plan_tiles(int NF, int NM, int max_smem) {
-  TilePlan p{};
+// Tile height: FG frame groups of NM threads, FPT frames per thread, with a
+// stage of roughly kStageTargetBytes.
+void tile_height(int NF, int NM, int *FG, int *FPT) {
   const int fg_max = kConsumers / NM;
   const int64_t frame_bytes = static_cast<int64_t>(NF) * 8;
-  p.FG = fg_max;
-  p.FPT = 0;
+  *FG = fg_max;
+  *FPT = 0;
   for (int fpt : {8, 4, 2, 1}) {
     if (static_cast<int64_t>(fg_max) * fpt * frame_bytes <= kStageTargetBytes) {
-      p.FPT = fpt;
+      *FPT = fpt;
       break;
     }
   }
-  if (p.FPT == 0) {
-    p.FPT = 1;
-    p.FG = std::max<int>(1, std::min<int64_t>(fg_max, kStageTargetBytes / frame_bytes));
+  if (*FPT == 0) {
+    *FPT = 1;
+    *FG = std::max<int>(1, std::min<int64_t>(fg_max, kStageTargetBytes / frame_bytes));
   }
+}
+
+// Shared memory: S stages | (resident) kLag+1 output slots of TF x NM | SmemAux.
+TilePlan plan_tiles(int NF, int NM, int max_smem, bool resident) {
+  TilePlan p{};
+  tile_height(NF, NM, &p.FG, &p.FPT);
   p.TF = p.FG * p.FPT;
-  const int64_t stage = static_cast<int64_t>(p.TF) * frame_bytes + 16;
+  const int64_t stage = static_cast<int64_t>(p.TF) * NF * 8 + 16;
   p.stride = static_cast<uint32_t>((stage + 127) / 128 * 128);
-  const int64_t budget = static_cast<int64_t>(std::min(max_smem, 227 * 1024)) - static_cast<int64_t>(sizeof(SmemAux)) - 128;
-  p.S = static_cast<int>(std::min<int64_t>(kMaxStages, budget / p.stride));
-  p.smem = static_cast<size_t>(p.S) * p.stride + sizeof(SmemAux);
+  p.ring_bytes = resident ? static_cast<int64_t>(kLag + 1) * p.TF * NM * 4 : 0;
+  p.ring_bytes = (p.ring_bytes + 127) / 128 * 128;
+  const int64_t budget = static_cast<int64_t>(std::min(max_smem, 227 * 1024)) -
+                         static_cast<int64_t>(sizeof(SmemAux)) - p.ring_bytes - 128;
+  p.S = budget > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, budget / p.stride)) : 0;
+  p.aux_offset = static_cast<uint32_t>(static_cast<int64_t>(p.S) * p.stride + p.ring_bytes);
+  p.smem = static_cast<size_t>(p.aux_offset) + sizeof(SmemAux);
   return p;
 }
 
@@ -467,22 +541,30 @@ struct StftLaunch {
 lm_status plan_launch(int64_t B, int64_t F, int32_t NF, int32_t NM, StftLaunch *ln) {
   DeviceInfo dev;
   if (lm_status st = current_device_info(&dev); st != LM_OK) return st;
-  ln->tp = plan_tiles(NF, NM, dev.max_smem_optin);
-  if (ln->tp.S < 2) return LM_ERR_UNSUPPORTED;
-  ln->tpc = (F + ln->tp.TF - 1) / ln->tp.TF;
+  int FG = 0, FPT = 0;
+  tile_height(NF, NM, &FG, &FPT);
+  const int TF = FG * FPT;
+  ln->tpc = (F + TF - 1) / TF;
   if (ln->tpc > INT32_MAX / 2) return LM_ERR_UNSUPPORTED;
   const int64_t n_tiles = B * ln->tpc;
   ln->grid = std::min<int64_t>(n_tiles, dev.sm_count);
   // Resident mode never deadlocks when every tile of the clip of step q sits
-  // at a step <= q + L - 1 of the static round-robin schedule.
+  // at a step <= q + L - 1 of the static round-robin schedule; the clip of
+  // tile q spans at most (grid + tpc - 2) / grid further steps.
   const int64_t L_need = 1 + (ln->grid + ln->tpc - 2) / ln->grid;
   const char *variant = env_or("LOGMEL_K1_VARIANT", "auto");
   const bool force_two = std::strcmp(variant, "twopass") == 0;
   const bool force_res = std::strcmp(variant, "resident") == 0;
-  ln->resident = !force_two && L_need <= 8;
+  ln->resident = !force_two && L_need <= kLag;
+  if (ln->resident) {
+    ln->tp = plan_tiles(NF, NM, dev.max_smem_optin, true);
+    if (ln->tp.S < 2) ln->resident = false;  // the output ring does not fit beside two stages
+  }
   if (force_res && !ln->resident) return LM_ERR_UNSUPPORTED;
-  ln->L = ln->resident ? (L_need <= 4 ? 4 : 8) : 0;
-  ln->kern = pick_kernel(ln->tp.FPT, ln->L, ln->resident);
+  if (!ln->resident) ln->tp = plan_tiles(NF, NM, dev.max_smem_optin, false);
+  if (ln->tp.S < 2) return LM_ERR_UNSUPPORTED;
+  ln->L = ln->resident ? kLag : 0;
+  ln->kern = pick_kernel(ln->tp.FPT, ln->resident);
   if (lm_status st = ensure_smem_attribute(reinterpret_cast<const void *>(ln->kern), static_cast<int>(ln->tp.smem));
       st != LM_OK)
     return st;
@@ -494,9 +576,17 @@ lm_status plan_launch(int64_t B, int64_t F, int32_t NF, int32_t NM, StftLaunch *
 
 }  // namespace
 
-size_t stft_workspace_bytes(int64_t B) {
-  const size_t b = B > 0 ? static_cast<size_t>(B) : 0;
-  return (kWorkspaceHeaderBytes + 2 * b * sizeof(uint32_t) + 255) / 256 * 256;
+// Workspace layout: header | clip_key[B] | tile_key[B * tiles_per_clip].
+static size_t tile_key_offset(int64_t B) {
+  return (kWorkspaceHeaderBytes + static_cast<size_t>(B) * sizeof(uint32_t) + 15) / 16 * 16;
+}
+
+size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM) {
+  if (B < 1 || F < 1 || NF < 1 || NM < 1 || NF > kMaxBins || NM > kMaxBands) return kWorkspaceHeaderBytes;
+  int FG = 0, FPT = 0;
+  tile_height(NF, NM, &FG, &FPT);
+  const int64_t tpc = (F + static_cast<int64_t>(FG) * FPT - 1) / (static_cast<int64_t>(FG) * FPT);
+  return (tile_key_offset(B) + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + 255) / 256 * 256;
 }
 
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
@@ -511,7 +601,8 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   if ((reinterpret_cast<uintptr_t>(stft) & 15) || (reinterpret_cast<uintptr_t>(filters) & 3) ||
       (reinterpret_cast<uintptr_t>(out) & 3) || (reinterpret_cast<uintptr_t>(workspace) & 3))
     return LM_ERR_MISALIGNED;
-  if (workspace_bytes < stft_workspace_bytes(B)) return LM_ERR_WORKSPACE;
+  const size_t ws_needed = stft_workspace_bytes(B, F, NF, NM);
+  if (workspace_bytes < ws_needed) return LM_ERR_WORKSPACE;
   {  // the output may not overlap either input
     const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + static_cast<uintptr_t>(B * F * NM) * 4;
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(stft), s1 = s0 + static_cast<uintptr_t>(B * F * NF) * 8;
@@ -533,7 +624,7 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   a.out = out;
   a.err = static_cast<uint32_t *>(workspace);
   a.clip_key = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + kWorkspaceHeaderBytes);
-  a.clip_done = a.clip_key + B;
+  a.tile_key = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + tile_key_offset(B));
   a.B = B;
   a.F = F;
   a.NF = NF;
@@ -544,11 +635,12 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   a.n_tiles = B * tpc;
   a.n_stages = tp.S;
   a.stage_stride = tp.stride;
+  a.aux_offset = tp.aux_offset;
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(F) * static_cast<uint64_t>(NF) * 8ull;
   a.grid_q = G / tpc;
   a.grid_r = static_cast<int32_t>(G % tpc);
 
-  LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, stft_workspace_bytes(B), stream));
+  LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, ws_needed, stream));
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(G));
@@ -591,9 +683,11 @@ lm_status stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM, lm_stft_la
 
 }  // namespace lm
 
-extern "C" lm_status lm_log_mel_from_stft_workspace_size(int64_t B, size_t *bytes) {
-  if (!bytes || B < 0) return LM_ERR_INVALID_ARG;
-  *bytes = lm::stft_workspace_bytes(B);
+extern "C" lm_status lm_log_mel_from_stft_workspace_size(int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                                         size_t *bytes) {
+  if (!bytes || B < 0 || F < 0 || NF < 1 || NM < 1) return LM_ERR_INVALID_ARG;
+  if (NF > 8193 || NM > 512) return LM_ERR_UNSUPPORTED;
+  *bytes = lm::stft_workspace_bytes(B, F, NF, NM);
   return LM_OK;
 }
 

@@ -57,12 +57,14 @@ def test_status_strings(L):
 
 def test_workspace_size(L):
     n = ctypes.c_size_t()
-    assert L.lm_log_mel_from_stft_workspace_size(256, ctypes.byref(n)) == 0
-    assert n.value >= 16 + 2 * 4 * 256 and n.value % 256 == 0
-    assert L.lm_log_mel_from_stft_workspace_size(-1, ctypes.byref(n)) == 1
+    assert L.lm_log_mel_from_stft_workspace_size(256, 3000, 201, 128, ctypes.byref(n)) == 0
+    # header + one u32 per clip + one u32 per 16-frame tile (188 per clip)
+    assert n.value >= 16 + 4 * 256 + 4 * 256 * 188 and n.value % 256 == 0
+    assert L.lm_log_mel_from_stft_workspace_size(-1, 10, 201, 128, ctypes.byref(n)) == 1
+    assert L.lm_log_mel_from_stft_workspace_size(2, 10, 201, 600, ctypes.byref(n)) == 2
 
 
-def _call(L, stft=0x10000, filt=0x20000, out=0x30000000, B=2, F=3, NF=201, NM=80, ws=0x40000, ws_bytes=4096):
+def _call(L, stft=0x10000, filt=0x20000, out=0x30000000, B=2, F=3, NF=201, NM=80, ws=0x40000, ws_bytes=1 << 20):
     return L.lm_log_mel_from_stft(stft, filt, out, B, F, NF, NM, ws, ws_bytes, None)
 
 

@@ -41,7 +41,7 @@ def _compare(got, ref):
 
 def _run(lm, oracle_mod, stft, W, check_ws=True):
     dev = torch.device("cuda")
-    ws = torch.empty(lm.log_mel_from_stft_workspace_size(stft.shape[0]), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(*stft.shape, W.shape[0]), dtype=torch.uint8, device=dev)
     out = lm.log_mel_from_stft(stft.to(dev), W.to(dev), workspace=ws)
     if check_ws:
         assert lm.workspace_error(ws) == 0
@@ -131,7 +131,7 @@ def test_full_size_headline_sampled(lm, oracle_mod):
     # 80 dB window property.
     w = workloads.WHISPER_STFT_B256
     stft, W = workloads.stft_workload_inputs(w, device="cuda")
-    ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B, w.F, w.NF, w.NM), dtype=torch.uint8, device="cuda")
     out = lm.log_mel_from_stft(stft, W, workspace=ws)
     assert lm.workspace_error(ws) == 0
     for b in (0, 131, 255):
