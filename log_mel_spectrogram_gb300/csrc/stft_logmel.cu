@@ -5,36 +5,40 @@
 //   mag = re^2 + im^2;  mel = mag . W^T;  ls = log10(max(mel, 1e-10));
 //   hi[b] = max over the clip of ls;  out = (max(ls, hi[b] - 8) + 4) / 4.
 //
-// Design (GB300, HBM-bound: 8 bytes read per bin, 4 written per band):
+// Design (GB300; HBM-bound: 8 bytes read per bin, 4 written per band):
 //
 //  * One persistent CTA per SM walks frame tiles in clip order
 //    (tile = blockIdx.x + k * gridDim.x).  A tile is TF consecutive frames
-//    of one clip and is contiguous in memory.
+//    of one clip and is contiguous in memory.  Tiles are numbered clip-major.
 //  * A producer warp streams tiles into an S-stage shared-memory ring with
 //    1-D bulk copies (cp.async.bulk, L2 evict-first), each stage guarded by a
 //    full/empty mbarrier pair.  Frames are 8*NF bytes, so a tile may start 8
 //    bytes off a 16-byte boundary: the copy starts at the aligned address
 //    below and the consumers index from the remainder.
-//  * 16 consumer warps compute the tile.  Thread (n, g) owns mel band n and
+//  * CW consumer warps compute the tile.  Thread (n, g) owns mel band n and
 //    frames g, g+FG, ...; its band's support (first..last nonzero of the
-//    dense filter row, found once per CTA) and up to 8 weights sit in
-//    registers, so the projection is a handful of FMAs per output fed
-//    straight from the staged complex values (power is formed on the fly).
-//  * The per-clip maximum: each warp reduces its tile maximum with shuffles
-//    and folds it into a shared slot; a monitor warp turns the slot into one
-//    atomicMax on the clip's order-preserving u32 key plus a release
-//    increment of the clip's tile counter.
-//  * Resident mode (default): consumers keep each tile's log values in
-//    registers for L more steps.  By then every tile of that clip has been
-//    published; the monitor confirms it (acquire load of the counter, bounded
-//    wait), hands the clip maximum over through an mbarrier, and the
-//    consumers write the final values once.  The output is written to HBM
-//    exactly once and never re-read: 1 read of the source + 1 write of the
-//    result, the spec's canonical traffic.  Cross-CTA waits need all CTAs
-//    resident, so this mode is launched cooperatively.
-//  * Two-pass mode (fallback when a clip spans too many steps, or forced by
-//    LOGMEL_K1_VARIANT=twopass): consumers write log values and atomicMax
-//    the clip key; a second kernel applies the floor and rescale in place.
+//    dense filter row, found once per CTA) and up to kRegTaps weights sit in
+//    registers.  Each tap is one 8-byte shared load and two packed f32x2
+//    operations: acc += (w*re, w*im) * (re, im), so power and projection are
+//    formed together and the two halves are summed once per output.
+//  * Per-clip maximum without a second HBM pass: each warp reduces its tile
+//    maximum with shuffles into a shared slot; a publisher warp stores the
+//    tile's maximum (order-preserving u32 key, 0 = not yet published) into a
+//    per-tile slot in global memory with one plain store -- no atomics, no
+//    fences.  Tiles of a clip have contiguous slots.
+//  * Resident mode (default): consumers keep each tile's log values in a
+//    shared-memory ring for kLag more steps.  A resolver warp, once its own
+//    CTA has published every step the clip can reach, reads the clip's slots
+//    in one warp-wide pass (repeating until none is zero), and hands the
+//    clip maximum to the consumers through an mbarrier; they then write the
+//    final values once.  The output is written to HBM exactly once and never
+//    re-read: one read of the source and one write of the result, the spec's
+//    canonical traffic.  Cross-CTA waits need all CTAs resident, so this mode
+//    is launched cooperatively.
+//  * Two-pass mode (a clip spans more steps than kLag, or forced with
+//    LOGMEL_K1_VARIANT=twopass): consumers write the log values, the
+//    publisher still fills the tile slots, and a second kernel reduces each
+//    clip's slots and applies the floor and rescale in place.
 #include <algorithm>
 #include <cfloat>
 #include <climits>
@@ -47,32 +51,28 @@
 namespace lm {
 namespace {
 
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kPublisherWarp = kConsumerWarps + 1;
-constexpr int kResolverWarp = kConsumerWarps + 2;
-constexpr int kThreads = (kConsumerWarps + 3) * 32;
-constexpr int kLag = 8;          // resident mode: steps a tile's log values stay in registers
-constexpr int kSlots = 32;       // ring of per-step tile-max and clip-max slots (> 2 kLag)
+constexpr int kLag = 8;          // resident mode: steps a tile's log values wait in shared memory
+constexpr int kSlots = 32;       // ring of per-step handshake slots (> kLag + 1)
 constexpr int kMaxStages = 8;
 constexpr int kRegTaps = 8;      // filter taps held in registers per band
-constexpr int kMaxBands = 512;   // = kConsumers: one band per consumer thread
+constexpr int kMaxBands = 512;
 constexpr int kMaxBins = 8193;
 constexpr int kStageTargetBytes = 48 * 1024;
+
+constexpr int threads_for(int cw) { return (cw + 3) * 32; }
 
 struct StftArgs {
   const float2 *stft;
   const float *filters;
   float *out;
   uint32_t *err;
-  uint32_t *clip_key;   // [B] two-pass mode: order-preserving key of the clip's max log value
-  uint32_t *tile_key;   // [n_tiles] resident mode: key of each tile's max, 0 = not yet published
+  uint32_t *tile_key;      // [n_tiles] key of each tile's max log value, 0 = not yet published
   int64_t B, F;
   int32_t NF, NM;
   int32_t FG;              // frame groups: active consumer threads = FG * NM
   int32_t TF;              // frames per tile (FG * FPT)
   int32_t tiles_per_clip;  // ceil(F / TF)
+  int32_t span;            // steps a clip can extend past any of its steps on one CTA
   int64_t n_tiles;         // B * tiles_per_clip
   int64_t grid_q;          // gridDim.x / tiles_per_clip
   int32_t grid_r;          // gridDim.x % tiles_per_clip
@@ -85,15 +85,18 @@ struct StftArgs {
 struct SmemAux {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t tmax_bar[kSlots];
-  uint64_t hi_bar[kSlots];
+  uint64_t tmax_bar[kSlots];  // consumers -> publisher: tile maximum folded in
+  uint64_t pub_bar[kSlots];   // publisher -> resolver: tile maximum stored
+  uint64_t hi_bar[kSlots];    // resolver -> consumers: clip maximum available
   uint32_t tmax_key[kSlots];
   float hi_val[kSlots];
+  int64_t desc_frame0[kSlots];  // producer -> consumers: first frame of step k's tile
+  int32_t desc_nf[kSlots];      // frames in the tile
+  int32_t desc_head[kSlots];    // byte offset of the tile inside its stage (0 or 8)
   int32_t band_start[kMaxBands];
   int32_t band_width[kMaxBands];
   int32_t max_width;
   int32_t abort_flag;
-  int64_t published;  // resident mode: steps whose tile maximum is in global memory
 };
 
 // Walks this CTA's tiles: clip index b and tile index within the clip.
@@ -121,30 +124,41 @@ struct TileIter {
   }
 };
 
-// sum_t w[t] * |fr[t]|^2 over the first `wd` taps, all from registers.
+// sum_t w[t] * |fr[t]|^2 over the first `wd` taps, weights from registers
+// (each w2[t] holds the weight twice).  Accumulates (w re^2, w im^2) in one
+// packed pair and adds the halves at the end.
 template <int W>
-__device__ __forceinline__ float band_sum(const float2 *fr, int wd, const float (&w)[kRegTaps]) {
-  float acc = 0.f;
+__device__ __forceinline__ float band_sum(const float2 *fr, int wd, const float2 (&w2)[kRegTaps]) {
+  float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
   for (int t = 0; t < W; ++t) {
     if (t < wd) {
       const float2 c = fr[t];
-      acc = fmaf(w[t], fmaf(c.x, c.x, c.y * c.y), acc);
+      acc = __ffma2_rn(__fmul2_rn(w2[t], c), c, acc);
     }
   }
-  return acc;
+  return acc.x + acc.y;
 }
 
-// Bands wider than kRegTaps: the remaining weights come from global memory
-// (L1-cached; the filter matrix is read-only).
-__device__ __forceinline__ float band_sum_wide(const float2 *fr, int wd, const float (&w)[kRegTaps],
+// Bands wider than kRegTaps: the remaining weights come through L1 (the
+// filter matrix is read-only).
+__device__ __forceinline__ float band_sum_wide(const float2 *fr, int wd, const float2 (&w2)[kRegTaps],
                                                const float *wrow) {
-  float acc = band_sum<kRegTaps>(fr, wd, w);
+  float acc = band_sum<kRegTaps>(fr, wd, w2);
   for (int t = kRegTaps; t < wd; ++t) {
     const float2 c = fr[t];
     acc = fmaf(__ldg(wrow + t), fmaf(c.x, c.x, c.y * c.y), acc);
   }
   return acc;
+}
+
+// log10(x) = log2(x) * log10(2) for normal x > 0 (the argument is floored
+// at 1e-10 first).  The hardware base-2 logarithm has an absolute error
+// below 2^-22 for these arguments, far inside the output tolerance.
+__device__ __forceinline__ float fast_log10(float x) {
+  float l2;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(x));
+  return l2 * 0.30102999566398120f;
 }
 
 __device__ __forceinline__ float rescale(float ls, float floor_v) {
@@ -158,85 +172,88 @@ struct Band {
   int n, fg;
   bool active;
   int st, wd;
-  float w[kRegTaps];
+  float2 w2[kRegTaps];
   const float *wrow;
 };
 
-// Consumer main loop.  W = number of register taps used (4 or 8), or 0 for
-// bands wider than kRegTaps (tail weights read through L1).
-template <int FPT, int W, bool kResident>
+// Consumer main loop.  W = number of register taps (4 or 8), or 0 for bands
+// wider than kRegTaps.
+template <int FPT, int W, bool kResident, int CW>
 __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, SmemAux &aux, float *ring,
                                         int64_t my_tiles, const Band &c, int lane) {
   volatile int *abort_flag = &aux.abort_flag;
   const int S = a.n_stages;
-  const int64_t fstep = static_cast<int64_t>(a.FG) * a.NF;  // complex values between a thread's frames
-  const int ostep = a.FG * a.NM;                           // outputs between a thread's frames
+  const int fstep = a.FG * a.NF;    // complex values between a thread's frames
+  const int ostep = a.FG * a.NM;    // outputs between a thread's frames
   const int slot_stride = a.TF * a.NM;
-  TileIter cit, sit;
-  cit.init(blockIdx.x, a.tiles_per_clip);
-  sit.init(blockIdx.x, a.tiles_per_clip);
+  const int own = c.fg * a.NM + c.n;  // this thread's first output inside a tile
   int s = 0, slot = 0, sslot = 0;
   uint32_t ph = 0;
 
-  // Final values of step q: (max(ls, hi - 8) + 4) / 4 from this thread's own ring entries.
+  // Final values of step q from this thread's own ring entries.  The tile
+  // descriptor of step q is still in its slot: the producer runs at most
+  // n_stages (< kSlots - kLag) steps ahead of the consumers.
   auto store_final = [&](int64_t q) {
-    mbar_wait(&aux.hi_bar[q & (kSlots - 1)], static_cast<uint32_t>((q / kSlots) & 1), abort_flag, a.err);
-    const float floor_v = aux.hi_val[q & (kSlots - 1)] - 8.0f;
-    const int nf = sit.frames(a);
-    const float *r = ring + sslot * slot_stride + c.fg * a.NM + c.n;
-    float *o = a.out + sit.first_frame(a) * a.NM + c.fg * a.NM + c.n;
+    const int d = static_cast<int>(q & (kSlots - 1));
+    mbar_wait(&aux.hi_bar[d], static_cast<uint32_t>((q / kSlots) & 1), abort_flag, a.err);
+    const float floor_v = aux.hi_val[d] - 8.0f;
+    const int nf = aux.desc_nf[d];
+    const float *r = ring + sslot * slot_stride + own;
+    float *o = a.out + aux.desc_frame0[d] * a.NM + own;
+    if (c.active) {
 #pragma unroll
-    for (int j = 0; j < FPT; ++j) {
-      if (c.active && c.fg + j * a.FG < nf) __stcs(o, rescale(*r, floor_v));
-      r += ostep;
-      o += ostep;
+      for (int j = 0; j < FPT; ++j)
+        if (c.fg + j * a.FG < nf) __stcs(o + j * ostep, rescale(r[j * ostep], floor_v));
     }
-    sit.next(a);
     if (++sslot == kLag + 1) sslot = 0;
   };
 
   for (int64_t k = 0; k < my_tiles; ++k) {
-    mbar_wait(&aux.full[s], ph, abort_flag, a.err);
-    const int64_t frame0 = cit.first_frame(a);
-    const int nf = cit.frames(a);
-    const float2 *fr = reinterpret_cast<const float2 *>(smem + static_cast<size_t>(s) * a.stage_stride +
-                                                        (((frame0 * a.NF) & 1) ? 8 : 0)) +
-                       c.st + static_cast<int64_t>(c.fg) * a.NF;
-    float *dst = kResident ? ring + slot * slot_stride + c.fg * a.NM + c.n
-                           : a.out + frame0 * a.NM + c.fg * a.NM + c.n;
-    float lmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < FPT; ++j) {
-      if (c.active && c.fg + j * a.FG < nf) {
-        float acc;
-        if constexpr (W > 0) {
-          acc = band_sum<W>(fr, c.wd, c.w);
-        } else {
-          acc = band_sum_wide(fr, c.wd, c.w, c.wrow);
-        }
-        const float v = __log10f(fmaxf(acc, 1e-10f));
-        lmax = fmaxf(lmax, v);
-        *dst = v;
+    if constexpr (!kResident) {
+      // Nothing else holds the consumers back in this mode: stay at most
+      // kSlots / 2 steps ahead of the publisher so no handshake slot is
+      // reused before the publisher has read it.
+      if (k >= kSlots / 2) {
+        const int64_t j = k - kSlots / 2;
+        mbar_wait(&aux.pub_bar[j & (kSlots - 1)], static_cast<uint32_t>((j / kSlots) & 1), abort_flag, a.err);
       }
-      fr += fstep;
-      dst += ostep;
+    }
+    mbar_wait(&aux.full[s], ph, abort_flag, a.err);
+    const int d = static_cast<int>(k & (kSlots - 1));
+    const int64_t frame0 = aux.desc_frame0[d];
+    const int nf = aux.desc_nf[d];
+    const float2 *fr = reinterpret_cast<const float2 *>(smem + static_cast<size_t>(s) * a.stage_stride +
+                                                        aux.desc_head[d]) +
+                       (c.st + c.fg * a.NF);
+    float *dst = kResident ? ring + slot * slot_stride + own : a.out + frame0 * a.NM + own;
+    float lmax = -INFINITY;
+    if (c.active) {
+#pragma unroll
+      for (int j = 0; j < FPT; ++j) {
+        if (nf == a.TF || c.fg + j * a.FG < nf) {
+          float acc;
+          if constexpr (W > 0) {
+            acc = band_sum<W>(fr + j * fstep, c.wd, c.w2);
+          } else {
+            acc = band_sum_wide(fr + j * fstep, c.wd, c.w2, c.wrow);
+          }
+          const float v = fast_log10(fmaxf(acc, 1e-10f));
+          lmax = fmaxf(lmax, v);
+          dst[j * ostep] = v;
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&aux.empty[s]);
-    lmax = warp_max(lmax);
-
+    const uint32_t wkey = __reduce_max_sync(0xffffffffu, float_to_ordered(lmax));
+    if (lane == 0) {
+      atomicMax(&aux.tmax_key[d], wkey);
+      mbar_arrive(&aux.tmax_bar[d]);
+    }
     if constexpr (kResident) {
-      const int r = static_cast<int>(k & (kSlots - 1));
-      if (lane == 0) {
-        atomicMax(&aux.tmax_key[r], float_to_ordered(lmax));
-        mbar_arrive(&aux.tmax_bar[r]);
-      }
       if (k >= kLag) store_final(k - kLag);
       if (++slot == kLag + 1) slot = 0;
-    } else {
-      if (lane == 0) atomicMax(a.clip_key + cit.b, float_to_ordered(lmax));
     }
-    cit.next(a);
     if (++s == S) {
       s = 0;
       ph ^= 1u;
@@ -247,8 +264,12 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
   }
 }
 
-template <int FPT, bool kResident>
-__global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs a) {
+template <int FPT, bool kResident, int CW>
+__global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const StftArgs a) {
+  constexpr int kConsumers = CW * 32;
+  constexpr int kProducerWarp = CW;
+  constexpr int kPublisherWarp = CW + 1;
+  constexpr int kResolverWarp = CW + 2;
   extern __shared__ __align__(128) unsigned char smem[];
   SmemAux &aux = *reinterpret_cast<SmemAux *>(smem + a.aux_offset);
   volatile int *abort_flag = &aux.abort_flag;
@@ -261,16 +282,16 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&aux.full[s], 1);
-      mbar_init(&aux.empty[s], kConsumerWarps);
+      mbar_init(&aux.empty[s], CW);
     }
     for (int r = 0; r < kSlots; ++r) {
-      mbar_init(&aux.tmax_bar[r], kConsumerWarps);
+      mbar_init(&aux.tmax_bar[r], CW);
+      mbar_init(&aux.pub_bar[r], 1);
       mbar_init(&aux.hi_bar[r], 1);
       aux.tmax_key[r] = 0u;
     }
     aux.max_width = 0;
     aux.abort_flag = 0;
-    aux.published = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -299,6 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
               *reinterpret_cast<const float2 *>(src + end - 8);
         }
         const uint32_t bytes = static_cast<uint32_t>(a1 - a0);
+        const int d = static_cast<int>(k & (kSlots - 1));
+        aux.desc_frame0[d] = it.first_frame(a);
+        aux.desc_nf[d] = it.frames(a);
+        aux.desc_head[d] = static_cast<int32_t>(start - a0);
         mbar_arrive_expect_tx(&aux.full[s], bytes);
         if (bytes > 0) bulk_g2s(dst, src + a0, bytes, &aux.full[s], pol);
         it.next(a);
@@ -312,57 +337,41 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
   }
 
   if (warp == kPublisherWarp) {
-    // ---- publisher: one store per tile of the tile's maximum key ----
-    if (!kResident || lane != 0) return;
+    // ---- publisher: one plain store per tile of the tile's maximum key ----
+    if (lane != 0) return;
     volatile uint32_t *tkey = aux.tmax_key;
-    volatile int64_t *published = &aux.published;
     for (int64_t k = 0; k < my_tiles; ++k) {
       const int r = static_cast<int>(k & (kSlots - 1));
       mbar_wait(&aux.tmax_bar[r], static_cast<uint32_t>((k / kSlots) & 1), abort_flag, a.err);
       const uint32_t key = tkey[r];
       tkey[r] = 0u;
       st_relaxed_gpu(a.tile_key + blockIdx.x + k * G, key);
-      *published = k + 1;
+      mbar_arrive(&aux.pub_bar[r]);
     }
     return;
   }
 
   if (warp == kResolverWarp) {
     // ---- resolver: clip maximum once every tile of the clip is published ----
-    // The slots of a clip are contiguous (tiles are numbered clip-major), so
-    // one warp-wide load pass reads them all; a zero slot means a tile of the
-    // clip is still in flight on some CTA.  Before handing over the maximum
-    // for step q the resolver waits until this CTA has published step q: that
-    // both covers this CTA's own tile and guarantees the consumers have taken
-    // the slot's previous value (step q - kSlots), so an mbarrier phase is
-    // never completed twice ahead of its waiters.
+    // For the first step q of a new clip it waits until this CTA has
+    // published step q + span (the last step the clip can reach here), then
+    // reads the clip's contiguous slots in warp-wide passes until none is
+    // zero.  Steps of an already resolved clip are answered at once.  The
+    // wait also keeps the resolver less than kSlots steps ahead of the
+    // consumers, so no handshake slot is reused before it was read.
     if (!kResident) return;
-    volatile int64_t *published = &aux.published;
     TileIter res;
     res.init(blockIdx.x, a.tiles_per_clip);
     int64_t cached_b = -1;
     float cached_hi = 0.f;
-    bool gave_up = false;
     for (int64_t q = 0; q < my_tiles; ++q) {
-      uint64_t t0 = 0;
-      while (!gave_up && *published <= q) {
-        int stop = 0;
-        if (lane == 0) {
-          const uint64_t now = global_timer_ns();
-          if (t0 == 0) t0 = now;
-          if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
-            *abort_flag = 1;
-            atomicOr(a.err, kErrClipTimeout);
-          }
-          stop = *abort_flag;
-        }
-        if (__shfl_sync(0xffffffffu, stop, 0)) gave_up = true;
-        else __nanosleep(32);
-      }
-      if (res.b != cached_b && !gave_up) {
+      if (res.b != cached_b) {
+        const int64_t target = min(q + a.span, my_tiles - 1);
+        mbar_wait(&aux.pub_bar[target & (kSlots - 1)], static_cast<uint32_t>((target / kSlots) & 1), abort_flag,
+                  a.err);
         const uint32_t *slots = a.tile_key + res.b * a.tiles_per_clip;
         uint32_t m = 0;
-        t0 = 0;
+        uint64_t t0 = 0;
         for (;;) {
           bool ok = true;
           m = 0;
@@ -383,11 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
             }
             stop = *abort_flag;
           }
-          if (__shfl_sync(0xffffffffu, stop, 0)) {
-            gave_up = true;
-            break;
-          }
-          __nanosleep(128);
+          if (__shfl_sync(0xffffffffu, stop, 0)) break;
+          __nanosleep(256);
         }
         cached_b = res.b;
         cached_hi = ordered_to_float(__reduce_max_sync(0xffffffffu, m));
@@ -404,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
 
   // ---------------------------- consumers ----------------------------
   // Support of each filter row: first and last nonzero bin.
-  for (int n = warp; n < a.NM; n += kConsumerWarps) {
+  for (int n = warp; n < a.NM; n += CW) {
     const float *row = a.filters + static_cast<int64_t>(n) * a.NF;
     int first = INT_MAX, last = -1;
     for (int k0 = 0; k0 < a.NF; k0 += 32) {
@@ -433,22 +439,35 @@ __global__ void __launch_bounds__(kThreads, 1) stft_logmel_kernel(const StftArgs
   band.wd = band.active ? aux.band_width[band.n] : 0;
   band.wrow = a.filters + static_cast<int64_t>(band.n) * a.NF + band.st;
 #pragma unroll
-  for (int t = 0; t < kRegTaps; ++t) band.w[t] = (t < band.wd) ? __ldg(band.wrow + t) : 0.f;
+  for (int t = 0; t < kRegTaps; ++t) {
+    const float wt = (t < band.wd) ? __ldg(band.wrow + t) : 0.f;
+    band.w2[t] = make_float2(wt, wt);
+  }
   float *ring = reinterpret_cast<float *>(smem + static_cast<size_t>(a.n_stages) * a.stage_stride);
   const int maxw = aux.max_width;
   if (maxw <= 4)
-    consume<FPT, 4, kResident>(a, smem, aux, ring, my_tiles, band, lane);
+    consume<FPT, 4, kResident, CW>(a, smem, aux, ring, my_tiles, band, lane);
   else if (maxw <= kRegTaps)
-    consume<FPT, kRegTaps, kResident>(a, smem, aux, ring, my_tiles, band, lane);
+    consume<FPT, kRegTaps, kResident, CW>(a, smem, aux, ring, my_tiles, band, lane);
   else
-    consume<FPT, 0, kResident>(a, smem, aux, ring, my_tiles, band, lane);
+    consume<FPT, 0, kResident, CW>(a, smem, aux, ring, my_tiles, band, lane);
 }
 
-// Two-pass epilogue: out = (max(out, hi[b] - 8) + 4) / 4 in place.
-__global__ void logmel_clamp_kernel(float *out, const uint32_t *clip_key, int64_t B, int64_t per_clip,
-                                    int vec4) {
+// Two-pass epilogue for one slice of one clip: the clip maximum is the
+// maximum of its tile slots; out = (max(out, hi - 8) + 4) / 4 in place.
+__global__ void __launch_bounds__(256) logmel_clamp_kernel(float *out, const uint32_t *tile_key, int64_t B,
+                                                           int64_t per_clip, int32_t tiles_per_clip, int vec4) {
+  __shared__ uint32_t warp_keys[8];
   for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
-    const float floor_v = ordered_to_float(clip_key[b]) - 8.0f;
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < tiles_per_clip; i += blockDim.x) m = max(m, tile_key[b * tiles_per_clip + i]);
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0) warp_keys[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = warp_keys[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = max(m, warp_keys[w]);
+    __syncthreads();
+    const float floor_v = ordered_to_float(m) - 8.0f;
     float *o = out + b * per_clip;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (vec4) {
@@ -470,32 +489,41 @@ __global__ void logmel_clamp_kernel(float *out, const uint32_t *clip_key, int64_
 
 using KernelFn = void (*)(StftArgs);
 
-template <int FPT>
+template <int FPT, int CW>
 KernelFn pick_variant(bool resident) {
-  return resident ? stft_logmel_kernel<FPT, true> : stft_logmel_kernel<FPT, false>;
+  return resident ? stft_logmel_kernel<FPT, true, CW> : stft_logmel_kernel<FPT, false, CW>;
 }
 
-KernelFn pick_kernel(int fpt, bool resident) {
+template <int CW>
+KernelFn pick_fpt(int fpt, bool resident) {
   switch (fpt) {
-    case 1: return pick_variant<1>(resident);
-    case 2: return pick_variant<2>(resident);
-    case 4: return pick_variant<4>(resident);
-    default: return pick_variant<8>(resident);
+    case 1: return pick_variant<1, CW>(resident);
+    case 2: return pick_variant<2, CW>(resident);
+    case 4: return pick_variant<4, CW>(resident);
+    default: return pick_variant<8, CW>(resident);
   }
 }
 
+KernelFn pick_kernel(int cw, int fpt, bool resident) {
+  (void)cw;
+  return pick_fpt<16>(fpt, resident);
+}
+
 struct TilePlan {
-  int FG, FPT, TF, S;
+  int CW, FG, FPT, TF, S;
   uint32_t stride;
   int64_t ring_bytes;
   uint32_t aux_offset;
   size_t smem;
 };
 
-// Tile height: FG frame groups of NM threads, FPT frames per thread, with a
-// stage of roughly kStageTargetBytes.
-void tile_height(int NF, int NM, int *FG, int *FPT) {
-  const int fg_max = kConsumers / NM;
+// Consumer warps CW, frame groups FG of NM threads, FPT frames per thread,
+// with a stage of roughly kStageTargetBytes.  Sixteen consumer warps: the
+// loop is latency-bound, and halving the warps (with twice the frames per
+// thread) measured 37% slower.
+void tile_height(int NF, int NM, int *CW, int *FG, int *FPT) {
+  *CW = 16;
+  const int fg_max = (*CW * 32) / NM;
   const int64_t frame_bytes = static_cast<int64_t>(NF) * 8;
   *FG = fg_max;
   *FPT = 0;
@@ -514,7 +542,7 @@ void tile_height(int NF, int NM, int *FG, int *FPT) {
 // Shared memory: S stages | (resident) kLag+1 output slots of TF x NM | SmemAux.
 TilePlan plan_tiles(int NF, int NM, int max_smem, bool resident) {
   TilePlan p{};
-  tile_height(NF, NM, &p.FG, &p.FPT);
+  tile_height(NF, NM, &p.CW, &p.FG, &p.FPT);
   p.TF = p.FG * p.FPT;
   const int64_t stage = static_cast<int64_t>(p.TF) * NF * 8 + 16;
   p.stride = static_cast<uint32_t>((stage + 127) / 128 * 128);
@@ -532,6 +560,7 @@ struct StftLaunch {
   TilePlan tp;
   int64_t tpc = 0;   // tiles per clip
   int64_t grid = 0;  // CTAs
+  int64_t span = 0;  // steps a clip can reach past any of its steps on one CTA
   int L = 0;         // lag in steps (resident mode)
   bool resident = false;
   KernelFn kern = nullptr;
@@ -541,21 +570,21 @@ struct StftLaunch {
 lm_status plan_launch(int64_t B, int64_t F, int32_t NF, int32_t NM, StftLaunch *ln) {
   DeviceInfo dev;
   if (lm_status st = current_device_info(&dev); st != LM_OK) return st;
-  int FG = 0, FPT = 0;
-  tile_height(NF, NM, &FG, &FPT);
+  int CW = 0, FG = 0, FPT = 0;
+  tile_height(NF, NM, &CW, &FG, &FPT);
   const int TF = FG * FPT;
   ln->tpc = (F + TF - 1) / TF;
   if (ln->tpc > INT32_MAX / 2) return LM_ERR_UNSUPPORTED;
   const int64_t n_tiles = B * ln->tpc;
   ln->grid = std::min<int64_t>(n_tiles, dev.sm_count);
-  // Resident mode never deadlocks when every tile of the clip of step q sits
-  // at a step <= q + L - 1 of the static round-robin schedule; the clip of
-  // tile q spans at most (grid + tpc - 2) / grid further steps.
-  const int64_t L_need = 1 + (ln->grid + ln->tpc - 2) / ln->grid;
+  // On the static round-robin schedule the tiles of the clip of step q lie
+  // at steps <= q + span.  Resident mode needs span < kLag: the values of
+  // step q are written at step q + kLag, after every tile of its clip.
+  ln->span = (ln->grid + ln->tpc - 2) / ln->grid;
   const char *variant = env_or("LOGMEL_K1_VARIANT", "auto");
   const bool force_two = std::strcmp(variant, "twopass") == 0;
   const bool force_res = std::strcmp(variant, "resident") == 0;
-  ln->resident = !force_two && L_need <= kLag;
+  ln->resident = !force_two && ln->span < kLag;
   if (ln->resident) {
     ln->tp = plan_tiles(NF, NM, dev.max_smem_optin, true);
     if (ln->tp.S < 2) ln->resident = false;  // the output ring does not fit beside two stages
@@ -564,29 +593,28 @@ lm_status plan_launch(int64_t B, int64_t F, int32_t NF, int32_t NM, StftLaunch *
   if (!ln->resident) ln->tp = plan_tiles(NF, NM, dev.max_smem_optin, false);
   if (ln->tp.S < 2) return LM_ERR_UNSUPPORTED;
   ln->L = ln->resident ? kLag : 0;
-  ln->kern = pick_kernel(ln->tp.FPT, ln->resident);
+  ln->kern = pick_kernel(ln->tp.CW, ln->tp.FPT, ln->resident);
   if (lm_status st = ensure_smem_attribute(reinterpret_cast<const void *>(ln->kern), static_cast<int>(ln->tp.smem));
       st != LM_OK)
     return st;
   int per_sm = 0;
-  LM_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln->kern, kThreads, ln->tp.smem));
+  LM_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln->kern, threads_for(ln->tp.CW), ln->tp.smem));
   if (per_sm < 1) return LM_ERR_UNSUPPORTED;
   return LM_OK;
 }
 
-}  // namespace
+// Workspace layout: header | tile_key[B * tiles_per_clip].
+size_t tile_key_offset() { return kWorkspaceHeaderBytes; }
 
-// Workspace layout: header | clip_key[B] | tile_key[B * tiles_per_clip].
-static size_t tile_key_offset(int64_t B) {
-  return (kWorkspaceHeaderBytes + static_cast<size_t>(B) * sizeof(uint32_t) + 15) / 16 * 16;
-}
+}  // namespace
 
 size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM) {
   if (B < 1 || F < 1 || NF < 1 || NM < 1 || NF > kMaxBins || NM > kMaxBands) return kWorkspaceHeaderBytes;
-  int FG = 0, FPT = 0;
-  tile_height(NF, NM, &FG, &FPT);
-  const int64_t tpc = (F + static_cast<int64_t>(FG) * FPT - 1) / (static_cast<int64_t>(FG) * FPT);
-  return (tile_key_offset(B) + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + 255) / 256 * 256;
+  int CW = 0, FG = 0, FPT = 0;
+  tile_height(NF, NM, &CW, &FG, &FPT);
+  const int64_t TF = static_cast<int64_t>(FG) * FPT;
+  const int64_t tpc = (F + TF - 1) / TF;
+  return (tile_key_offset() + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + 255) / 256 * 256;
 }
 
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
@@ -613,54 +641,50 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   StftLaunch ln;
   if (lm_status st = plan_launch(B, F, NF, NM, &ln); st != LM_OK) return st;
   const TilePlan &tp = ln.tp;
-  const bool resident = ln.resident;
-  const KernelFn kern = ln.kern;
-  const int64_t G = ln.grid;
-  const int64_t tpc = ln.tpc;
 
   StftArgs a{};
   a.stft = static_cast<const float2 *>(stft);
   a.filters = filters;
   a.out = out;
   a.err = static_cast<uint32_t *>(workspace);
-  a.clip_key = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + kWorkspaceHeaderBytes);
-  a.tile_key = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + tile_key_offset(B));
+  a.tile_key = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + tile_key_offset());
   a.B = B;
   a.F = F;
   a.NF = NF;
   a.NM = NM;
   a.FG = tp.FG;
   a.TF = tp.TF;
-  a.tiles_per_clip = static_cast<int32_t>(tpc);
-  a.n_tiles = B * tpc;
+  a.tiles_per_clip = static_cast<int32_t>(ln.tpc);
+  a.span = static_cast<int32_t>(ln.span);
+  a.n_tiles = B * ln.tpc;
   a.n_stages = tp.S;
   a.stage_stride = tp.stride;
   a.aux_offset = tp.aux_offset;
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(F) * static_cast<uint64_t>(NF) * 8ull;
-  a.grid_q = G / tpc;
-  a.grid_r = static_cast<int32_t>(G % tpc);
+  a.grid_q = ln.grid / ln.tpc;
+  a.grid_r = static_cast<int32_t>(ln.grid % ln.tpc);
 
   LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, ws_needed, stream));
 
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(G));
-  cfg.blockDim = dim3(kThreads);
+  cfg.gridDim = dim3(static_cast<unsigned>(ln.grid));
+  cfg.blockDim = dim3(threads_for(tp.CW));
   cfg.dynamicSmemBytes = tp.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = resident ? 1 : 0;
-  LM_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a));
+  cfg.numAttrs = ln.resident ? 1 : 0;
+  LM_CUDA_TRY(cudaLaunchKernelEx(&cfg, ln.kern, a));
 
-  if (!resident) {
+  if (!ln.resident) {
     const int64_t per_clip = F * NM;
     const int vec4 = (per_clip % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
     const int64_t work = vec4 ? per_clip / 4 : per_clip;
     const unsigned gx = static_cast<unsigned>(std::min<int64_t>((work + 255) / 256, 1024));
     const unsigned gy = static_cast<unsigned>(std::min<int64_t>(B, 65535));
-    logmel_clamp_kernel<<<dim3(gx, gy), 256, 0, stream>>>(out, a.clip_key, B, per_clip, vec4);
+    logmel_clamp_kernel<<<dim3(gx, gy), 256, 0, stream>>>(out, a.tile_key, B, per_clip, a.tiles_per_clip, vec4);
     LM_CUDA_TRY(cudaGetLastError());
   }
   return LM_OK;
