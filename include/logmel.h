@@ -141,6 +141,39 @@ typedef struct lm_stft_launch_info {
 lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM,
                                         lm_stft_launch_info *info);
 
+/* ---- Allocation-free variant (the source pages have no counterpart) ----
+ *
+ * Same computation, arguments and results as lm_log_mel_from_stft, without
+ * the workspace argument.  It is meant for callers that cannot allocate
+ * device memory themselves: code on a real-time audio thread, where a
+ * cudaMalloc may block or synchronise the whole device, or a host
+ * application that owns every byte of device memory and has no scratch to
+ * hand out.
+ *
+ * Scratch comes from one fixed array of LM_NOALLOC_SCRATCH_BYTES compiled
+ * into the library; every GPU that loads the library holds that array until
+ * the process exits.  The call allocates and frees nothing.
+ *  - A problem needing more scratch than that (16 bytes plus 4 bytes per
+ *    tile of frames; for NF = 201, NM = 128 a tile is 16 frames, so up to
+ *    about 262,000 tiles, e.g. 256 clips of up to 16,383 frames) returns
+ *    LM_ERR_WORKSPACE and enqueues nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call uses the same array, which keeps the previous call's
+ *    contents; each call clears the part it needs before its kernel runs.
+ *    Calls whose work can overlap on the GPU (different streams, or host
+ *    threads without ordering between them) race on the array: the caller
+ *    must order them.
+ *  - The device error word of these calls lives in the shared array and is
+ *    not readable through lm_workspace_error.
+ */
+#define LM_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+lm_status lm_log_mel_from_stft_noalloc(const void *stft, const float *mel_filters, float *out,
+                                       int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                       lm_stream_t stream);
+
 /* Synchronises `stream`, then reads the device error word of a workspace
  * used by lm_log_mel_from_stft or lm_mel_spectrogram.  *device_error = 0
  * means no kernel reported a problem.  Returns LM_ERR_DEVICE_FAULT when it

@@ -44,6 +44,7 @@
 #include <climits>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -725,4 +726,43 @@ extern "C" lm_status lm_log_mel_from_stft(const void *stft, const float *mel_fil
 extern "C" lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM,
                                                    lm_stft_launch_info *info) {
   return lm::stft_describe(B, F, NF, NM, info);
+}
+
+// ---- allocation-free variant -------------------------------------------------
+// Scratch for lm_log_mel_from_stft_noalloc: one fixed array in device memory,
+// present on every GPU that loads this library until the process exits.  Host
+// code may not pass `g_noalloc_scratch` itself to a kernel (in host code the
+// name is a host-side stand-in, not a device address); its device address is
+// looked up once per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoallocMaxDevices] = {};
+}  // namespace
+
+extern "C" lm_status lm_log_mel_from_stft_noalloc(const void *stft, const float *mel_filters, float *out,
+                                                  int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                                  lm_stream_t stream) {
+  if (B < 0 || F < 0 || NF < 1 || NM < 1) return LM_ERR_INVALID_ARG;
+  if (NF > 8193 || NM > 512) return LM_ERR_UNSUPPORTED;
+  if (B == 0 || F == 0) return LM_OK;
+  if (lm::stft_workspace_bytes(B, F, NF, NM) > LM_NOALLOC_SCRATCH_BYTES) return LM_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return lm::cuda_fail(e);
+  if (dev < 0 || dev >= kNoallocMaxDevices) return LM_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void *p = nullptr;
+      if (cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch); e != cudaSuccess) return lm::cuda_fail(e);
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // stft_logmel_run clears the scratch it uses before launching.
+  return lm::stft_logmel_run(stft, mel_filters, out, B, F, NF, NM, scratch, LM_NOALLOC_SCRATCH_BYTES,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
