@@ -284,6 +284,7 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": (trec["dram_bytes_per_launch"] if trec else None),
+                     "traffic_source": ("profiles/traffic.json" if trec else "stale or missing"),
                      "kernel": "stft_logmel_kernel (one cooperative launch per step, timed with the "
                                "workspace memset that precedes it)",
                      "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)},
