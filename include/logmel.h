@@ -190,13 +190,13 @@ lm_status lm_workspace_error(const void *workspace, size_t workspace_bytes, uint
  * onesided always true). */
 typedef struct lm_mel_params {
   int32_t sample_rate; /* Hz, > 0 */
-  int32_t n_fft;       /* 400, or a power of two in [64, 16384] */
+  int32_t n_fft;       /* 400, or a power of two in [64, 4096] */
   int32_t win_length;  /* 0 = n_fft; otherwise 1..n_fft, window centred in the frame */
   int32_t hop_length;  /* > 0 */
   int32_t n_mels;      /* 1..256 */
   float f_min;         /* Hz, >= 0 */
   float f_max;         /* Hz, > f_min; <= 0 means sample_rate / 2 */
-  int32_t pad;         /* extra zero padding on both sides before framing, >= 0 */
+  int32_t pad;         /* extra zero padding on both sides before framing; only 0 so far */
   int32_t center;      /* 1: pad n_fft/2 on both sides with pad_mode */
   int32_t pad_mode;    /* lm_pad_mode */
   float power;         /* 1 (magnitude) or 2 (power) */
@@ -220,8 +220,9 @@ lm_status lm_mel_plan_destroy(lm_mel_plan *plan);
 /* Number of output frames for a signal of T samples. */
 lm_status lm_mel_n_frames(const lm_mel_plan *plan, int64_t T, int64_t *n_frames);
 
-/* Bytes of device workspace lm_mel_spectrogram needs for B clips. */
-lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, size_t *bytes);
+/* Bytes of device workspace lm_mel_spectrogram needs for B clips of T
+ * samples (a header and, for log plans, one u32 per tile of frames). */
+lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, int64_t T, size_t *bytes);
 
 /*
  * Mel spectrogram of B waveforms (flashmel page, usage and "how it works").
@@ -230,7 +231,7 @@ lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, size_t *byte
  *             by 1/32768), contiguous, 4-byte aligned.          (read-only)
  *   out       device, [B][n_mels][n_frames] f32 (LM_F32) or f16 (LM_F16),
  *             4-byte aligned.  log_mel plans require LM_F32.
- *   workspace device, >= lm_mel_workspace_size(plan, B) bytes.
+ *   workspace device, >= lm_mel_workspace_size(plan, B, T) bytes.
  *
  * Errors: LM_ERR_INVALID_ARG (null pointers, T too short for reflect
  * padding, n_frames < 1), LM_ERR_UNSUPPORTED (dtype combination),

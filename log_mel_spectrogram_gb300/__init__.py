@@ -21,8 +21,7 @@ from . import _native
 from ._native import LogmelError
 
 __all__ = ["log_mel_from_stft", "log_mel_from_stft_workspace_size", "workspace_error", "LogmelError",
-           "describe_log_mel_from_stft",
-           "library_path"]
+           "describe_log_mel_from_stft", "MelSpectrogram", "mel_spectrogram", "library_path"]
 
 
 def library_path():
@@ -92,3 +91,103 @@ def workspace_error(workspace: torch.Tensor, stream=None) -> int:
     _native.lib().lm_workspace_error(workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                      ctypes.byref(v), _stream_handle(stream))
     return int(v.value)
+
+
+class MelSpectrogram:
+    """Waveform -> mel spectrogram with torchaudio MelSpectrogram argument names
+    (window fixed to periodic Hann, onesided).  Holds one library plan per
+    CUDA device.  ``log_mel=True`` adds log10(max(x, 1e-10)), the per-clip
+    clamp at max - 8 and the (x + 4) / 4 rescale."""
+
+    def __init__(self, sample_rate: int = 16000, n_fft: int = 400, win_length: int | None = None,
+                 hop_length: int | None = None, f_min: float = 0.0, f_max: float | None = None, pad: int = 0,
+                 n_mels: int = 128, power: float = 2.0, normalized: bool = False, center: bool = True,
+                 pad_mode: str = "reflect", norm: str | None = None, mel_scale: str = "htk",
+                 log_mel: bool = False, dtype: torch.dtype = torch.float32):
+        self.params = _native.MelParams(
+            sample_rate=int(sample_rate), n_fft=int(n_fft), win_length=int(win_length or 0),
+            hop_length=int(hop_length if hop_length is not None else (win_length or n_fft) // 2),
+            n_mels=int(n_mels), f_min=float(f_min), f_max=float(f_max if f_max is not None else 0.0),
+            pad=int(pad), center=int(bool(center)), pad_mode=_native.PAD_MODES[pad_mode], power=float(power),
+            normalized=int(bool(normalized)), mel_scale=_native.MEL_SCALES[mel_scale],
+            slaney_norm=int(norm == "slaney"), log_mel=int(bool(log_mel)))
+        if dtype not in (torch.float32, torch.float16):
+            raise ValueError("dtype must be torch.float32 or torch.float16")
+        self.dtype = dtype
+        self.n_mels = int(n_mels)
+        self._plans: dict[int, int] = {}
+
+    def _plan(self, device: torch.device) -> int:
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        plan = self._plans.get(idx)
+        if plan is None:
+            with torch.cuda.device(idx):
+                handle = ctypes.c_void_p()
+                _native.check(_native.lib().lm_mel_plan_create(ctypes.byref(self.params), ctypes.byref(handle)),
+                              "lm_mel_plan_create")
+            plan = self._plans[idx] = handle.value
+        return plan
+
+    def n_frames(self, T: int) -> int:
+        if not self._plans:
+            self._plan(torch.device("cuda", torch.cuda.current_device()))
+        n = ctypes.c_int64()
+        _native.check(_native.lib().lm_mel_n_frames(next(iter(self._plans.values())), int(T), ctypes.byref(n)),
+                      "lm_mel_n_frames")
+        return int(n.value)
+
+    def __call__(self, wave: torch.Tensor, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+        _require_cuda(wave, "wave")
+        if wave.dtype == torch.int16:
+            in_code = _native.DTYPES["i16"]
+        elif wave.dtype == torch.float32:
+            in_code = _native.DTYPES["f32"]
+        else:
+            raise ValueError("wave must be float32 or int16")
+        lead = wave.shape[:-1]
+        T = wave.shape[-1]
+        w2 = wave.reshape(-1, T)
+        B = w2.shape[0]
+        with torch.cuda.device(wave.device):
+            plan = self._plan(wave.device)
+            nfr = ctypes.c_int64()
+            _native.check(_native.lib().lm_mel_n_frames(plan, T, ctypes.byref(nfr)), "lm_mel_n_frames")
+            shape = (B, self.n_mels, nfr.value)
+            if out is None:
+                out = torch.empty(shape, dtype=self.dtype, device=wave.device)
+            elif tuple(out.shape) != shape or out.dtype != self.dtype or not out.is_contiguous():
+                raise ValueError(f"out must be a contiguous {shape} {self.dtype} tensor")
+            need = ctypes.c_size_t()
+            _native.check(_native.lib().lm_mel_workspace_size(plan, B, T, ctypes.byref(need)), "lm_mel_workspace_size")
+            if workspace is None:
+                workspace = torch.empty(max(need.value, 16), dtype=torch.uint8, device=wave.device)
+            out_code = _native.DTYPES["f16" if self.dtype == torch.float16 else "f32"]
+            rc = _native.lib().lm_mel_spectrogram(plan, w2.data_ptr(), in_code, B, T, out.data_ptr(), out_code,
+                                                  workspace.data_ptr(),
+                                                  workspace.numel() * workspace.element_size(),
+                                                  _stream_handle(stream))
+            _native.check(rc, "lm_mel_spectrogram")
+        return out.reshape(*lead, self.n_mels, nfr.value)
+
+    def close(self) -> None:
+        for plan in self._plans.values():
+            _native.lib().lm_mel_plan_destroy(plan)
+        self._plans.clear()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def mel_spectrogram(wave: torch.Tensor, **kwargs) -> torch.Tensor:
+    """One-shot functional form of MelSpectrogram (builds a plan per call)."""
+    m = MelSpectrogram(**kwargs)
+    try:
+        out = m(wave)
+        torch.cuda.current_stream(wave.device).synchronize()
+        return out
+    finally:
+        m.close()

@@ -80,7 +80,7 @@ def lib() -> ctypes.CDLL:
         L.lm_mel_plan_destroy.restype = ctypes.c_int
         L.lm_mel_n_frames.argtypes = [vp, i64, ctypes.POINTER(i64)]
         L.lm_mel_n_frames.restype = ctypes.c_int
-        L.lm_mel_workspace_size.argtypes = [vp, i64, ctypes.POINTER(sz)]
+        L.lm_mel_workspace_size.argtypes = [vp, i64, i64, ctypes.POINTER(sz)]
         L.lm_mel_workspace_size.restype = ctypes.c_int
         L.lm_mel_spectrogram.argtypes = [vp, vp, i32, i64, i64, vp, i32, vp, sz, vp]
         L.lm_mel_spectrogram.restype = ctypes.c_int

@@ -1,0 +1,144 @@
+// fft.cuh -- shared-memory mixed-radix complex FFT (Stockham autosort) for
+// the waveform path, plus the small in-register DFT kernels it is made of.
+//
+// Forward transform, X[k] = sum_n x[n] exp(-2 pi i n k / M).  A pass of
+// radix R after earlier passes whose radices multiply to P takes element
+// i + j*M/R (j < R) of every frame, multiplies it by exp(-2 pi i j k / (P R))
+// with k = i mod P, applies an R-point DFT and writes output l to position
+// (i - k) R + k + l P.  After the last pass (P = M) the result is in natural
+// order, so no bit reversal is needed.  Twiddles come from a table
+// W[t] = exp(-2 pi i t / M), t < M, built on the host in double precision.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace lm {
+namespace fft {
+
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+  return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
+}
+// (-i) * z
+__device__ __forceinline__ float2 mul_neg_i(float2 z) { return make_float2(z.y, -z.x); }
+__device__ __forceinline__ float2 cscale(float2 z, float s) { return make_float2(z.x * s, z.y * s); }
+
+template <int R>
+struct Dft;
+
+template <>
+struct Dft<2> {
+  __device__ __forceinline__ static void run(float2 (&u)[2]) {
+    const float2 a = u[0], b = u[1];
+    u[0] = cadd(a, b);
+    u[1] = csub(a, b);
+  }
+};
+
+template <>
+struct Dft<4> {
+  __device__ __forceinline__ static void run(float2 (&u)[4]) {
+    const float2 t0 = cadd(u[0], u[2]), t1 = csub(u[0], u[2]);
+    const float2 t2 = cadd(u[1], u[3]), t3 = mul_neg_i(csub(u[1], u[3]));
+    u[0] = cadd(t0, t2);
+    u[2] = csub(t0, t2);
+    u[1] = cadd(t1, t3);
+    u[3] = csub(t1, t3);
+  }
+};
+
+template <>
+struct Dft<8> {
+  // Two 4-point DFTs over the even and odd inputs, joined with the eighth
+  // roots of unity exp(-2 pi i l / 8), l < 4.
+  __device__ __forceinline__ static void run(float2 (&u)[8]) {
+    constexpr float h = 0.70710678118654752f;  // sqrt(1/2)
+    float2 e[4] = {u[0], u[2], u[4], u[6]};
+    float2 o[4] = {u[1], u[3], u[5], u[7]};
+    Dft<4>::run(e);
+    Dft<4>::run(o);
+    const float2 o1 = make_float2(h * (o[1].x + o[1].y), h * (o[1].y - o[1].x));   // (1 - i)/sqrt2
+    const float2 o2 = mul_neg_i(o[2]);                                               // -i
+    const float2 o3 = make_float2(h * (o[3].y - o[3].x), -h * (o[3].x + o[3].y));  // (-1 - i)/sqrt2
+    u[0] = cadd(e[0], o[0]);
+    u[4] = csub(e[0], o[0]);
+    u[1] = cadd(e[1], o1);
+    u[5] = csub(e[1], o1);
+    u[2] = cadd(e[2], o2);
+    u[6] = csub(e[2], o2);
+    u[3] = cadd(e[3], o3);
+    u[7] = csub(e[3], o3);
+  }
+};
+
+template <>
+struct Dft<5> {
+  // U_l = sum_j u_j w^{jl}, w = exp(-2 pi i / 5) = c1 - i s1, w^2 = c2 - i s2.
+  __device__ __forceinline__ static void run(float2 (&u)[5]) {
+    constexpr float c1 = 0.30901699437494742f;   // cos(2 pi / 5)
+    constexpr float c2 = -0.80901699437494742f;  // cos(4 pi / 5)
+    constexpr float s1 = 0.95105651629515357f;   // sin(2 pi / 5)
+    constexpr float s2 = 0.58778525229247313f;   // sin(4 pi / 5)
+    const float2 a1 = cadd(u[1], u[4]), a2 = cadd(u[2], u[3]);
+    const float2 b1 = csub(u[1], u[4]), b2 = csub(u[2], u[3]);
+    const float2 t1 = make_float2(u[0].x + c1 * a1.x + c2 * a2.x, u[0].y + c1 * a1.y + c2 * a2.y);
+    const float2 t2 = make_float2(u[0].x + c2 * a1.x + c1 * a2.x, u[0].y + c2 * a1.y + c1 * a2.y);
+    const float2 r1 = make_float2(s1 * b1.x + s2 * b2.x, s1 * b1.y + s2 * b2.y);  // U1 = t1 - i r1
+    const float2 r2 = make_float2(s2 * b1.x - s1 * b2.x, s2 * b1.y - s1 * b2.y);  // U2 = t2 - i r2
+    u[0] = make_float2(u[0].x + a1.x + a2.x, u[0].y + a1.y + a2.y);
+    u[1] = cadd(t1, mul_neg_i(r1));
+    u[4] = csub(t1, mul_neg_i(r1));
+    u[2] = cadd(t2, mul_neg_i(r2));
+    u[3] = csub(t2, mul_neg_i(r2));
+  }
+};
+
+// One Stockham pass over `frames` frames of M points stored back to back.
+template <int M, int R, int P>
+__device__ __forceinline__ void pass(const float2 *__restrict__ in, float2 *__restrict__ out,
+                                     const float2 *__restrict__ W, int frames) {
+  constexpr int T = M / R;
+  constexpr int TW = M / (P * R);  // twiddle table stride
+  for (int g = threadIdx.x; g < frames * T; g += blockDim.x) {
+    const int f = g / T;
+    const int i = g - f * T;
+    const int k = i % P;
+    const float2 *src = in + f * M + i;
+    float2 u[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) u[j] = src[j * T];
+    if constexpr (P > 1) {
+#pragma unroll
+      for (int j = 1; j < R; ++j) u[j] = cmul(u[j], W[j * k * TW]);
+    }
+    Dft<R>::run(u);
+    float2 *dst = out + f * M + (i - k) * R + k;
+#pragma unroll
+    for (int l = 0; l < R; ++l) dst[l * P] = u[l];
+  }
+}
+
+// Radix of the pass that follows span P: 5 while M/P has a factor 5, then 8
+// while possible, then the leftover 4 or 2.
+template <int M, int P>
+constexpr int next_radix() {
+  return ((M / P) % 5 == 0) ? 5 : ((M / P) % 8 == 0) ? 8 : ((M / P) % 4 == 0) ? 4 : 2;
+}
+
+// Runs every pass, ping-ponging between a and b.  Returns true when the
+// result ends in b.
+template <int M, int P = 1>
+__device__ __forceinline__ bool run(float2 *a, float2 *b, const float2 *W, int frames) {
+  if constexpr (P == M) {
+    return false;
+  } else {
+    constexpr int R = next_radix<M, P>();
+    pass<M, R, P>(a, b, W, frames);
+    __syncthreads();
+    return !run<M, P * R>(b, a, W, frames);
+  }
+}
+
+}  // namespace fft
+}  // namespace lm

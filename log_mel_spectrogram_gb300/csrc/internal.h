@@ -51,6 +51,11 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
                           int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
                           cudaStream_t stream);
 
+// Per-clip floor and rescale in place: out[b] = (max(out[b], hi_b - 8) + 4) / 4,
+// hi_b = the largest of the clip's tiles_per_clip order-preserving keys.
+lm_status launch_clip_clamp(float *out, const uint32_t *tile_key, int64_t B, int64_t per_clip,
+                            int32_t tiles_per_clip, cudaStream_t stream);
+
 lm_status stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM, lm_stft_launch_info *info);
 
 }  // namespace lm

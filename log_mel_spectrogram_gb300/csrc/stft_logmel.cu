@@ -679,15 +679,18 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   cfg.numAttrs = ln.resident ? 1 : 0;
   LM_CUDA_TRY(cudaLaunchKernelEx(&cfg, ln.kern, a));
 
-  if (!ln.resident) {
-    const int64_t per_clip = F * NM;
-    const int vec4 = (per_clip % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-    const int64_t work = vec4 ? per_clip / 4 : per_clip;
-    const unsigned gx = static_cast<unsigned>(std::min<int64_t>((work + 255) / 256, 1024));
-    const unsigned gy = static_cast<unsigned>(std::min<int64_t>(B, 65535));
-    logmel_clamp_kernel<<<dim3(gx, gy), 256, 0, stream>>>(out, a.tile_key, B, per_clip, a.tiles_per_clip, vec4);
-    LM_CUDA_TRY(cudaGetLastError());
-  }
+  if (!ln.resident) return launch_clip_clamp(out, a.tile_key, B, F * NM, a.tiles_per_clip, stream);
+  return LM_OK;
+}
+
+lm_status launch_clip_clamp(float *out, const uint32_t *tile_key, int64_t B, int64_t per_clip,
+                            int32_t tiles_per_clip, cudaStream_t stream) {
+  const int vec4 = (per_clip % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
+  const int64_t work = vec4 ? per_clip / 4 : per_clip;
+  const unsigned gx = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 1024)));
+  const unsigned gy = static_cast<unsigned>(std::min<int64_t>(B, 65535));
+  logmel_clamp_kernel<<<dim3(gx, gy), 256, 0, stream>>>(out, tile_key, B, per_clip, tiles_per_clip, vec4);
+  LM_CUDA_TRY(cudaGetLastError());
   return LM_OK;
 }
 

@@ -1,28 +1,526 @@
-// wave_mel.cu -- waveform -> mel spectrogram (placeholder entry points until
-// the FFT kernel lands; every call reports LM_ERR_UNSUPPORTED).
+// wave_mel.cu -- waveform -> mel spectrogram (the torchaudio-style
+// MelSpectrogram on the "flashmel" PyPI page: usage, argument list and
+// "How it works"), with the optional log10 / per-clip clamp / rescale of
+// the KBench "audio_mel_spectrogram_fused" spec.
+//
+// Plan (host, once): periodic Hann window (win_length centred in n_fft,
+// optional 1/sqrt(sum w^2) normalisation folded in), FFT twiddles and the
+// triangular mel filterbank, all computed in double and rounded to f32; the
+// filterbank is packed per band as first nonzero bin, width and weights.
+//
+// Kernel (one persistent CTA per SM slot, tiles of TF consecutive frames of
+// one clip):
+//  1. framing: frame t reads samples t*hop - n_fft/2 + j of the clip; the
+//     padding (reflect / constant / replicate / circular) is index
+//     arithmetic, and tiles that touch no edge load samples directly.  Pairs
+//     of windowed samples form the N/2 complex points z[n] = x[2n] + i x[2n+1];
+//  2. an N/2-point complex FFT in shared memory (fft.cuh);
+//  3. the real-input untangle X[k] = E[k] + exp(-2 pi i k/N) O[k], with
+//     E = (Z[k] + conj Z[N/2-k]) / 2 and O = (Z[k] - conj Z[N/2-k]) / (2i),
+//     straight into a power tile |X[k]|^power (odd row stride);
+//  4. the banded mel projection, one output per thread, lanes over frames so
+//     each band's row of the output [B, n_mels, n_frames] is written as a run
+//     of consecutive frames; f32 or f16 (round to nearest even) at the store;
+//  5. log plans store log10(max(mel, 1e-10)) and publish each tile's maximum
+//     into a per-tile slot; a second kernel (the clamp epilogue shared with
+//     the STFT path) turns slots into clip maxima and rescales in place.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda_fp16.h>
+
+#include "fft.cuh"
 #include "internal.h"
+#include "ptx.cuh"
+
+struct lm_mel_plan {
+  lm_mel_params p;
+  int device;
+  int n_freqs;   // n_fft / 2 + 1
+  int wmax;      // widest filter row, in bins
+  float *window; // [n_fft]
+  float2 *tw_m;  // [n_fft/2]      exp(-2 pi i t / (n_fft/2))
+  float2 *tw_n;  // [n_fft/2 + 1]  exp(-2 pi i k / n_fft)
+  int *fstart;   // [n_mels]
+  int *fwidth;   // [n_mels]
+  float *fw;     // [n_mels][wmax]
+};
+
+namespace lm {
+namespace {
+
+constexpr int kWaveThreads = 256;
+
+struct WaveArgs {
+  const void *wave;
+  void *out;
+  uint32_t *tile_key;
+  int64_t B, T, n_frames;
+  int32_t in_i16, out_f16, log_mel, power_is_one;
+  int32_t hop, pad_left, pad_mode;
+  int32_t n_mels, wmax, tiles_per_clip, TF;
+  const float *window;
+  const float2 *tw_m;
+  const float2 *tw_n;
+  const int *fstart;
+  const int *fwidth;
+  const float *fw;
+};
+
+__device__ __forceinline__ int64_t map_index(int64_t s, int64_t T, int mode, bool *zero) {
+  *zero = false;
+  if (s >= 0 && s < T) return s;
+  switch (mode) {
+    case LM_PAD_CONSTANT: *zero = true; return 0;
+    case LM_PAD_REPLICATE: return s < 0 ? 0 : T - 1;
+    case LM_PAD_CIRCULAR: { int64_t r = s % T; return r < 0 ? r + T : r; }
+    default: return s < 0 ? -s : 2 * (T - 1) - s;  // reflect, edge not repeated
+  }
+}
+
+__device__ __forceinline__ float load_sample(const WaveArgs &a, int64_t b, int64_t s) {
+  if (a.in_i16) return static_cast<float>(static_cast<const int16_t *>(a.wave)[b * a.T + s]) * (1.0f / 32768.0f);
+  return static_cast<const float *>(a.wave)[b * a.T + s];
+}
+
+template <int NFFT>
+struct WaveCfg {
+  static constexpr int M = NFFT / 2;
+  static constexpr int NF = NFFT / 2 + 1;
+  static constexpr int NFP = NF | 1;  // odd power-tile row stride
+  // frames per tile: enough work for 256 threads, bounded by shared memory
+  static constexpr int TF = NFFT <= 512 ? 16 : (NFFT <= 1024 ? 8 : (NFFT <= 4096 ? 2 : 1));
+  static constexpr int PW = (TF * NFP + 1) / 2 * 2;  // power-tile floats, even so what follows stays 8-byte aligned
+};
+
+// Shared memory: bufA, bufB [TF*M] float2 | power [TF*NFP] | tw_m [M] | tw_n [M+1]
+//                | window [NFFT] | fstart, fwidth [n_mels] | fw [n_mels*wmax] | keys
+template <int NFFT>
+size_t wave_smem_bytes(int n_mels, int wmax) {
+  using C = WaveCfg<NFFT>;
+  size_t b = 2 * sizeof(float2) * C::TF * C::M;
+  b += sizeof(float) * C::PW;
+  b += sizeof(float2) * (2 * C::M + 1);
+  b += sizeof(float) * NFFT;
+  b += sizeof(int) * 2 * n_mels + sizeof(float) * n_mels * wmax;
+  b += 16;
+  return (b + 15) / 16 * 16;
+}
+
+template <int NFFT>
+__global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a) {
+  using C = WaveCfg<NFFT>;
+  constexpr int M = C::M, TF = C::TF, NFP = C::NFP;
+  extern __shared__ __align__(16) unsigned char smem[];
+  float2 *bufA = reinterpret_cast<float2 *>(smem);
+  float2 *bufB = bufA + TF * M;
+  float *pw = reinterpret_cast<float *>(bufB + TF * M);
+  float2 *twm = reinterpret_cast<float2 *>(pw + C::PW);
+  float2 *twn = twm + M;
+  float *win = reinterpret_cast<float *>(twn + M + 1);
+  int *fstart = reinterpret_cast<int *>(win + NFFT);
+  int *fwidth = fstart + a.n_mels;
+  float *fw = reinterpret_cast<float *>(fwidth + a.n_mels);
+  uint32_t *blk_key = reinterpret_cast<uint32_t *>(fw + a.n_mels * a.wmax);
+
+  for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
+  for (int i = threadIdx.x; i <= M; i += blockDim.x) twn[i] = a.tw_n[i];
+  for (int i = threadIdx.x; i < NFFT; i += blockDim.x) win[i] = a.window[i];
+  for (int i = threadIdx.x; i < a.n_mels; i += blockDim.x) {
+    fstart[i] = a.fstart[i];
+    fwidth[i] = a.fwidth[i];
+  }
+  for (int i = threadIdx.x; i < a.n_mels * a.wmax; i += blockDim.x) fw[i] = a.fw[i];
+
+  const int64_t n_tiles = a.B * a.tiles_per_clip;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t b = tile / a.tiles_per_clip;
+    const int tloc = static_cast<int>(tile - b * a.tiles_per_clip);
+    const int64_t t0 = static_cast<int64_t>(tloc) * TF;
+    const int64_t left = a.n_frames - t0;
+    const int nf = left < TF ? static_cast<int>(left) : TF;
+    if (threadIdx.x == 0) *blk_key = 0u;
+    __syncthreads();  // tables loaded / previous tile finished with every buffer
+
+    // 1. framing, padding, window, pairing into complex points
+    const int64_t s_first = t0 * a.hop - a.pad_left;
+    const int64_t s_last = (t0 + nf - 1) * a.hop - a.pad_left + NFFT - 1;
+    const bool interior = s_first >= 0 && s_last < a.T;
+    for (int idx = threadIdx.x; idx < TF * M; idx += blockDim.x) {
+      const int f = idx / M;
+      const int n = idx - f * M;
+      float2 z = make_float2(0.f, 0.f);
+      if (f < nf) {
+        const int64_t s = (t0 + f) * a.hop - a.pad_left + 2 * n;
+        float x0, x1;
+        if (interior) {
+          x0 = load_sample(a, b, s);
+          x1 = load_sample(a, b, s + 1);
+        } else {
+          bool z0, z1;
+          const int64_t i0 = map_index(s, a.T, a.pad_mode, &z0);
+          const int64_t i1 = map_index(s + 1, a.T, a.pad_mode, &z1);
+          x0 = z0 ? 0.f : load_sample(a, b, i0);
+          x1 = z1 ? 0.f : load_sample(a, b, i1);
+        }
+        z = make_float2(x0 * win[2 * n], x1 * win[2 * n + 1]);
+      }
+      bufA[idx] = z;
+    }
+    __syncthreads();
+
+    // 2. N/2-point complex FFT of every frame
+    const bool in_b = fft::run<M>(bufA, bufB, twm, TF);
+    const float2 *Z = in_b ? bufB : bufA;
+
+    // 3. untangle the real spectrum and take |X|^power
+    for (int idx = threadIdx.x; idx < TF * (M + 1); idx += blockDim.x) {
+      const int f = idx / (M + 1);
+      const int k = idx - f * (M + 1);
+      const float2 A = Z[f * M + (k == M ? 0 : k)];
+      const float2 Bz = Z[f * M + (k == 0 ? 0 : M - k)];
+      const float2 Bc = make_float2(Bz.x, -Bz.y);
+      const float2 E = make_float2(0.5f * (A.x + Bc.x), 0.5f * (A.y + Bc.y));
+      // O = (A - Bc) / (2i) = -i (A - Bc) / 2
+      const float2 O = make_float2(0.5f * (A.y - Bc.y), -0.5f * (A.x - Bc.x));
+      const float2 X = fft::cadd(E, fft::cmul(twn[k], O));
+      float p = fmaf(X.x, X.x, X.y * X.y);
+      if (a.power_is_one) p = sqrtf(p);
+      pw[f * NFP + k] = p;
+    }
+    __syncthreads();
+
+    // 4. mel projection and store; lanes run over frames of one band
+    float lmax = -INFINITY;
+    for (int idx = threadIdx.x; idx < a.n_mels * TF; idx += blockDim.x) {
+      const int m = idx / TF;
+      const int f = idx - m * TF;
+      if (f < nf) {
+        const int st = fstart[m], wd = fwidth[m];
+        const float *w = fw + m * a.wmax;
+        const float *pr = pw + f * NFP + st;
+        float acc = 0.f;
+        for (int t = 0; t < wd; ++t) acc = fmaf(w[t], pr[t], acc);
+        const int64_t o = (b * a.n_mels + m) * a.n_frames + t0 + f;
+        if (a.log_mel) {
+          float l2;
+          asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(fmaxf(acc, 1e-10f)));
+          const float v = l2 * 0.30102999566398120f;  // log10(x) = log2(x) log10(2)
+          lmax = fmaxf(lmax, v);
+          static_cast<float *>(a.out)[o] = v;
+        } else if (a.out_f16) {
+          static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
+        } else {
+          static_cast<float *>(a.out)[o] = acc;
+        }
+      }
+    }
+    if (a.log_mel) {
+      const uint32_t key = __reduce_max_sync(0xffffffffu, float_to_ordered(lmax));
+      if ((threadIdx.x & 31) == 0) atomicMax(blk_key, key);
+      __syncthreads();
+      if (threadIdx.x == 0) a.tile_key[tile] = *blk_key;
+    }
+  }
+}
+
+using WaveKernel = void (*)(WaveArgs);
+
+template <int NFFT>
+void wave_entry(WaveKernel *k, size_t *smem, int *tf, int n_mels, int wmax) {
+  *k = wave_mel_kernel<NFFT>;
+  *smem = wave_smem_bytes<NFFT>(n_mels, wmax);
+  *tf = WaveCfg<NFFT>::TF;
+}
+
+bool pick_wave_kernel(int n_fft, int n_mels, int wmax, WaveKernel *k, size_t *smem, int *tf) {
+  switch (n_fft) {
+    case 64: wave_entry<64>(k, smem, tf, n_mels, wmax); return true;
+    case 128: wave_entry<128>(k, smem, tf, n_mels, wmax); return true;
+    case 256: wave_entry<256>(k, smem, tf, n_mels, wmax); return true;
+    case 400: wave_entry<400>(k, smem, tf, n_mels, wmax); return true;
+    case 512: wave_entry<512>(k, smem, tf, n_mels, wmax); return true;
+    case 1024: wave_entry<1024>(k, smem, tf, n_mels, wmax); return true;
+    case 2048: wave_entry<2048>(k, smem, tf, n_mels, wmax); return true;
+    case 4096: wave_entry<4096>(k, smem, tf, n_mels, wmax); return true;
+    default: return false;
+  }
+}
+
+bool supported_nfft(int n) {
+  if (n == 400) return true;
+  if (n < 64 || n > 4096) return false;
+  return (n & (n - 1)) == 0;
+}
+
+// ---- host-side tables, double precision ----
+
+double hz_to_mel(double hz, int scale) {
+  if (scale == LM_MEL_HTK) return 2595.0 * std::log10(1.0 + hz / 700.0);
+  // Slaney: 3 mels per 200 Hz up to 1 kHz (mel 15), then 27 mels per factor 6.4
+  if (hz < 1000.0) return 3.0 * hz / 200.0;
+  return 15.0 + 27.0 * std::log(hz / 1000.0) / std::log(6.4);
+}
+
+double mel_to_hz(double mel, int scale) {
+  if (scale == LM_MEL_HTK) return 700.0 * (std::pow(10.0, mel / 2595.0) - 1.0);
+  if (mel < 15.0) return 200.0 * mel / 3.0;
+  return 1000.0 * std::exp((mel - 15.0) * std::log(6.4) / 27.0);
+}
+
+struct HostTables {
+  std::vector<float> window;
+  std::vector<float2> tw_m, tw_n;
+  std::vector<int> fstart, fwidth;
+  std::vector<float> fw;
+  int wmax = 0;
+};
+
+void build_tables(const lm_mel_params &p, HostTables *t) {
+  const int N = p.n_fft, M = N / 2, n_freqs = N / 2 + 1;
+  const int wl = p.win_length > 0 ? p.win_length : N;
+  std::vector<double> w(N, 0.0);
+  const int left = (N - wl) / 2;
+  double energy = 0.0;
+  for (int j = 0; j < wl; ++j) {
+    const double v = 0.5 - 0.5 * std::cos(2.0 * M_PI * j / wl);  // periodic Hann of length wl
+    w[left + j] = v;
+    energy += v * v;
+  }
+  const double norm = p.normalized ? 1.0 / std::sqrt(energy) : 1.0;
+  t->window.resize(N);
+  for (int j = 0; j < N; ++j) t->window[j] = static_cast<float>(w[j] * norm);
+  t->tw_m.resize(M);
+  for (int i = 0; i < M; ++i) {
+    const double ang = -2.0 * M_PI * i / M;
+    t->tw_m[i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+  }
+  t->tw_n.resize(M + 1);
+  for (int k = 0; k <= M; ++k) {
+    const double ang = -2.0 * M_PI * k / N;
+    t->tw_n[k] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+  }
+  // triangles in Hz between n_mels + 2 points equally spaced in mel
+  const double f_max = p.f_max > 0.f ? p.f_max : p.sample_rate / 2.0;
+  const double m0 = hz_to_mel(p.f_min, p.mel_scale), m1 = hz_to_mel(f_max, p.mel_scale);
+  std::vector<double> edge(p.n_mels + 2);
+  for (int i = 0; i < p.n_mels + 2; ++i) edge[i] = mel_to_hz(m0 + (m1 - m0) * i / (p.n_mels + 1), p.mel_scale);
+  const double bin_hz = (p.sample_rate / 2.0) / (n_freqs - 1);
+  std::vector<std::vector<double>> rows(p.n_mels);
+  t->fstart.assign(p.n_mels, 0);
+  t->fwidth.assign(p.n_mels, 0);
+  for (int m = 0; m < p.n_mels; ++m) {
+    const double lo = edge[m], c = edge[m + 1], hi = edge[m + 2];
+    const double area = p.slaney_norm ? 2.0 / (hi - lo) : 1.0;
+    int first = -1, last = -1;
+    std::vector<double> row(n_freqs);
+    for (int k = 0; k < n_freqs; ++k) {
+      const double f = k * bin_hz;
+      const double rise = (f - lo) / (c - lo), fall = (hi - f) / (hi - c);
+      row[k] = std::max(0.0, std::min(rise, fall)) * area;
+      if (row[k] > 0.0) {
+        if (first < 0) first = k;
+        last = k;
+      }
+    }
+    if (first >= 0) {
+      t->fstart[m] = first;
+      t->fwidth[m] = last - first + 1;
+      rows[m].assign(row.begin() + first, row.begin() + last + 1);
+    }
+    t->wmax = std::max(t->wmax, t->fwidth[m]);
+  }
+  t->wmax = std::max(t->wmax, 1);
+  t->fw.assign(static_cast<size_t>(p.n_mels) * t->wmax, 0.f);
+  for (int m = 0; m < p.n_mels; ++m)
+    for (int j = 0; j < t->fwidth[m]; ++j) t->fw[static_cast<size_t>(m) * t->wmax + j] = static_cast<float>(rows[m][j]);
+}
+
+template <typename T>
+lm_status upload(const std::vector<T> &h, T **d) {
+  *d = nullptr;
+  if (h.empty()) return LM_OK;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void **>(d), h.size() * sizeof(T));
+  if (e == cudaErrorMemoryAllocation) {
+    (void)cudaGetLastError();
+    return LM_ERR_OUT_OF_MEMORY;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  LM_CUDA_TRY(cudaMemcpy(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return LM_OK;
+}
+
+void free_plan(lm_mel_plan *pl) {
+  if (!pl) return;
+  cudaFree(pl->window);
+  cudaFree(pl->tw_m);
+  cudaFree(pl->tw_n);
+  cudaFree(pl->fstart);
+  cudaFree(pl->fwidth);
+  cudaFree(pl->fw);
+  delete pl;
+}
+
+lm_status validate(const lm_mel_params &p) {
+  if (p.sample_rate <= 0 || p.hop_length <= 0 || p.n_mels <= 0 || p.n_fft <= 0) return LM_ERR_INVALID_ARG;
+  if (!(p.f_min >= 0.f) || (p.f_max > 0.f && !(p.f_max > p.f_min))) return LM_ERR_INVALID_ARG;
+  if (p.f_max <= 0.f && !(p.sample_rate / 2.0 > p.f_min)) return LM_ERR_INVALID_ARG;
+  if (p.win_length < 0 || p.win_length > p.n_fft || p.pad < 0) return LM_ERR_INVALID_ARG;
+  if (p.pad_mode < LM_PAD_REFLECT || p.pad_mode > LM_PAD_CIRCULAR) return LM_ERR_INVALID_ARG;
+  if (p.mel_scale != LM_MEL_HTK && p.mel_scale != LM_MEL_SLANEY) return LM_ERR_INVALID_ARG;
+  if (!supported_nfft(p.n_fft) || p.n_mels > 256) return LM_ERR_UNSUPPORTED;
+  if (p.power != 1.f && p.power != 2.f) return LM_ERR_UNSUPPORTED;
+  if (p.pad != 0) return LM_ERR_UNSUPPORTED;
+  return LM_OK;
+}
+
+int64_t frames_for(const lm_mel_params &p, int64_t T) {
+  const int64_t len = p.center ? T + 2 * (p.n_fft / 2) : T;
+  if (len < p.n_fft) return 0;
+  return 1 + (len - p.n_fft) / p.hop_length;
+}
+
+int tile_frames(int n_fft) {
+  WaveKernel k;
+  size_t smem;
+  int tf = 1;
+  pick_wave_kernel(n_fft, 1, 1, &k, &smem, &tf);
+  return tf;
+}
+
+}  // namespace
+}  // namespace lm
 
 extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan **plan) {
   if (!params || !plan) return LM_ERR_INVALID_ARG;
   *plan = nullptr;
-  return LM_ERR_UNSUPPORTED;
+  if (lm_status st = lm::validate(*params); st != LM_OK) return st;
+  lm::HostTables t;
+  lm::build_tables(*params, &t);
+  auto *pl = new lm_mel_plan{};
+  pl->p = *params;
+  pl->n_freqs = params->n_fft / 2 + 1;
+  pl->wmax = t.wmax;
+  if (cudaError_t e = cudaGetDevice(&pl->device); e != cudaSuccess) {
+    delete pl;
+    return lm::cuda_fail(e);
+  }
+  lm_status st = lm::upload(t.window, &pl->window);
+  if (st == LM_OK) st = lm::upload(t.tw_m, &pl->tw_m);
+  if (st == LM_OK) st = lm::upload(t.tw_n, &pl->tw_n);
+  if (st == LM_OK) st = lm::upload(t.fstart, &pl->fstart);
+  if (st == LM_OK) st = lm::upload(t.fwidth, &pl->fwidth);
+  if (st == LM_OK) st = lm::upload(t.fw, &pl->fw);
+  if (st != LM_OK) {
+    lm::free_plan(pl);
+    return st;
+  }
+  *plan = pl;
+  return LM_OK;
 }
-extern "C" lm_status lm_mel_plan_destroy(lm_mel_plan *plan) { return plan ? LM_ERR_UNSUPPORTED : LM_OK; }
+
+extern "C" lm_status lm_mel_plan_destroy(lm_mel_plan *plan) {
+  if (!plan) return LM_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(plan->device);
+  cudaDeviceSynchronize();
+  lm::free_plan(plan);
+  cudaSetDevice(prev);
+  return LM_OK;
+}
+
 extern "C" lm_status lm_mel_n_frames(const lm_mel_plan *plan, int64_t T, int64_t *n_frames) {
-  (void)T;
-  if (!plan || !n_frames) return LM_ERR_INVALID_ARG;
-  return LM_ERR_UNSUPPORTED;
+  if (!plan || !n_frames || T < 0) return LM_ERR_INVALID_ARG;
+  *n_frames = lm::frames_for(plan->p, T);
+  return LM_OK;
 }
-extern "C" lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, size_t *bytes) {
-  (void)B;
-  if (!plan || !bytes) return LM_ERR_INVALID_ARG;
-  return LM_ERR_UNSUPPORTED;
+
+extern "C" lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, int64_t T, size_t *bytes) {
+  if (!plan || !bytes || B < 0 || T < 0) return LM_ERR_INVALID_ARG;
+  const int64_t nfr = lm::frames_for(plan->p, T);
+  const int tf = lm::tile_frames(plan->p.n_fft);
+  const int64_t tpc = nfr > 0 ? (nfr + tf - 1) / tf : 0;
+  *bytes = (lm::kWorkspaceHeaderBytes + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + 255) / 256 * 256;
+  return LM_OK;
 }
+
 extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wave, int32_t in_dtype, int64_t B,
                                         int64_t T, void *out, int32_t out_dtype, void *workspace,
                                         size_t workspace_bytes, lm_stream_t stream) {
-  (void)wave; (void)in_dtype; (void)B; (void)T; (void)out; (void)out_dtype; (void)workspace;
-  (void)workspace_bytes; (void)stream;
-  if (!plan) return LM_ERR_INVALID_ARG;
-  return LM_ERR_UNSUPPORTED;
+  if (!plan || B < 0 || T < 0) return LM_ERR_INVALID_ARG;
+  if (in_dtype != LM_F32 && in_dtype != LM_I16) return LM_ERR_UNSUPPORTED;
+  if (out_dtype != LM_F32 && out_dtype != LM_F16) return LM_ERR_UNSUPPORTED;
+  if (plan->p.log_mel && out_dtype != LM_F32) return LM_ERR_UNSUPPORTED;
+  const lm_mel_params &p = plan->p;
+  const int64_t nfr = lm::frames_for(p, T);
+  if (B == 0) return LM_OK;
+  if (T < 1 || nfr < 1) return LM_ERR_INVALID_ARG;
+  if (p.center && p.pad_mode == LM_PAD_REFLECT && T <= p.n_fft / 2) return LM_ERR_INVALID_ARG;
+  if (!wave || !out || !workspace) return workspace ? LM_ERR_INVALID_ARG : LM_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(wave) & 3) || (reinterpret_cast<uintptr_t>(out) & 3) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 3))
+    return LM_ERR_MISALIGNED;
+  size_t need = 0;
+  lm_mel_workspace_size(plan, B, T, &need);
+  if (workspace_bytes < need) return LM_ERR_WORKSPACE;
+  int dev = 0;
+  LM_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != plan->device) return LM_ERR_INVALID_ARG;
+
+  lm::WaveKernel kern;
+  size_t smem = 0;
+  int tf = 1;
+  lm::pick_wave_kernel(p.n_fft, p.n_mels, plan->wmax, &kern, &smem, &tf);
+  lm::DeviceInfo di;
+  if (lm_status st = lm::current_device_info(&di); st != LM_OK) return st;
+  if (smem > static_cast<size_t>(di.max_smem_optin)) return LM_ERR_UNSUPPORTED;
+  if (lm_status st = lm::ensure_smem_attribute(reinterpret_cast<const void *>(kern), static_cast<int>(smem));
+      st != LM_OK)
+    return st;
+  int per_sm = 0;
+  LM_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, lm::kWaveThreads, smem));
+  if (per_sm < 1) return LM_ERR_UNSUPPORTED;
+
+  lm::WaveArgs a{};
+  a.wave = wave;
+  a.out = out;
+  a.tile_key = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + lm::kWorkspaceHeaderBytes);
+  a.B = B;
+  a.T = T;
+  a.n_frames = nfr;
+  a.in_i16 = in_dtype == LM_I16;
+  a.out_f16 = out_dtype == LM_F16;
+  a.log_mel = p.log_mel != 0;
+  a.power_is_one = p.power == 1.f;
+  a.hop = p.hop_length;
+  a.pad_left = p.center ? p.n_fft / 2 : 0;
+  a.pad_mode = p.pad_mode;
+  a.n_mels = p.n_mels;
+  a.wmax = plan->wmax;
+  a.TF = tf;
+  a.tiles_per_clip = static_cast<int32_t>((nfr + tf - 1) / tf);
+  a.window = plan->window;
+  a.tw_m = plan->tw_m;
+  a.tw_n = plan->tw_n;
+  a.fstart = plan->fstart;
+  a.fwidth = plan->fwidth;
+  a.fw = plan->fw;
+  const int64_t n_tiles = B * a.tiles_per_clip;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_tiles, static_cast<int64_t>(di.sm_count) * per_sm));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (a.log_mel) LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, need, s));
+  kern<<<grid, lm::kWaveThreads, smem, s>>>(a);
+  LM_CUDA_TRY(cudaGetLastError());
+  if (a.log_mel) {
+    if (lm_status st = lm::launch_clip_clamp(static_cast<float *>(out), a.tile_key, B, p.n_mels * nfr,
+                                             a.tiles_per_clip, s);
+        st != LM_OK)
+      return st;
+  }
+  return LM_OK;
 }

@@ -1,0 +1,129 @@
+"""GPU parity of the waveform -> mel spectrogram path against the CPU oracle.
+
+Gates: f32 output |gpu - oracle| <= 1e-4 + 1e-4 |oracle|; f16 output is
+compared with the oracle rounded to f16, |gpu - ref16| <= 2e-3 + 2e-3 |ref16|.
+Inputs come from workloads.py and are identical on both sides.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import __graft_entry__
+    __graft_entry__.build()
+    import log_mel_spectrogram_gb300
+    return log_mel_spectrogram_gb300
+
+
+def _gate(got, ref, tol):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    err = np.abs(got - ref)
+    bad = err > tol + tol * np.abs(ref)
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} outside tolerance; max err {err.max():.3g} at "
+                           f"{np.unravel_index(np.argmax(err), err.shape)}")
+
+
+def _run(lm, oracle_mod, wave, sample_rate, n_fft, hop, n_mels, f_min=0.0, f_max=None, center=True,
+         pad_mode="reflect", power=2.0, mel_scale="htk", norm=None, log_mel=False, out_dtype="f32"):
+    m = lm.MelSpectrogram(sample_rate=sample_rate, n_fft=n_fft, hop_length=hop, n_mels=n_mels, f_min=f_min,
+                          f_max=f_max, center=center, pad_mode=pad_mode, power=power, mel_scale=mel_scale,
+                          norm=norm, log_mel=log_mel,
+                          dtype=torch.float16 if out_dtype == "f16" else torch.float32)
+    got = m(wave.cuda())
+    torch.cuda.synchronize()
+    ref = oracle_mod.mel_spectrogram(wave.numpy(), sample_rate, n_fft, hop, n_mels, f_min=f_min, f_max=f_max,
+                                     center=center, pad_mode=pad_mode, power=power, mel_scale=mel_scale,
+                                     norm=norm, log_mel=log_mel, out_dtype=out_dtype)
+    m.close()
+    tol = 2e-3 if out_dtype == "f16" else 1e-4
+    _gate(got.float().cpu().numpy(), ref.astype(np.float64), tol)
+    return got
+
+
+def test_whisper_sines_small(lm, oracle_mod):
+    w = workloads.WAVE_WHISPER
+    x = workloads.wave_workload_inputs(w, B=2, T=16000 * 3)
+    _run(lm, oracle_mod, x, 16000, 400, 160, 128, f_max=8000.0, log_mel=True)
+    _run(lm, oracle_mod, x, 16000, 400, 160, 128, f_max=8000.0, log_mel=False)
+
+
+def test_pcm16_slaney_small(lm, oracle_mod):
+    w = workloads.WAVE_PCM16
+    x = workloads.wave_workload_inputs(w, B=3, T=22050)
+    _run(lm, oracle_mod, x, 22050, 1024, 256, 128, f_max=11025.0, mel_scale="slaney", out_dtype="f16")
+    _run(lm, oracle_mod, x, 22050, 1024, 256, 128, f_max=11025.0, mel_scale="slaney", out_dtype="f32")
+
+
+@pytest.mark.parametrize("n_fft", [64, 128, 256, 512, 2048, 4096])
+def test_power_of_two_sizes(lm, oracle_mod, n_fft):
+    x = workloads.wave_sines(2, max(4 * n_fft, 3000), 16000, seed=n_fft)
+    _run(lm, oracle_mod, x, 16000, n_fft, n_fft // 4, 40 if n_fft <= 128 else 80, f_max=8000.0)
+
+
+@pytest.mark.parametrize("pad_mode", ["reflect", "constant", "replicate", "circular"])
+def test_pad_modes(lm, oracle_mod, pad_mode):
+    x = workloads.wave_sines(2, 3333, 16000, seed=7)
+    _run(lm, oracle_mod, x, 16000, 400, 160, 64, f_max=8000.0, pad_mode=pad_mode)
+
+
+def test_center_false_power_one_norm_fmin(lm, oracle_mod):
+    x = workloads.wave_sines(3, 5000, 16000, seed=9)
+    _run(lm, oracle_mod, x, 16000, 400, 100, 80, f_min=60.0, f_max=7600.0, center=False, power=1.0)
+    _run(lm, oracle_mod, x, 16000, 512, 128, 96, mel_scale="slaney", norm="slaney")
+    _run(lm, oracle_mod, x, 16000, 256, 37, 256, f_max=8000.0)  # odd hop, 256 bands
+
+
+def test_short_and_ragged_signals(lm, oracle_mod):
+    # T just above n_fft / 2 (the least reflect padding allows): one or two frames
+    x = workloads.wave_sines(2, 201, 16000, seed=3)
+    _run(lm, oracle_mod, x, 16000, 400, 160, 40, f_max=8000.0)
+    x = workloads.wave_pcm16(1, 700, seed=4)
+    _run(lm, oracle_mod, x, 22050, 1024, 256, 64, mel_scale="slaney", log_mel=True)
+
+
+def test_silence_and_log_window(lm, oracle_mod):
+    x = workloads.wave_sines(3, 8000, 16000, seed=5)
+    x[1] = 0.0
+    x[2, 4000:] *= 1e-6
+    got = _run(lm, oracle_mod, x, 16000, 400, 160, 128, f_max=8000.0, log_mel=True).cpu()
+    assert torch.all(got[1] == -1.5)
+    mx = got.amax(dim=(1, 2))
+    assert torch.all(got.amin(dim=(1, 2)) >= mx - 2.0 - 1e-5)
+
+
+def test_whisper_full_size_sampled(lm, oracle_mod):
+    # 8 x 480000 f32, n_fft 400, hop 160, 128 HTK bands, log: the whole batch
+    # on the GPU, the oracle on two clips.
+    w = workloads.WAVE_WHISPER
+    x = workloads.wave_workload_inputs(w)
+    m = lm.MelSpectrogram(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, log_mel=True)
+    got = m(x.cuda())
+    torch.cuda.synchronize()
+    assert got.shape == (8, 128, 3001)
+    for b in (0, 7):
+        ref = oracle_mod.mel_spectrogram(x[b:b + 1].numpy(), 16000, 400, 160, 128, f_max=8000.0, log_mel=True)
+        _gate(got[b:b + 1].cpu().numpy(), ref, 1e-4)
+    m.close()
+
+
+def test_pcm16_full_size_sampled(lm, oracle_mod):
+    w = workloads.WAVE_PCM16
+    x = workloads.wave_workload_inputs(w)
+    m = lm.MelSpectrogram(sample_rate=22050, n_fft=1024, hop_length=256, n_mels=128, f_max=11025.0,
+                          mel_scale="slaney", dtype=torch.float16)
+    got = m(x.cuda())
+    torch.cuda.synchronize()
+    assert got.shape == (32, 128, 862) and got.dtype == torch.float16
+    for b in (0, 31):
+        ref = oracle_mod.mel_spectrogram(x[b:b + 1].numpy(), 22050, 1024, 256, 128, f_max=11025.0,
+                                         mel_scale="slaney", out_dtype="f16")
+        _gate(got[b:b + 1].float().cpu().numpy(), ref.astype(np.float64), 2e-3)
+    m.close()
