@@ -139,21 +139,104 @@ class ClockSampler:
 
 
 def cpu_baseline(stft_host, W_host, target_s: float = 12.0) -> dict:
-    """Times the oracle (as it stands) on a bounded sample of clips."""
+    """Times the oracle (as it stands) on a bounded sample: the given clips,
+    processed repeatedly until about target_s seconds of CPU work are done."""
     import oracle
     oracle.build()
     n_clips = stft_host.shape[0]
-    k = 2
+    done = 0
     t0 = time.perf_counter()
-    oracle.log_mel_from_stft(stft_host[:k], W_host)
-    dt = time.perf_counter() - t0
-    per_clip = dt / k
-    k2 = int(max(1, min(n_clips, target_s / max(per_clip, 1e-6))))
-    t0 = time.perf_counter()
-    oracle.log_mel_from_stft(stft_host[:k2], W_host)
-    dt2 = time.perf_counter() - t0
-    return {"value": k2 / dt2, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{k2} of {n_clips} clips ({dt2:.1f} s), dense double-precision oracle, OpenMP over clips"}
+    while True:
+        oracle.log_mel_from_stft(stft_host, W_host)
+        done += n_clips
+        dt = time.perf_counter() - t0
+        if dt >= target_s:
+            break
+    return {"value": done / dt, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} clips ({n_clips} distinct clips of the workload, repeated) in {dt:.1f} s, dense "
+                      "double-precision oracle, OpenMP over clips"}
+
+
+class StftJob:
+    """log_mel_from_stft on the B=256, F=3000, NF=201, NM=128 batch (or --batch B)."""
+
+    def __init__(self, lm, workloads, dev, batch):
+        import torch
+        w = workloads.WHISPER_STFT_B256
+        if batch and batch != w.B:
+            import dataclasses
+            w = dataclasses.replace(w, B=batch, name=w.name.replace(f"b{w.B}_", f"b{batch}_"))
+        self.lm, self.w, self.dev = lm, w, dev
+        self.stft, self.W = workloads.stft_workload_inputs(w, device=dev)
+        self.out = torch.empty((w.B, w.F, w.NM), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B, w.F, w.NF, w.NM), dtype=torch.uint8,
+                              device=dev)
+        self.info = lm.describe_log_mel_from_stft(w.B, w.F, w.NF, w.NM)
+        self.units = w.B
+        self.bytes = w.canonical_bytes
+        self.kernels = self.info["kernels"]
+        self.flush_l2 = False  # 1.63 GB per step, 12x the L2
+        self.inputs = [self.stft, self.W]
+
+    def step(self, inputs=None):
+        stft, W = inputs if inputs is not None else (self.stft, self.W)
+        self.lm.log_mel_from_stft(stft, W, out=self.out, workspace=self.ws)
+
+    def error(self):
+        return self.lm.workspace_error(self.ws)
+
+    def config(self):
+        w, info = self.w, self.info
+        return {"workload": w.name, "B": w.B, "F": w.F, "NF": w.NF, "NM": w.NM,
+                "canonical_bytes_per_step": w.canonical_bytes,
+                "l2": "no flush: each step streams 1.63 GB of inputs and outputs, 12x the 129 MB L2",
+                "variant": "resident" if info["resident"] else "twopass", "grid": info["grid"],
+                "frames_per_tile": info["frames_per_tile"], "stages": info["stages"], "lag": info["lag"]}
+
+    def kernel_note(self):
+        return ("stft_logmel_kernel (one cooperative launch per step, timed with the workspace memset that "
+                "precedes it)")
+
+    def cpu_sample(self):
+        return self.stft[: min(64, self.w.B)].cpu().numpy(), self.W.cpu().numpy()
+
+
+class WaveJob:
+    """mel_spectrogram on one of the two waveform workloads."""
+
+    def __init__(self, lm, workloads, dev, name):
+        import torch
+        w = {"wave_whisper": workloads.WAVE_WHISPER, "wave_pcm16": workloads.WAVE_PCM16}[name]
+        self.lm, self.w, self.dev = lm, w, dev
+        self.x = workloads.wave_workload_inputs(w, device=dev)
+        self.mel = lm.MelSpectrogram(sample_rate=w.sample_rate, n_fft=w.n_fft, hop_length=w.hop_length,
+                                     n_mels=w.n_mels, f_min=w.f_min, f_max=w.f_max, center=w.center,
+                                     pad_mode=w.pad_mode, power=w.power, mel_scale=w.mel_scale, norm=w.norm,
+                                     log_mel=w.log_mel,
+                                     dtype=torch.float16 if w.out_dtype == "f16" else torch.float32)
+        self.out = self.mel(self.x)
+        self.units = w.B
+        self.bytes = w.canonical_bytes
+        self.kernels = 2 if w.log_mel else 1
+        self.flush_l2 = True  # 14-28 MB per step fits in L2
+        self.inputs = [self.x]
+
+    def step(self, inputs=None):
+        x = inputs[0] if inputs is not None else self.x
+        self.mel(x, out=self.out)
+
+    def error(self):
+        return 0
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "B": w.B, "T": w.T, "sample_rate": w.sample_rate, "n_fft": w.n_fft,
+                "hop_length": w.hop_length, "n_mels": w.n_mels, "mel_scale": w.mel_scale, "in": w.in_dtype,
+                "out": w.out_dtype, "log_mel": w.log_mel, "canonical_bytes_per_step": w.canonical_bytes,
+                "l2": "flushed between timed steps by writing 512 MB (outside the per-step events)"}
+
+    def kernel_note(self):
+        return "wave_mel_kernel" + (" + logmel_clamp_kernel" if self.w.log_mel else "")
 
 
 def run_ours(args, world, rank, local):
@@ -178,20 +261,15 @@ def run_ours(args, world, rank, local):
     barrier()
     import log_mel_spectrogram_gb300 as lm
 
-    w = workloads.WHISPER_STFT_B256
-    if args.batch and args.batch != w.B:
-        import dataclasses
-        w = dataclasses.replace(w, B=args.batch, name=w.name.replace(f"b{w.B}_", f"b{args.batch}_"))
-    stft, W = workloads.stft_workload_inputs(w, device=dev)
-    out = torch.empty((w.B, w.F, w.NM), dtype=torch.float32, device=dev)
-    ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B, w.F, w.NF, w.NM), dtype=torch.uint8, device=dev)
-    info = lm.describe_log_mel_from_stft(w.B, w.F, w.NF, w.NM)
+    job = StftJob(lm, workloads, dev, args.batch) if args.workload == "stft" else WaveJob(lm, workloads, dev,
+                                                                                             args.workload)
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if job.flush_l2 else None
 
     for _ in range(args.warmup):
-        lm.log_mel_from_stft(stft, W, out=out, workspace=ws)
+        job.step()
     torch.cuda.synchronize(dev)
-    if lm.workspace_error(ws):
+    if job.error():
         raise RuntimeError("device error word set during warm-up")
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -205,16 +283,20 @@ def run_ours(args, world, rank, local):
         t_end = torch.cuda.Event(enable_timing=True)
         t_begin.record(stream)
         for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
             starts[i].record(stream)
-            lm.log_mel_from_stft(stft, W, out=out, workspace=ws)
+            job.step()
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         clk.mark(wall0, time.time())
         barrier()
-    total_ms = t_begin.elapsed_time(t_end)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if lm.workspace_error(ws):
+    # Steps run back to back unless an L2 flush separates them; then only the
+    # steps themselves are counted.
+    total_ms = sum(launch_ms) if flush is not None else t_begin.elapsed_time(t_end)
+    if job.error():
         raise RuntimeError("device error word set during the timed region")
 
     if world > 1:
@@ -223,28 +305,31 @@ def run_ours(args, world, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = world * w.B * args.steps / (total_ms / 1e3)
+    value = world * job.units * args.steps / (total_ms / 1e3)
 
     # end to end: pinned host input -> device -> library call -> host result
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 5))
     e2e_value = None
+    h2d = sum(t.numel() * t.element_size() for t in job.inputs)
+    d2h = job.out.numel() * job.out.element_size()
     if e2e_steps:
-        stft_h = torch.empty(stft.shape, dtype=stft.dtype, pin_memory=True)
-        stft_h.copy_(stft)
-        W_h = W.cpu().pin_memory()
-        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        d_stft = torch.empty_like(stft)
-        d_W = torch.empty_like(W)
+        host_in = []
+        for t in job.inputs:
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            host_in.append(h)
+        dev_in = [torch.empty_like(t) for t in job.inputs]
+        out_h = torch.empty(job.out.shape, dtype=job.out.dtype, pin_memory=True)
         torch.cuda.synchronize(dev)
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            d_stft.copy_(stft_h, non_blocking=True)
-            d_W.copy_(W_h, non_blocking=True)
-            lm.log_mel_from_stft(d_stft, d_W, out=out, workspace=ws)
-            out_h.copy_(out, non_blocking=True)
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            job.step(dev_in)
+            out_h.copy_(job.out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -254,15 +339,17 @@ def run_ours(args, world, rank, local):
             t = torch.tensor([e2e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        e2e_value = world * w.B * e2e_steps / (e2e_ms / 1e3)
-        del d_stft, stft_h, out_h
+        e2e_value = world * job.units * e2e_steps / (e2e_ms / 1e3)
+        del host_in, dev_in, out_h
 
     peak, peak_kind = _peaks()
     mean_launch_s = statistics.mean(launch_ms) / 1e3
-    achieved = w.canonical_bytes / mean_launch_s / 1e9
-    trec = _traffic_record()
+    achieved = job.bytes / mean_launch_s / 1e9
+    trec = _traffic_record() if args.workload == "stft" and not args.batch else None
+    config = job.config()
+    config["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     result = {
-        "metric": METRIC,
+        "metric": METRIC if args.workload == "stft" else f"{job.w.name} clips/sec",
         "value": value,
         "unit": "clips/s",
         "n_gpus": world,
@@ -273,30 +360,22 @@ def run_ours(args, world, rank, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic (seeded speech-tilted Gaussian complex64 STFT, linspace triangular filters)",
+        "data": "synthetic (seeded, generated on the device; see workloads.py)",
         "achieved_hbm_gbs": achieved,
-        "config": {"workload": w.name, "B": w.B, "F": w.F, "NF": w.NF, "NM": w.NM,
-                   "canonical_bytes_per_step": w.canonical_bytes,
-                   "l2": "no flush: each step streams 1.63 GB of inputs and outputs, 12x the 129 MB L2",
-                   "variant": "resident" if info["resident"] else "twopass", "grid": info["grid"],
-                   "frames_per_tile": info["frames_per_tile"], "stages": info["stages"], "lag": info["lag"],
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": (trec["dram_bytes_per_launch"] if trec else None),
                      "traffic_source": ("profiles/traffic.json" if trec else "stale or missing"),
-                     "kernel": "stft_logmel_kernel (one cooperative launch per step, timed with the "
-                               "workspace memset that precedes it)",
+                     "kernel": job.kernel_note(),
                      "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)},
         "e2e": {"value": e2e_value, "unit": "clips/s", "steps": e2e_steps,
-                "h2d_bytes_per_step": stft.numel() * 8 + W.numel() * 4,
-                "d2h_bytes_per_step": out.numel() * 4},
-        "gpu_launches": args.steps * info["kernels"],
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * job.kernels,
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = stft[: min(64, w.B)].cpu().numpy()
-        result["cpu_baseline"] = cpu_baseline(sample, W.cpu().numpy())
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "stft":
+        result["cpu_baseline"] = cpu_baseline(*job.cpu_sample())
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -344,6 +423,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs on smaller cases)")
+    ap.add_argument("--workload", choices=["stft", "wave_whisper", "wave_pcm16"], default="stft",
+                    help="stft (default, the headline) or one of the waveform workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
