@@ -122,7 +122,7 @@ __device__ __forceinline__ void pass(const float2 *__restrict__ in, float2 *__re
 // Radix of the pass that follows span P: 5 while M/P has a factor 5, then 8
 // while possible, then the leftover 4 or 2.
 template <int M, int P>
-constexpr int next_radix() {
+__host__ __device__ constexpr int next_radix() {
   return ((M / P) % 5 == 0) ? 5 : ((M / P) % 8 == 0) ? 8 : ((M / P) % 4 == 0) ? 4 : 2;
 }
 

@@ -112,6 +112,15 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
   return v;
 }
 
+__device__ __forceinline__ uint4 ld_relaxed_gpu_v4(const uint32_t *p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

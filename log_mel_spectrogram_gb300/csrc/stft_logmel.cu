@@ -52,8 +52,9 @@
 namespace lm {
 namespace {
 
-constexpr int kLag = 8;          // resident mode: steps a tile's log values wait in shared memory
-constexpr int kSlots = 32;       // ring of per-step handshake slots (> kLag + 1)
+constexpr int kLag = 12;         // resident mode: steps a tile's log values wait in shared memory
+constexpr int kResolveWindow = 4;  // steps whose clip maxima the resolver reads per round
+constexpr int kSlots = 32;       // ring of per-step handshake slots (> kLag + kResolveWindow)
 constexpr int kMaxStages = 8;
 constexpr int kRegTaps = 8;      // filter taps held in registers per band
 constexpr int kMaxBands = 512;
@@ -353,58 +354,98 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
   }
 
   if (warp == kResolverWarp) {
-    // ---- resolver: clip maximum once every tile of the clip is published ----
-    // For the first step q of a new clip it waits until this CTA has
-    // published step q + span (the last step the clip can reach here), then
-    // reads the clip's contiguous slots in warp-wide passes until none is
-    // zero.  Steps of an already resolved clip are answered at once.  The
-    // wait also keeps the resolver less than kSlots steps ahead of the
-    // consumers, so no handshake slot is reused before it was read.
+    // ---- resolver: clip maxima for kResolveWindow steps per round ----
+    // A round serves steps q0 .. q0+W-1 once this CTA has published the last
+    // of them (which also keeps the resolver less than kSlots steps ahead of
+    // the consumers, so no handshake slot is reused before it was read).
+    // The whole warp reads each step's clip slots with 16-byte loads -- the
+    // loads of all W clips are in flight together -- and a step is handed to
+    // the consumers as soon as none of its clip's slots is zero.
     if (!kResident) return;
-    TileIter res;
-    res.init(blockIdx.x, a.tiles_per_clip);
-    int64_t cached_b = -1;
-    float cached_hi = 0.f;
-    for (int64_t q = 0; q < my_tiles; ++q) {
-      if (res.b != cached_b) {
-        const int64_t target = min(q + a.span, my_tiles - 1);
-        mbar_wait(&aux.pub_bar[target & (kSlots - 1)], static_cast<uint32_t>((target / kSlots) & 1), abort_flag,
-                  a.err);
-        const uint32_t *slots = a.tile_key + res.b * a.tiles_per_clip;
-        uint32_t m = 0;
-        uint64_t t0 = 0;
-        for (;;) {
-          bool ok = true;
-          m = 0;
-#pragma unroll 4
-          for (int i = lane; i < a.tiles_per_clip; i += 32) {
-            const uint32_t v = ld_relaxed_gpu(slots + i);
-            ok = ok && (v != 0u);
-            m = max(m, v);
-          }
-          if (__all_sync(0xffffffffu, ok)) break;
-          int stop = 0;
-          if (lane == 0) {
-            const uint64_t now = global_timer_ns();
-            if (t0 == 0) t0 = now;
-            if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
-              *abort_flag = 1;
-              atomicOr(a.err, kErrClipTimeout);
-            }
-            stop = *abort_flag;
-          }
-          if (__shfl_sync(0xffffffffu, stop, 0)) break;
-          __nanosleep(256);
-        }
-        cached_b = res.b;
-        cached_hi = ordered_to_float(__reduce_max_sync(0xffffffffu, m));
+    constexpr int W = kResolveWindow;
+    TileIter it;
+    it.init(blockIdx.x, a.tiles_per_clip);
+    const int tpc = a.tiles_per_clip;
+    for (int64_t q0 = 0; q0 < my_tiles; q0 += W) {
+      const int64_t last = min(q0 + W - 1, my_tiles - 1);
+      mbar_wait(&aux.pub_bar[last & (kSlots - 1)], static_cast<uint32_t>((last / kSlots) & 1), abort_flag, a.err);
+      const uint32_t *base[W];
+      int head[W];
+      unsigned pending = 0;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const uint32_t *slots = a.tile_key + it.b * tpc;
+        head[w] = static_cast<int>((reinterpret_cast<uintptr_t>(slots) & 15) >> 2);  // slots before the clip's first
+        base[w] = slots - head[w];                                                   // 16-byte aligned
+        if (q0 + w < my_tiles) pending |= 1u << w;
+        it.next(a);
       }
-      if (lane == 0) {
-        aux.hi_val[q & (kSlots - 1)] = cached_hi;
-        mbar_arrive(&aux.hi_bar[q & (kSlots - 1)]);
+      uint64_t t0 = 0;
+      while (pending) {
+        uint32_t m[W];
+        bool ok[W];
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          m[w] = 0;
+          ok[w] = true;
+          if (pending & (1u << w)) {
+            const int nvec = (head[w] + tpc + 3) >> 2;
+            for (int v = lane; v < nvec; v += 32) {
+              const uint4 x = ld_relaxed_gpu_v4(base[w] + 4 * v);
+              const uint32_t e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int slot = 4 * v + j - head[w];
+                if (slot >= 0 && slot < tpc) {
+                  ok[w] = ok[w] && (e[j] != 0u);
+                  m[w] = max(m[w], e[j]);
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          if (pending & (1u << w)) {
+            const bool all = __all_sync(0xffffffffu, ok[w]);
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, m[w]);
+            if (all) {
+              const int64_t q = q0 + w;
+              if (lane == 0) {
+                aux.hi_val[q & (kSlots - 1)] = ordered_to_float(mx);
+                mbar_arrive(&aux.hi_bar[q & (kSlots - 1)]);
+              }
+              pending &= ~(1u << w);
+            }
+          }
+        }
+        if (!pending) break;
+        int stop = 0;
+        if (lane == 0) {
+          const uint64_t now = global_timer_ns();
+          if (t0 == 0) t0 = now;
+          if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            atomicOr(a.err, kErrClipTimeout);
+          }
+          stop = *abort_flag;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) {
+          // give up: hand over whatever was read so the consumers can drain
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            if ((pending & (1u << w)) && lane == 0) {
+              const int64_t q = q0 + w;
+              aux.hi_val[q & (kSlots - 1)] = 0.f;
+              mbar_arrive(&aux.hi_bar[q & (kSlots - 1)]);
+            }
+          }
+          pending = 0;
+          break;
+        }
+        __nanosleep(64);
       }
       __syncwarp();
-      res.next(a);
     }
     return;
   }
@@ -585,7 +626,10 @@ lm_status plan_launch(int64_t B, int64_t F, int32_t NF, int32_t NM, StftLaunch *
   const char *variant = env_or("LOGMEL_K1_VARIANT", "auto");
   const bool force_two = std::strcmp(variant, "twopass") == 0;
   const bool force_res = std::strcmp(variant, "resident") == 0;
-  ln->resident = !force_two && ln->span < kLag;
+  // The resolver serves step q once this CTA published step q + W - 1, so
+  // resident mode needs every tile of that clip by step q + kLag - 1:
+  // span + W - 1 <= kLag - 1.
+  ln->resident = !force_two && ln->span + kResolveWindow <= kLag;
   if (ln->resident) {
     ln->tp = plan_tiles(NF, NM, dev.max_smem_optin, true);
     if (ln->tp.S < 2) ln->resident = false;  // the output ring does not fit beside two stages
@@ -615,7 +659,9 @@ size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM) {
   tile_height(NF, NM, &CW, &FG, &FPT);
   const int64_t TF = static_cast<int64_t>(FG) * FPT;
   const int64_t tpc = (F + TF - 1) / TF;
-  return (tile_key_offset() + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + 255) / 256 * 256;
+  // + 16: the resolver reads slots in aligned 16-byte groups and may touch
+  // up to three slots past the last clip.
+  return (tile_key_offset() + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + 16 + 255) / 256 * 256;
 }
 
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
