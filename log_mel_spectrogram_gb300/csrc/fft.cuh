@@ -126,6 +126,17 @@ __host__ __device__ constexpr int next_radix() {
   return ((M / P) % 5 == 0) ? 5 : ((M / P) % 8 == 0) ? 8 : ((M / P) % 4 == 0) ? 4 : 2;
 }
 
+// Number of passes for an M-point transform (the result ends in the second
+// buffer when it is odd).
+template <int M, int P = 1>
+__host__ __device__ constexpr int num_passes() {
+  if constexpr (P == M) {
+    return 0;
+  } else {
+    return 1 + num_passes<M, P * next_radix<M, P>()>();
+  }
+}
+
 // Runs every pass, ping-ponging between a and b.  Returns true when the
 // result ends in b.
 template <int M, int P = 1>

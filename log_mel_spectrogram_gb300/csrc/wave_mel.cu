@@ -63,6 +63,11 @@ struct WaveArgs {
   int32_t in_i16, out_f16, log_mel, power_is_one;
   int32_t hop, pad_left, pad_mode;
   int32_t n_mels, wmax, tiles_per_clip, TF;
+  uint32_t *err;           // device error word (workspace header)
+  uint64_t total_bytes;    // B * T * sample size
+  uint32_t seg_offset;     // shared-memory offset of the two sample-span buffers
+  uint32_t seg_bytes;      // bytes per span buffer (multiple of 128)
+  int32_t use_seg;         // 1: stage interior tiles' samples with bulk copies
   const float *window;
   const float2 *tw_m;
   const float2 *tw_n;
@@ -94,21 +99,23 @@ struct WaveCfg {
   static constexpr int NFP = NF | 1;  // odd power-tile row stride
   // frames per tile: enough work for 256 threads, bounded by shared memory
   static constexpr int TF = NFFT <= 512 ? 16 : (NFFT <= 1024 ? 8 : (NFFT <= 4096 ? 2 : 1));
-  static constexpr int PW = (TF * NFP + 1) / 2 * 2;  // power-tile floats, even so what follows stays 8-byte aligned
+  // The power tile (TF rows of NFP floats) lives in whichever FFT buffer does
+  // not hold the transform's result; it needs at most half of it.
+  static constexpr bool kResultInB = fft::num_passes<M>() % 2 == 1;
+  static_assert(TF * NFP * sizeof(float) <= TF * M * sizeof(float2), "power tile must fit an FFT buffer");
 };
 
-// Shared memory: bufA, bufB [TF*M] float2 | power [TF*NFP] | tw_m [M] | tw_n [M+1]
+// Shared memory: bufA, bufB [TF*M] float2 (the power tile reuses one) | tw_m [M] | tw_n [M+1]
 //                | window [NFFT] | fstart, fwidth [n_mels] | fw [n_mels*wmax] | keys
 template <int NFFT>
 size_t wave_smem_bytes(int n_mels, int wmax) {
   using C = WaveCfg<NFFT>;
   size_t b = 2 * sizeof(float2) * C::TF * C::M;
-  b += sizeof(float) * C::PW;
   b += sizeof(float2) * (2 * C::M + 1);
   b += sizeof(float) * NFFT;
   b += sizeof(int) * 2 * n_mels + sizeof(float) * n_mels * wmax;
-  b += 16;
-  return (b + 15) / 16 * 16;
+  b += 16;  // tile key and abort flag
+  return (b + 127) / 128 * 128;  // the sample-span buffers follow, 128-byte aligned
 }
 
 template <int NFFT>
@@ -118,14 +125,56 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   extern __shared__ __align__(16) unsigned char smem[];
   float2 *bufA = reinterpret_cast<float2 *>(smem);
   float2 *bufB = bufA + TF * M;
-  float *pw = reinterpret_cast<float *>(bufB + TF * M);
-  float2 *twm = reinterpret_cast<float2 *>(pw + C::PW);
+  float *pw = reinterpret_cast<float *>(C::kResultInB ? bufA : bufB);
+  float2 *twm = bufB + TF * M;
   float2 *twn = twm + M;
   float *win = reinterpret_cast<float *>(twn + M + 1);
   int *fstart = reinterpret_cast<int *>(win + NFFT);
   int *fwidth = fstart + a.n_mels;
   float *fw = reinterpret_cast<float *>(fwidth + a.n_mels);
   uint32_t *blk_key = reinterpret_cast<uint32_t *>(fw + a.n_mels * a.wmax);
+  int *abort_flag_p = reinterpret_cast<int *>(blk_key + 1);
+  volatile int *abort_flag = abort_flag_p;
+  unsigned char *seg = smem + a.seg_offset;  // two buffers of seg_bytes
+  uint64_t *seg_bar = reinterpret_cast<uint64_t *>(seg + 2 * static_cast<size_t>(a.seg_bytes));
+  const int es = a.in_i16 ? 2 : 4;
+
+  // The contiguous samples an interior tile (no padding in play) reads:
+  // bulk-copy range [a0, a0 + bytes) of the waveform, 16-byte aligned.
+  auto span_of = [&](int64_t tile, uint64_t *a0, uint32_t *bytes) -> bool {
+    if (!a.use_seg) return false;
+    const int64_t b = tile / a.tiles_per_clip;
+    const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(TF);
+    const int64_t left = a.n_frames - t0;
+    const int nf = left < TF ? static_cast<int>(left) : TF;
+    const int64_t s_first = t0 * a.hop - a.pad_left;
+    const int64_t s_last = (t0 + nf - 1) * a.hop - a.pad_left + NFFT - 1;
+    if (s_first < 0 || s_last >= a.T) return false;
+    const uint64_t start = static_cast<uint64_t>(b * a.T + s_first) * es;
+    const uint64_t end = static_cast<uint64_t>(b * a.T + s_last + 1) * es;
+    *a0 = start & ~15ull;
+    const uint64_t a1 = (end + 15ull) & ~15ull;
+    if (a1 > a.total_bytes) return false;
+    *bytes = static_cast<uint32_t>(a1 - *a0);
+    return true;
+  };
+  auto issue_span = [&](int64_t tile, int buf) {
+    uint64_t a0;
+    uint32_t bytes;
+    if (span_of(tile, &a0, &bytes)) {
+      mbar_arrive_expect_tx(&seg_bar[buf], bytes);
+      bulk_g2s(seg + buf * static_cast<size_t>(a.seg_bytes), static_cast<const char *>(a.wave) + a0, bytes,
+               &seg_bar[buf], policy_evict_first());
+    }
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&seg_bar[0], 1);
+    mbar_init(&seg_bar[1], 1);
+    *abort_flag_p = 0;
+    fence_mbar_init();
+    if (blockIdx.x < a.B * a.tiles_per_clip) issue_span(blockIdx.x, 0);
+  }
+  uint32_t fill0 = 0u, fill1 = 0u;  // completed span copies per buffer (the same in every thread)
 
   for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
   for (int i = threadIdx.x; i <= M; i += blockDim.x) twn[i] = a.tw_n[i];
@@ -137,7 +186,9 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   for (int i = threadIdx.x; i < a.n_mels * a.wmax; i += blockDim.x) fw[i] = a.fw[i];
 
   const int64_t n_tiles = a.B * a.tiles_per_clip;
-  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+  int it = 0;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    const int buf = it & 1;
     const int64_t b = tile / a.tiles_per_clip;
     const int tloc = static_cast<int>(tile - b * a.tiles_per_clip);
     const int64_t t0 = static_cast<int64_t>(tloc) * TF;
@@ -145,11 +196,25 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
     const int nf = left < TF ? static_cast<int>(left) : TF;
     if (threadIdx.x == 0) *blk_key = 0u;
     __syncthreads();  // tables loaded / previous tile finished with every buffer
+    // Prefetch the next tile's samples into the other span buffer; the
+    // previous tile's framing, its last reader, finished before the barrier.
+    if (threadIdx.x == 0 && tile + gridDim.x < n_tiles) issue_span(tile + gridDim.x, buf ^ 1);
+    uint64_t span_a0;
+    uint32_t span_bytes;
+    const bool staged = span_of(tile, &span_a0, &span_bytes);
+    if (staged) {
+      mbar_wait(&seg_bar[buf], (buf ? fill1 : fill0) & 1u, abort_flag, a.err);
+      if (buf) ++fill1; else ++fill0;
+    }
 
     // 1. framing, padding, window, pairing into complex points
     const int64_t s_first = t0 * a.hop - a.pad_left;
     const int64_t s_last = (t0 + nf - 1) * a.hop - a.pad_left + NFFT - 1;
     const bool interior = s_first >= 0 && s_last < a.T;
+    // staged: sample s of the clip is element (s - s_first) + head of the span buffer
+    const int64_t head = staged ? (static_cast<int64_t>(b * a.T + s_first) * es - static_cast<int64_t>(span_a0)) / es : 0;
+    const float *segf = reinterpret_cast<const float *>(seg + buf * static_cast<size_t>(a.seg_bytes));
+    const int16_t *segh = reinterpret_cast<const int16_t *>(segf);
     for (int idx = threadIdx.x; idx < TF * M; idx += blockDim.x) {
       const int f = idx / M;
       const int n = idx - f * M;
@@ -157,7 +222,16 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
       if (f < nf) {
         const int64_t s = (t0 + f) * a.hop - a.pad_left + 2 * n;
         float x0, x1;
-        if (interior) {
+        if (staged) {
+          const int e = static_cast<int>(head) + f * a.hop + 2 * n;
+          if (a.in_i16) {
+            x0 = static_cast<float>(segh[e]) * (1.0f / 32768.0f);
+            x1 = static_cast<float>(segh[e + 1]) * (1.0f / 32768.0f);
+          } else {
+            x0 = segf[e];
+            x1 = segf[e + 1];
+          }
+        } else if (interior) {
           x0 = load_sample(a, b, s);
           x1 = load_sample(a, b, s + 1);
         } else {
@@ -175,7 +249,7 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
 
     // 2. N/2-point complex FFT of every frame
     const bool in_b = fft::run<M>(bufA, bufB, twm, TF);
-    const float2 *Z = in_b ? bufB : bufA;
+    const float2 *Z = in_b ? bufB : bufA;  // == kResultInB; pw is the other buffer
 
     // 3. untangle the real spectrum and take |X|^power
     for (int idx = threadIdx.x; idx < TF * (M + 1); idx += blockDim.x) {
@@ -476,8 +550,21 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   size_t smem = 0;
   int tf = 1;
   lm::pick_wave_kernel(p.n_fft, p.n_mels, plan->wmax, &kern, &smem, &tf);
+  // Two buffers for the contiguous samples of one tile of frames (plus 32
+  // bytes of alignment slack), then two mbarriers.
+  const int esize = in_dtype == LM_I16 ? 2 : 4;
+  const size_t seg_bytes =
+      (static_cast<size_t>((tf - 1) * static_cast<int64_t>(p.hop_length) + p.n_fft) * esize + 32 + 127) / 128 * 128;
+  const size_t seg_offset = smem;
   lm::DeviceInfo di;
   if (lm_status st = lm::current_device_info(&di); st != LM_OK) return st;
+  bool use_seg = (reinterpret_cast<uintptr_t>(wave) & 15) == 0 &&
+                 seg_offset + 2 * seg_bytes + 16 <= static_cast<size_t>(di.max_smem_optin);
+  // Without staging (unaligned input, or a hop so long the spans do not fit)
+  // every tile gathers its samples from global memory; the two mbarriers are
+  // still reserved, right after the tables, since every CTA initialises them.
+  const size_t seg_used = use_seg ? seg_bytes : 0;
+  smem = seg_offset + 2 * seg_used + 16;
   if (smem > static_cast<size_t>(di.max_smem_optin)) return LM_ERR_UNSUPPORTED;
   if (lm_status st = lm::ensure_smem_attribute(reinterpret_cast<const void *>(kern), static_cast<int>(smem));
       st != LM_OK)
@@ -510,10 +597,16 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   a.fstart = plan->fstart;
   a.fwidth = plan->fwidth;
   a.fw = plan->fw;
+  a.err = static_cast<uint32_t *>(workspace);
+  a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(T) * esize;
+  a.seg_offset = static_cast<uint32_t>(seg_offset);
+  a.seg_bytes = static_cast<uint32_t>(seg_used);
+  a.use_seg = use_seg;
   const int64_t n_tiles = B * a.tiles_per_clip;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_tiles, static_cast<int64_t>(di.sm_count) * per_sm));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (a.log_mel) LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, need, s));
+  // Clears the device error word (and, for log plans, the tile slots).
+  LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, a.log_mel ? need : lm::kWorkspaceHeaderBytes, s));
   kern<<<grid, lm::kWaveThreads, smem, s>>>(a);
   LM_CUDA_TRY(cudaGetLastError());
   if (a.log_mel) {

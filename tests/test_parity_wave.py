@@ -127,3 +127,21 @@ def test_pcm16_full_size_sampled(lm, oracle_mod):
                                          mel_scale="slaney", out_dtype="f16")
         _gate(got[b:b + 1].float().cpu().numpy(), ref.astype(np.float64), 2e-3)
     m.close()
+
+
+def test_unaligned_input_and_long_hop_fallbacks(lm, oracle_mod):
+    # A waveform view starting 4 bytes past a 16-byte boundary cannot be bulk
+    # copied, and a hop this long makes a tile's sample span too big for shared
+    # memory: both take the per-sample path and must agree with the oracle.
+    base = workloads.wave_sines(1, 24001, 16000, seed=12)
+    x = base[0, 1:].reshape(2, 12000)  # contiguous, but the storage offset is one float
+    got_ref = _run(lm, oracle_mod, x.contiguous(), 16000, 400, 160, 64, f_max=8000.0)
+    m = lm.MelSpectrogram(sample_rate=16000, n_fft=400, hop_length=160, n_mels=64, f_max=8000.0)
+    xs = base.cuda()[0, 1:24001].view(2, 12000)
+    assert xs.data_ptr() % 16 == 4
+    got = m(xs)
+    torch.cuda.synchronize()
+    assert torch.equal(got.cpu(), got_ref.cpu())
+    m.close()
+    y = workloads.wave_sines(2, 40000, 16000, seed=13)
+    _run(lm, oracle_mod, y, 16000, 400, 3000, 64, f_max=8000.0)
