@@ -196,7 +196,7 @@ typedef struct lm_mel_params {
   int32_t n_mels;      /* 1..256 */
   float f_min;         /* Hz, >= 0 */
   float f_max;         /* Hz, > f_min; <= 0 means sample_rate / 2 */
-  int32_t pad;         /* extra zero padding on both sides before framing; only 0 so far */
+  int32_t pad;         /* zeros added on both sides before centre padding, >= 0 */
   int32_t center;      /* 1: pad n_fft/2 on both sides with pad_mode */
   int32_t pad_mode;    /* lm_pad_mode */
   float power;         /* 1 (magnitude) or 2 (power) */

@@ -61,7 +61,8 @@ struct WaveArgs {
   uint32_t *tile_key;
   int64_t B, T, n_frames;
   int32_t in_i16, out_f16, log_mel, power_is_one;
-  int32_t hop, pad_left, pad_mode;
+  int32_t hop, pad_left, pad_mode;  // pad_left: centre padding plus the zero `pad`, in samples
+  int32_t pad_zero;                 // zeros added on both sides before centre padding
   int32_t n_mels, wmax, tiles_per_clip, TF;
   uint32_t *err;           // device error word (workspace header)
   uint64_t total_bytes;    // B * T * sample size
@@ -235,11 +236,14 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
           x0 = load_sample(a, b, s);
           x1 = load_sample(a, b, s + 1);
         } else {
+          // Centre padding applies to the signal already extended by pad_zero
+          // zeros on both sides (length T + 2 pad_zero); map there, then back.
+          const int64_t Tz = a.T + 2 * a.pad_zero;
           bool z0, z1;
-          const int64_t i0 = map_index(s, a.T, a.pad_mode, &z0);
-          const int64_t i1 = map_index(s + 1, a.T, a.pad_mode, &z1);
-          x0 = z0 ? 0.f : load_sample(a, b, i0);
-          x1 = z1 ? 0.f : load_sample(a, b, i1);
+          const int64_t i0 = map_index(s + a.pad_zero, Tz, a.pad_mode, &z0) - a.pad_zero;
+          const int64_t i1 = map_index(s + 1 + a.pad_zero, Tz, a.pad_mode, &z1) - a.pad_zero;
+          x0 = (z0 || i0 < 0 || i0 >= a.T) ? 0.f : load_sample(a, b, i0);
+          x1 = (z1 || i1 < 0 || i1 >= a.T) ? 0.f : load_sample(a, b, i1);
         }
         z = make_float2(x0 * win[2 * n], x1 * win[2 * n + 1]);
       }
@@ -448,12 +452,12 @@ lm_status validate(const lm_mel_params &p) {
   if (p.mel_scale != LM_MEL_HTK && p.mel_scale != LM_MEL_SLANEY) return LM_ERR_INVALID_ARG;
   if (!supported_nfft(p.n_fft) || p.n_mels > 256) return LM_ERR_UNSUPPORTED;
   if (p.power != 1.f && p.power != 2.f) return LM_ERR_UNSUPPORTED;
-  if (p.pad != 0) return LM_ERR_UNSUPPORTED;
   return LM_OK;
 }
 
 int64_t frames_for(const lm_mel_params &p, int64_t T) {
-  const int64_t len = p.center ? T + 2 * (p.n_fft / 2) : T;
+  const int64_t Tz = T + 2 * static_cast<int64_t>(p.pad);
+  const int64_t len = p.center ? Tz + 2 * (p.n_fft / 2) : Tz;
   if (len < p.n_fft) return 0;
   return 1 + (len - p.n_fft) / p.hop_length;
 }
@@ -534,7 +538,8 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   const int64_t nfr = lm::frames_for(p, T);
   if (B == 0) return LM_OK;
   if (T < 1 || nfr < 1) return LM_ERR_INVALID_ARG;
-  if (p.center && p.pad_mode == LM_PAD_REFLECT && T <= p.n_fft / 2) return LM_ERR_INVALID_ARG;
+  if (p.center && p.pad_mode == LM_PAD_REFLECT && T + 2 * static_cast<int64_t>(p.pad) <= p.n_fft / 2)
+    return LM_ERR_INVALID_ARG;
   if (!wave || !out || !workspace) return workspace ? LM_ERR_INVALID_ARG : LM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(wave) & 3) || (reinterpret_cast<uintptr_t>(out) & 3) ||
       (reinterpret_cast<uintptr_t>(workspace) & 3))
@@ -585,7 +590,8 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   a.log_mel = p.log_mel != 0;
   a.power_is_one = p.power == 1.f;
   a.hop = p.hop_length;
-  a.pad_left = p.center ? p.n_fft / 2 : 0;
+  a.pad_left = (p.center ? p.n_fft / 2 : 0) + p.pad;
+  a.pad_zero = p.pad;
   a.pad_mode = p.pad_mode;
   a.n_mels = p.n_mels;
   a.wmax = plan->wmax;

@@ -70,6 +70,11 @@ def lib() -> ctypes.CDLL:
             L.oracle_mel_spectrogram.argtypes = [vp, i32, i64, i64, i64, i64, i64, i64, dbl, dbl,
                                                  i32, i32, dbl, i32, i32, i32, i32, vp]
             L.oracle_mel_spectrogram.restype = i32
+            L.oracle_power_spectrogram_ex.argtypes = [vp, i64, i64, i64, i64, i64, i32, i32, i32, dbl, vp]
+            L.oracle_power_spectrogram_ex.restype = i32
+            L.oracle_mel_spectrogram_ex.argtypes = [vp, i32, i64, i64, i64, i64, i64, i64, i64, i64, dbl, dbl,
+                                                    i32, i32, i32, dbl, i32, i32, i32, i32, vp]
+            L.oracle_mel_spectrogram_ex.restype = i32
             _lib = L
     return _lib
 
@@ -142,14 +147,20 @@ def n_frames(T: int, n_fft: int, hop: int, center: bool = True) -> int:
 
 
 def power_spectrogram(x: np.ndarray, n_fft: int, hop: int, center: bool = True,
-                      pad_mode: str = "reflect", power: float = 2.0) -> np.ndarray:
+                      pad_mode: str = "reflect", power: float = 2.0, win_length: int | None = None,
+                      pad: int = 0, normalized: bool = False) -> np.ndarray:
     """[n_frames, n_fft/2+1] float64 power spectrogram of one signal."""
     x = np.ascontiguousarray(x, dtype=np.float64)
-    nfr = n_frames(x.shape[0], n_fft, hop, center)
+    nfr = n_frames(x.shape[0] + 2 * pad, n_fft, hop, center)
     spec = np.empty((nfr, n_fft // 2 + 1), dtype=np.float64)
-    _check(lib().oracle_power_spectrogram(_ptr(x), x.shape[0], n_fft, hop, int(center),
-                                          PAD_MODES[pad_mode], float(power), _ptr(spec)),
-           "power_spectrogram")
+    if win_length is None and pad == 0 and not normalized:
+        rc = lib().oracle_power_spectrogram(_ptr(x), x.shape[0], n_fft, hop, int(center), PAD_MODES[pad_mode],
+                                            float(power), _ptr(spec))
+    else:
+        rc = lib().oracle_power_spectrogram_ex(_ptr(x), x.shape[0], n_fft, int(win_length or 0), hop, int(pad),
+                                               int(center), PAD_MODES[pad_mode], int(normalized), float(power),
+                                               _ptr(spec))
+    _check(rc, "power_spectrogram")
     return spec
 
 
@@ -161,7 +172,8 @@ def mel_spectrogram(wave: np.ndarray, sample_rate: int, n_fft: int, hop_length: 
                     f_min: float = 0.0, f_max: float | None = None, center: bool = True,
                     pad_mode: str = "reflect", power: float = 2.0, mel_scale: str = "htk",
                     norm: str | None = None, log_mel: bool = False,
-                    out_dtype: str = "f32") -> np.ndarray:
+                    out_dtype: str = "f32", win_length: int | None = None, pad: int = 0,
+                    normalized: bool = False) -> np.ndarray:
     """wave [B,T] f32 or i16 -> [B, n_mels, n_frames] f32 or f16."""
     wave = np.ascontiguousarray(wave)
     if wave.dtype == np.int16:
@@ -172,18 +184,25 @@ def mel_spectrogram(wave: np.ndarray, sample_rate: int, n_fft: int, hop_length: 
     B, T = wave.shape
     if f_max is None:
         f_max = sample_rate / 2.0
-    nfr = n_frames(T, n_fft, hop_length, center)
+    nfr = n_frames(T + 2 * pad, n_fft, hop_length, center)
     if out_dtype == "f16":
         out = np.empty((B, n_mels, nfr), dtype=np.uint16)
         out_code = 2
     else:
         out = np.empty((B, n_mels, nfr), dtype=np.float32)
         out_code = 0
-    _check(lib().oracle_mel_spectrogram(_ptr(wave), in_code, B, T, sample_rate, n_fft, hop_length,
-                                        n_mels, float(f_min), float(f_max), int(center),
-                                        PAD_MODES[pad_mode], float(power), MEL_SCALES[mel_scale],
-                                        int(norm == "slaney"), int(log_mel), out_code, _ptr(out)),
-           "mel_spectrogram")
+    if win_length is None and pad == 0 and not normalized:
+        rc = lib().oracle_mel_spectrogram(_ptr(wave), in_code, B, T, sample_rate, n_fft, hop_length, n_mels,
+                                          float(f_min), float(f_max), int(center), PAD_MODES[pad_mode],
+                                          float(power), MEL_SCALES[mel_scale], int(norm == "slaney"),
+                                          int(log_mel), out_code, _ptr(out))
+    else:
+        rc = lib().oracle_mel_spectrogram_ex(_ptr(wave), in_code, B, T, sample_rate, n_fft, int(win_length or 0),
+                                             hop_length, int(pad), n_mels, float(f_min), float(f_max),
+                                             int(center), PAD_MODES[pad_mode], int(normalized), float(power),
+                                             MEL_SCALES[mel_scale], int(norm == "slaney"), int(log_mel),
+                                             out_code, _ptr(out))
+    _check(rc, "mel_spectrogram")
     if out_dtype == "f16":
         return out.view(np.float16)
     return out

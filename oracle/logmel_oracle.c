@@ -273,25 +273,47 @@ static int pad_signal(const double *x, int64_t T, int64_t p, int mode, double *o
   return ORACLE_OK;
 }
 
-/* Power spectrogram of one signal: spec[n_frames][n_fft/2 + 1] in double,
- * |X_k|^power with X_k = sum_j x_pad[t*hop + j] w[j] exp(-2 pi i j k / n_fft),
- * summed directly (O(n_fft^2) per frame). */
-int oracle_power_spectrogram(const double *x, int64_t T, int64_t n_fft, int64_t hop, int center,
-                             int pad_mode, double power, double *spec) {
-  if (!x || !spec || n_fft < 1 || hop < 1 || T < 1) return ORACLE_BAD_ARG;
+/* Power spectrogram of one signal with the full torchaudio Spectrogram
+ * argument set: spec[n_frames][n_fft/2 + 1] in double.
+ *   1. pad > 0: `pad` zeros are added on both sides first;
+ *   2. center: n_fft/2 more samples on both sides, filled per pad_mode;
+ *   3. the window is a periodic Hann of length win_length (0 = n_fft),
+ *      centred in n_fft samples with zeros around it;
+ *   4. X_k = sum_j x_pad[t*hop + j] w[j] exp(-2 pi i j k / n_fft), summed
+ *      directly (O(n_fft^2) per frame);
+ *   5. normalized: X is divided by sqrt(sum_j w[j]^2);
+ *   6. spec = |X_k|^power. */
+int oracle_power_spectrogram_ex(const double *x, int64_t T, int64_t n_fft, int64_t win_length, int64_t hop,
+                                int64_t pad, int center, int pad_mode, int normalized, double power,
+                                double *spec) {
+  if (!x || !spec || n_fft < 1 || hop < 1 || T < 1 || pad < 0) return ORACLE_BAD_ARG;
+  int64_t wl = win_length > 0 ? win_length : n_fft;
+  if (wl > n_fft) return ORACLE_BAD_ARG;
+  int64_t T1 = T + 2 * pad;
   int64_t p = center ? n_fft / 2 : 0;
-  int64_t n_frames = oracle_n_frames(T, n_fft, hop, center);
+  int64_t n_frames = oracle_n_frames(T1, n_fft, hop, center);
   if (n_frames < 1) return ORACLE_BAD_ARG;
   int64_t n_freqs = n_fft / 2 + 1;
-  double *xp = (double *)malloc(sizeof(double) * (size_t)(T + 2 * p));
-  double *w = (double *)malloc(sizeof(double) * (size_t)n_fft);
+  double *x1 = (double *)calloc((size_t)T1, sizeof(double));
+  double *xp = (double *)malloc(sizeof(double) * (size_t)(T1 + 2 * p));
+  double *w = (double *)calloc((size_t)n_fft, sizeof(double));
   double *cs = (double *)malloc(sizeof(double) * (size_t)n_fft);
   double *sn = (double *)malloc(sizeof(double) * (size_t)n_fft);
   double *fr = (double *)malloc(sizeof(double) * (size_t)n_fft);
-  int err = (xp && w && cs && sn && fr) ? ORACLE_OK : ORACLE_NO_MEM;
-  if (err == ORACLE_OK) err = pad_signal(x, T, p, pad_mode, xp);
+  int err = (x1 && xp && w && cs && sn && fr) ? ORACLE_OK : ORACLE_NO_MEM;
   if (err == ORACLE_OK) {
-    oracle_hann_window(n_fft, w);
+    memcpy(x1 + pad, x, sizeof(double) * (size_t)T);
+    err = pad_signal(x1, T1, p, pad_mode, xp);
+  }
+  if (err == ORACLE_OK) {
+    int64_t left = (n_fft - wl) / 2;
+    oracle_hann_window(wl, w + left);
+    double scale = 1.0;
+    if (normalized) {
+      double e = 0.0;
+      for (int64_t j = 0; j < n_fft; ++j) e += w[j] * w[j];
+      scale = 1.0 / sqrt(e);
+    }
     for (int64_t m = 0; m < n_fft; ++m) { /* e^{-2 pi i m / n_fft} for m = (j k) mod n_fft */
       double ang = 2.0 * M_PI * (double)m / (double)n_fft;
       cs[m] = cos(ang);
@@ -306,17 +328,26 @@ int oracle_power_spectrogram(const double *x, int64_t T, int64_t n_fft, int64_t 
           re += fr[j] * cs[m];
           im -= fr[j] * sn[m];
         }
+        re *= scale;
+        im *= scale;
         double p2 = re * re + im * im;
         spec[t * n_freqs + k] = (power == 2.0) ? p2 : pow(sqrt(p2), power);
       }
     }
   }
+  free(x1);
   free(xp);
   free(w);
   free(cs);
   free(sn);
   free(fr);
   return err;
+}
+
+/* The common case: window of n_fft samples, no extra padding, no normalisation. */
+int oracle_power_spectrogram(const double *x, int64_t T, int64_t n_fft, int64_t hop, int center,
+                             int pad_mode, double power, double *spec) {
+  return oracle_power_spectrogram_ex(x, T, n_fft, 0, hop, 0, center, pad_mode, 0, power, spec);
 }
 
 /* Round a double to IEEE binary16, nearest-even, directly (no trip through
@@ -350,16 +381,16 @@ uint16_t oracle_f64_to_f16(double v) {
 /* out[B][n_mels][n_frames] as f32 or f16 (raw bits).  log_mel = 1 applies the
  * log10 floor / per-clip clamp / rescale of the KBench spec over the whole
  * (n_mels, n_frames) plane of each clip. */
-int oracle_mel_spectrogram(const void *wave, int in_dtype, int64_t B, int64_t T,
-                           int64_t sample_rate, int64_t n_fft, int64_t hop, int64_t n_mels,
-                           double f_min, double f_max, int center, int pad_mode, double power,
-                           int mel_scale, int slaney_norm, int log_mel, int out_dtype,
-                           void *out) {
-  if (!wave || !out || B < 1 || T < 1 || n_fft < 2 || hop < 1 || n_mels < 1) return ORACLE_BAD_ARG;
+int oracle_mel_spectrogram_ex(const void *wave, int in_dtype, int64_t B, int64_t T,
+                              int64_t sample_rate, int64_t n_fft, int64_t win_length, int64_t hop,
+                              int64_t pad, int64_t n_mels, double f_min, double f_max, int center,
+                              int pad_mode, int normalized, double power, int mel_scale,
+                              int slaney_norm, int log_mel, int out_dtype, void *out) {
+  if (!wave || !out || B < 1 || T < 1 || n_fft < 2 || hop < 1 || n_mels < 1 || pad < 0) return ORACLE_BAD_ARG;
   int64_t n_freqs = n_fft / 2 + 1;
-  int64_t n_frames = oracle_n_frames(T, n_fft, hop, center);
+  int64_t n_frames = oracle_n_frames(T + 2 * pad, n_fft, hop, center);
   if (n_frames < 1) return ORACLE_BAD_ARG;
-  if (center && pad_mode == ORACLE_PAD_REFLECT && n_fft / 2 >= T) return ORACLE_BAD_ARG;
+  if (center && pad_mode == ORACLE_PAD_REFLECT && n_fft / 2 >= T + 2 * pad) return ORACLE_BAD_ARG;
   double *fb = (double *)malloc(sizeof(double) * (size_t)(n_mels * n_freqs));
   if (!fb) return ORACLE_NO_MEM;
   int err = oracle_mel_filterbank(n_freqs, f_min, f_max, n_mels, (double)sample_rate, mel_scale,
@@ -381,7 +412,8 @@ int oracle_mel_spectrogram(const void *wave, int in_dtype, int64_t B, int64_t T,
         else
           x[i] = (double)((const float *)wave)[b * T + i];
       }
-      e = oracle_power_spectrogram(x, T, n_fft, hop, center, pad_mode, power, spec);
+      e = oracle_power_spectrogram_ex(x, T, n_fft, win_length, hop, pad, center, pad_mode, normalized, power,
+                                      spec);
     }
     if (e == ORACLE_OK) {
       double hi = -INFINITY;
@@ -416,4 +448,14 @@ int oracle_mel_spectrogram(const void *wave, int in_dtype, int64_t B, int64_t T,
   }
   free(fb);
   return err;
+}
+
+/* The common case: window of n_fft samples, no extra padding, no normalisation. */
+int oracle_mel_spectrogram(const void *wave, int in_dtype, int64_t B, int64_t T,
+                           int64_t sample_rate, int64_t n_fft, int64_t hop, int64_t n_mels,
+                           double f_min, double f_max, int center, int pad_mode, double power,
+                           int mel_scale, int slaney_norm, int log_mel, int out_dtype,
+                           void *out) {
+  return oracle_mel_spectrogram_ex(wave, in_dtype, B, T, sample_rate, n_fft, 0, hop, 0, n_mels, f_min, f_max,
+                                   center, pad_mode, 0, power, mel_scale, slaney_norm, log_mel, out_dtype, out);
 }

@@ -243,3 +243,33 @@ def test_f16_output_is_rounded_f32_path(oracle_mod):
     # most one f16 ulp; values this far from the range limits stay finite.
     assert np.all(np.isfinite(a.astype(np.float32)))
     np.testing.assert_allclose(a.astype(np.float64), b.astype(np.float64), rtol=2 ** -10, atol=0)
+
+
+@pytest.mark.parametrize("win_length,pad,normalized,center,pad_mode",
+                         [(300, 0, False, True, "reflect"), (400, 37, False, True, "reflect"),
+                          (400, 0, True, True, "constant"), (256, 11, True, False, "reflect"),
+                          (333, 5, True, True, "replicate")])
+def test_power_spectrogram_full_argument_set(oracle_mod, win_length, pad, normalized, center, pad_mode):
+    # torchaudio's Spectrogram: zero `pad` first, then torch.stft with a periodic
+    # Hann of win_length centred in n_fft, and for normalized=True ("window")
+    # a division of X by sqrt(sum w^2).  torch.stft in float64 is the reference.
+    rng = np.random.default_rng(win_length + pad)
+    n_fft, hop, T = 400, 128, 2100
+    x = rng.standard_normal(T)
+    spec = oracle_mod.power_spectrogram(x, n_fft, hop, center=center, pad_mode=pad_mode, win_length=win_length,
+                                        pad=pad, normalized=normalized)
+    xt = torch.nn.functional.pad(torch.from_numpy(x)[None], (pad, pad), mode="constant")[0]
+    win = torch.hann_window(win_length, periodic=True, dtype=torch.float64)
+    X = torch.stft(xt, n_fft, hop_length=hop, win_length=win_length, window=win, center=center,
+                   pad_mode=pad_mode, return_complex=True, onesided=True)
+    if normalized:
+        X = X / win.pow(2).sum().sqrt()
+    ref = (X.abs() ** 2).T.numpy()
+    assert spec.shape == ref.shape
+    np.testing.assert_allclose(spec, ref, rtol=1e-9, atol=1e-9)
+
+
+def test_pad_changes_frame_count(oracle_mod):
+    x = workloads.wave_sines(1, 1000, 16000, 2).numpy()
+    out = oracle_mod.mel_spectrogram(x, 16000, 400, 160, 40, pad=80)
+    assert out.shape == (1, 40, 1 + (1000 + 160) // 160)

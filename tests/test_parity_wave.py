@@ -32,16 +32,18 @@ def _gate(got, ref, tol):
 
 
 def _run(lm, oracle_mod, wave, sample_rate, n_fft, hop, n_mels, f_min=0.0, f_max=None, center=True,
-         pad_mode="reflect", power=2.0, mel_scale="htk", norm=None, log_mel=False, out_dtype="f32"):
+         pad_mode="reflect", power=2.0, mel_scale="htk", norm=None, log_mel=False, out_dtype="f32",
+         win_length=None, pad=0, normalized=False):
     m = lm.MelSpectrogram(sample_rate=sample_rate, n_fft=n_fft, hop_length=hop, n_mels=n_mels, f_min=f_min,
                           f_max=f_max, center=center, pad_mode=pad_mode, power=power, mel_scale=mel_scale,
-                          norm=norm, log_mel=log_mel,
+                          norm=norm, log_mel=log_mel, win_length=win_length, pad=pad, normalized=normalized,
                           dtype=torch.float16 if out_dtype == "f16" else torch.float32)
     got = m(wave.cuda())
     torch.cuda.synchronize()
     ref = oracle_mod.mel_spectrogram(wave.numpy(), sample_rate, n_fft, hop, n_mels, f_min=f_min, f_max=f_max,
                                      center=center, pad_mode=pad_mode, power=power, mel_scale=mel_scale,
-                                     norm=norm, log_mel=log_mel, out_dtype=out_dtype)
+                                     norm=norm, log_mel=log_mel, out_dtype=out_dtype, win_length=win_length,
+                                     pad=pad, normalized=normalized)
     m.close()
     tol = 2e-3 if out_dtype == "f16" else 1e-4
     _gate(got.float().cpu().numpy(), ref.astype(np.float64), tol)
@@ -145,3 +147,19 @@ def test_unaligned_input_and_long_hop_fallbacks(lm, oracle_mod):
     m.close()
     y = workloads.wave_sines(2, 40000, 16000, seed=13)
     _run(lm, oracle_mod, y, 16000, 400, 3000, 64, f_max=8000.0)
+
+
+@pytest.mark.parametrize("win_length,pad,normalized,center,pad_mode,n_fft",
+                         [(300, 0, False, True, "reflect", 400), (400, 37, False, True, "reflect", 400),
+                          (400, 0, True, True, "constant", 400), (256, 11, True, False, "reflect", 512),
+                          (333, 5, True, True, "replicate", 400), (1024, 300, False, True, "circular", 1024),
+                          (700, 64, True, True, "reflect", 1024)])
+def test_full_torchaudio_argument_set(lm, oracle_mod, win_length, pad, normalized, center, pad_mode, n_fft):
+    # win_length < n_fft (window centred with zeros around it), `pad` zeros
+    # before centre padding, the "window" normalisation, every pad mode.
+    x = workloads.wave_sines(2, 6000, 16000, seed=win_length + pad)
+    _run(lm, oracle_mod, x, 16000, n_fft, n_fft // 4, 64, f_max=8000.0, center=center, pad_mode=pad_mode,
+         win_length=win_length, pad=pad, normalized=normalized)
+    p = workloads.wave_pcm16(1, 4000, seed=pad)
+    _run(lm, oracle_mod, p, 16000, n_fft, n_fft // 4, 48, mel_scale="slaney", norm="slaney", out_dtype="f16",
+         win_length=win_length, pad=pad, normalized=normalized, center=center, pad_mode=pad_mode)
