@@ -21,7 +21,8 @@ from . import _native
 from ._native import LogmelError
 
 __all__ = ["log_mel_from_stft", "log_mel_from_stft_workspace_size", "workspace_error", "LogmelError",
-           "describe_log_mel_from_stft", "MelSpectrogram", "mel_spectrogram", "library_path"]
+           "describe_log_mel_from_stft", "MelSpectrogram", "mel_spectrogram", "library_path",
+           "log_mel_from_stft_op", "mel_spectrogram_op"]
 
 
 def library_path():
@@ -32,6 +33,13 @@ def _stream_handle(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream)
+
+
+def _no_grad_inputs(*tensors: torch.Tensor) -> None:
+    """Inference only: a tensor that requires grad under grad mode is refused."""
+    if torch.is_grad_enabled() and any(t.requires_grad for t in tensors):
+        raise RuntimeError("log_mel_spectrogram_gb300 ops are inference-only: inputs must not require grad "
+                           "(use torch.no_grad() or detach())")
 
 
 def _require_cuda(t: torch.Tensor, name: str) -> None:
@@ -52,6 +60,7 @@ def log_mel_from_stft_workspace_size(B: int, F: int, NF: int, NM: int) -> int:
 def log_mel_from_stft(stft: torch.Tensor, mel_filters: torch.Tensor, out: torch.Tensor | None = None,
                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """stft [B,F,NF] complex64, mel_filters [NM,NF] float32 -> [B,F,NM] float32."""
+    _no_grad_inputs(stft, mel_filters)
     _require_cuda(stft, "stft")
     _require_cuda(mel_filters, "mel_filters")
     if stft.dtype != torch.complex64 or stft.dim() != 3:
@@ -138,6 +147,7 @@ class MelSpectrogram:
 
     def __call__(self, wave: torch.Tensor, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                  stream=None) -> torch.Tensor:
+        _no_grad_inputs(wave)
         _require_cuda(wave, "wave")
         if wave.dtype == torch.int16:
             in_code = _native.DTYPES["i16"]
@@ -191,3 +201,68 @@ def mel_spectrogram(wave: torch.Tensor, **kwargs) -> torch.Tensor:
         return out
     finally:
         m.close()
+
+
+# ---------------------------------------------------------------------------
+# torch integration: custom ops with shape-only fake implementations, so that
+# torch.compile(fullgraph=True) traces through the library calls.  Inference
+# only: a tensor that requires grad under grad mode is rejected.
+# ---------------------------------------------------------------------------
+
+@torch.library.custom_op("logmel_gb300::log_mel_from_stft", mutates_args=())
+def log_mel_from_stft_op(stft: torch.Tensor, mel_filters: torch.Tensor) -> torch.Tensor:
+    """Custom-op form of log_mel_from_stft (same arguments and result)."""
+    _no_grad_inputs(stft, mel_filters)
+    return log_mel_from_stft(stft.contiguous(), mel_filters.contiguous())
+
+
+@log_mel_from_stft_op.register_fake
+def _(stft, mel_filters):
+    return stft.new_empty((stft.shape[0], stft.shape[1], mel_filters.shape[0]), dtype=torch.float32)
+
+
+_OP_PLANS: dict = {}
+
+
+def _op_frames(T: int, n_fft: int, hop: int, pad: int, center: bool) -> int:
+    length = T + 2 * pad + (2 * (n_fft // 2) if center else 0)
+    return 0 if length < n_fft else 1 + (length - n_fft) // hop
+
+
+@torch.library.custom_op("logmel_gb300::mel_spectrogram", mutates_args=())
+def mel_spectrogram_op(wave: torch.Tensor, sample_rate: int, n_fft: int, win_length: int, hop_length: int,
+                       f_min: float, f_max: float, pad: int, n_mels: int, power: float, normalized: bool,
+                       center: bool, pad_mode: str, norm: str, mel_scale: str, log_mel: bool,
+                       half: bool) -> torch.Tensor:
+    """Custom-op form of MelSpectrogram(...)(wave); plans are cached per argument set."""
+    _no_grad_inputs(wave)
+    key = (sample_rate, n_fft, win_length, hop_length, f_min, f_max, pad, n_mels, power, normalized, center,
+           pad_mode, norm, mel_scale, log_mel, half)
+    m = _OP_PLANS.get(key)
+    if m is None:
+        m = _OP_PLANS[key] = MelSpectrogram(
+            sample_rate=sample_rate, n_fft=n_fft, win_length=win_length or None, hop_length=hop_length,
+            f_min=f_min, f_max=f_max if f_max > 0 else None, pad=pad, n_mels=n_mels, power=power,
+            normalized=normalized, center=center, pad_mode=pad_mode, norm=norm or None, mel_scale=mel_scale,
+            log_mel=log_mel, dtype=torch.float16 if half else torch.float32)
+    return m(wave.contiguous())
+
+
+@mel_spectrogram_op.register_fake
+def _(wave, sample_rate, n_fft, win_length, hop_length, f_min, f_max, pad, n_mels, power, normalized, center,
+      pad_mode, norm, mel_scale, log_mel, half):
+    nfr = _op_frames(wave.shape[-1], n_fft, hop_length, pad, center)
+    return wave.new_empty((*wave.shape[:-1], n_mels, nfr), dtype=torch.float16 if half else torch.float32)
+
+
+def _refuse_backward(ctx, inputs, output):
+    raise RuntimeError("log_mel_spectrogram_gb300 ops are inference-only: inputs must not require grad "
+                       "(use torch.no_grad() or detach())")
+
+
+def _no_backward(ctx, grad):
+    raise RuntimeError("log_mel_spectrogram_gb300 ops have no backward")
+
+
+log_mel_from_stft_op.register_autograd(_no_backward, setup_context=_refuse_backward)
+mel_spectrogram_op.register_autograd(_no_backward, setup_context=_refuse_backward)
