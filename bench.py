@@ -32,6 +32,7 @@ if str(ROOT) not in sys.path:
     sys.path.insert(0, str(ROOT))
 
 METRIC = "log-mel clips/sec and achieved HBM GB/s vs GB300 peak (B=256 Whisper STFT)"
+L2_BYTES = 129 * 2 ** 20  # GB300 L2
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -175,7 +176,9 @@ class StftJob:
         self.units = w.B
         self.bytes = w.canonical_bytes
         self.kernels = self.info["kernels"]
-        self.flush_l2 = False  # 1.63 GB per step, 12x the L2
+        # The headline batch streams 1.63 GB per step, 12x the L2; smaller
+        # batches that could sit in L2 are flushed between steps.
+        self.flush_l2 = w.canonical_bytes < 4 * L2_BYTES
         self.inputs = [self.stft, self.W]
 
     def step(self, inputs=None):
@@ -189,7 +192,8 @@ class StftJob:
         w, info = self.w, self.info
         return {"workload": w.name, "B": w.B, "F": w.F, "NF": w.NF, "NM": w.NM,
                 "canonical_bytes_per_step": w.canonical_bytes,
-                "l2": "no flush: each step streams 1.63 GB of inputs and outputs, 12x the 129 MB L2",
+                "l2": ("flushed between timed steps by writing 512 MB (outside the per-step events)" if self.flush_l2
+                       else f"no flush: each step streams {w.canonical_bytes / 1e9:.2f} GB, more than 4x the L2"),
                 "variant": "resident" if info["resident"] else "twopass", "grid": info["grid"],
                 "frames_per_tile": info["frames_per_tile"], "stages": info["stages"], "lag": info["lag"]}
 
@@ -204,9 +208,12 @@ class StftJob:
 class WaveJob:
     """mel_spectrogram on one of the two waveform workloads."""
 
-    def __init__(self, lm, workloads, dev, name):
+    def __init__(self, lm, workloads, dev, name, batch=0):
         import torch
         w = {"wave_whisper": workloads.WAVE_WHISPER, "wave_pcm16": workloads.WAVE_PCM16}[name]
+        if batch and batch != w.B:
+            import dataclasses
+            w = dataclasses.replace(w, B=batch, name=w.name.replace(f"_b{w.B}_", f"_b{batch}_"))
         self.lm, self.w, self.dev = lm, w, dev
         self.x = workloads.wave_workload_inputs(w, device=dev)
         self.mel = lm.MelSpectrogram(sample_rate=w.sample_rate, n_fft=w.n_fft, hop_length=w.hop_length,
@@ -262,7 +269,7 @@ def run_ours(args, world, rank, local):
     import log_mel_spectrogram_gb300 as lm
 
     job = StftJob(lm, workloads, dev, args.batch) if args.workload == "stft" else WaveJob(lm, workloads, dev,
-                                                                                             args.workload)
+                                                                                             args.workload, args.batch)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if job.flush_l2 else None
 
@@ -271,6 +278,16 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if job.error():
         raise RuntimeError("device error word set during warm-up")
+    run_step = job.step
+    if args.graph:
+        # One step captured once and replayed: the same kernels, without the
+        # per-call host work (argument checks, plan lookup, launch calls).
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            job.step()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        run_step = graph.replay
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -286,7 +303,7 @@ def run_ours(args, world, rank, local):
             if flush is not None:
                 flush.fill_(i & 0xFF)
             starts[i].record(stream)
-            job.step()
+            run_step()
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
@@ -298,6 +315,17 @@ def run_ours(args, world, rank, local):
     total_ms = sum(launch_ms) if flush is not None else t_begin.elapsed_time(t_end)
     if job.error():
         raise RuntimeError("device error word set during the timed region")
+
+    # Host-observed latency of one call: wall clock from the call to the end
+    # of a synchronize, with the inputs warm in L2.  Reported beside the
+    # device-timed throughput; it is what a B=1 caller waits for.
+    lat = []
+    for _ in range(min(args.steps, 200)):
+        h0 = time.perf_counter()
+        run_step()
+        torch.cuda.synchronize(dev)
+        lat.append((time.perf_counter() - h0) * 1e3)
+    lat.sort()
 
     if world > 1:
         import torch.distributed as dist
@@ -348,6 +376,7 @@ def run_ours(args, world, rank, local):
     trec = _traffic_record() if args.workload == "stft" and not args.batch else None
     config = job.config()
     config["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    config["launch"] = "cuda graph replay" if args.graph else "eager library call"
     result = {
         "metric": METRIC if args.workload == "stft" else f"{job.w.name} clips/sec",
         "value": value,
@@ -371,6 +400,8 @@ def run_ours(args, world, rank, local):
                      "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)},
         "e2e": {"value": e2e_value, "unit": "clips/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "host_latency_ms": {"median": lat[len(lat) // 2], "p90": lat[(9 * len(lat)) // 10], "samples": len(lat),
+                            "launch": "cuda graph replay" if args.graph else "eager library call"},
         "gpu_launches": args.steps * job.kernels,
         "clocks": clk.summary(),
     }
@@ -423,6 +454,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs on smaller cases)")
+    ap.add_argument("--graph", action="store_true", help="replay one captured CUDA graph per step")
     ap.add_argument("--workload", choices=["stft", "wave_whisper", "wave_pcm16"], default="stft",
                     help="stft (default, the headline) or one of the waveform workloads")
     args = ap.parse_args()

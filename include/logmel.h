@@ -190,7 +190,7 @@ lm_status lm_workspace_error(const void *workspace, size_t workspace_bytes, uint
  * onesided always true). */
 typedef struct lm_mel_params {
   int32_t sample_rate; /* Hz, > 0 */
-  int32_t n_fft;       /* 400, or a power of two in [64, 4096] */
+  int32_t n_fft;       /* 400, or a power of two in [64, 16384] */
   int32_t win_length;  /* 0 = n_fft; otherwise 1..n_fft, window centred in the frame */
   int32_t hop_length;  /* > 0 */
   int32_t n_mels;      /* 1..256 */

@@ -451,25 +451,44 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
   }
 
   // ---------------------------- consumers ----------------------------
-  // Support of each filter row: first and last nonzero bin.
-  for (int n = warp; n < a.NM; n += CW) {
-    const float *row = a.filters + static_cast<int64_t>(n) * a.NF;
-    int first = INT_MAX, last = -1;
-    for (int k0 = 0; k0 < a.NF; k0 += 32) {
-      const int k = k0 + lane;
-      const float v = k < a.NF ? __ldg(row + k) : 0.f;
-      const unsigned m = __ballot_sync(0xffffffffu, v != 0.f);
-      if (m) {
-        if (first == INT_MAX) first = k0 + __ffs(m) - 1;
-        last = k0 + 31 - __clz(m);
+  // Support of each filter row: first and last nonzero bin.  All consumer
+  // threads sweep the dense matrix together with eight independent loads in
+  // flight each, folding nonzeros into shared minima and maxima
+  // (band_width holds the last nonzero bin until the final pass).
+  for (int n = threadIdx.x; n < a.NM; n += kConsumers) {
+    aux.band_start[n] = INT_MAX;
+    aux.band_width[n] = -1;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  {
+    constexpr int U = 8;
+    const int64_t total = static_cast<int64_t>(a.NM) * a.NF;
+    for (int64_t i0 = threadIdx.x; i0 < total; i0 += U * kConsumers) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + u * kConsumers;
+        v[u] = i < total ? __ldg(a.filters + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (v[u] != 0.f) {
+          const int64_t i = i0 + u * kConsumers;
+          const int r = static_cast<int>(i / a.NF);
+          const int col = static_cast<int>(i - static_cast<int64_t>(r) * a.NF);
+          atomicMin(&aux.band_start[r], col);
+          atomicMax(&aux.band_width[r], col);
+        }
       }
     }
-    if (lane == 0) {
-      const int width = last >= 0 ? last - first + 1 : 0;
-      aux.band_start[n] = last >= 0 ? first : 0;
-      aux.band_width[n] = width;
-      atomicMax(&aux.max_width, width);
-    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  for (int n = threadIdx.x; n < a.NM; n += kConsumers) {
+    const int first = aux.band_start[n], last = aux.band_width[n];
+    const int width = last >= 0 ? last - first + 1 : 0;
+    aux.band_start[n] = last >= 0 ? first : 0;
+    aux.band_width[n] = width;
+    atomicMax(&aux.max_width, width);
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 

@@ -100,6 +100,10 @@ struct WaveCfg {
   static constexpr int NFP = NF | 1;  // odd power-tile row stride
   // frames per tile: enough work for 256 threads, bounded by shared memory
   static constexpr int TF = NFFT <= 512 ? 16 : (NFFT <= 1024 ? 8 : (NFFT <= 4096 ? 2 : 1));
+  // Up to 4096 every table sits in shared memory; beyond, only the FFT
+  // twiddles do and the window, untangle twiddles and filterbank are read
+  // through L1 from global memory.
+  static constexpr bool kSmallTables = NFFT <= 4096;
   // The power tile (TF rows of NFP floats) lives in whichever FFT buffer does
   // not hold the transform's result; it needs at most half of it.
   static constexpr bool kResultInB = fft::num_passes<M>() % 2 == 1;
@@ -112,9 +116,12 @@ template <int NFFT>
 size_t wave_smem_bytes(int n_mels, int wmax) {
   using C = WaveCfg<NFFT>;
   size_t b = 2 * sizeof(float2) * C::TF * C::M;
-  b += sizeof(float2) * (2 * C::M + 1);
-  b += sizeof(float) * NFFT;
-  b += sizeof(int) * 2 * n_mels + sizeof(float) * n_mels * wmax;
+  b += sizeof(float2) * C::M;
+  if (C::kSmallTables) {
+    b += sizeof(float2) * (C::M + 1);
+    b += sizeof(float) * NFFT;
+    b += sizeof(int) * 2 * n_mels + sizeof(float) * n_mels * wmax;
+  }
   b += 16;  // tile key and abort flag
   return (b + 127) / 128 * 128;  // the sample-span buffers follow, 128-byte aligned
 }
@@ -128,12 +135,18 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   float2 *bufB = bufA + TF * M;
   float *pw = reinterpret_cast<float *>(C::kResultInB ? bufA : bufB);
   float2 *twm = bufB + TF * M;
-  float2 *twn = twm + M;
-  float *win = reinterpret_cast<float *>(twn + M + 1);
-  int *fstart = reinterpret_cast<int *>(win + NFFT);
-  int *fwidth = fstart + a.n_mels;
-  float *fw = reinterpret_cast<float *>(fwidth + a.n_mels);
-  uint32_t *blk_key = reinterpret_cast<uint32_t *>(fw + a.n_mels * a.wmax);
+  float2 *twn_s = twm + M;
+  float *win_s = reinterpret_cast<float *>(twn_s + M + 1);
+  int *fstart_s = reinterpret_cast<int *>(win_s + NFFT);
+  int *fwidth_s = fstart_s + a.n_mels;
+  float *fw_s = reinterpret_cast<float *>(fwidth_s + a.n_mels);
+  uint32_t *blk_key = C::kSmallTables ? reinterpret_cast<uint32_t *>(fw_s + a.n_mels * a.wmax)
+                                      : reinterpret_cast<uint32_t *>(twm + M);
+  const float2 *twn = C::kSmallTables ? twn_s : a.tw_n;
+  const float *win = C::kSmallTables ? win_s : a.window;
+  const int *fstart = C::kSmallTables ? fstart_s : a.fstart;
+  const int *fwidth = C::kSmallTables ? fwidth_s : a.fwidth;
+  const float *fw = C::kSmallTables ? fw_s : a.fw;
   int *abort_flag_p = reinterpret_cast<int *>(blk_key + 1);
   volatile int *abort_flag = abort_flag_p;
   unsigned char *seg = smem + a.seg_offset;  // two buffers of seg_bytes
@@ -178,13 +191,15 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   uint32_t fill0 = 0u, fill1 = 0u;  // completed span copies per buffer (the same in every thread)
 
   for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
-  for (int i = threadIdx.x; i <= M; i += blockDim.x) twn[i] = a.tw_n[i];
-  for (int i = threadIdx.x; i < NFFT; i += blockDim.x) win[i] = a.window[i];
-  for (int i = threadIdx.x; i < a.n_mels; i += blockDim.x) {
-    fstart[i] = a.fstart[i];
-    fwidth[i] = a.fwidth[i];
+  if constexpr (C::kSmallTables) {
+    for (int i = threadIdx.x; i <= M; i += blockDim.x) twn_s[i] = a.tw_n[i];
+    for (int i = threadIdx.x; i < NFFT; i += blockDim.x) win_s[i] = a.window[i];
+    for (int i = threadIdx.x; i < a.n_mels; i += blockDim.x) {
+      fstart_s[i] = a.fstart[i];
+      fwidth_s[i] = a.fwidth[i];
+    }
+    for (int i = threadIdx.x; i < a.n_mels * a.wmax; i += blockDim.x) fw_s[i] = a.fw[i];
   }
-  for (int i = threadIdx.x; i < a.n_mels * a.wmax; i += blockDim.x) fw[i] = a.fw[i];
 
   const int64_t n_tiles = a.B * a.tiles_per_clip;
   int it = 0;
@@ -272,28 +287,47 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
     }
     __syncthreads();
 
-    // 4. mel projection and store; lanes run over frames of one band
+    // 4. mel projection and store
     float lmax = -INFINITY;
-    for (int idx = threadIdx.x; idx < a.n_mels * TF; idx += blockDim.x) {
-      const int m = idx / TF;
-      const int f = idx - m * TF;
-      if (f < nf) {
+    auto emit = [&](int m, int f, float acc) {
+      const int64_t o = (b * a.n_mels + m) * a.n_frames + t0 + f;
+      if (a.log_mel) {
+        float l2;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(fmaxf(acc, 1e-10f)));
+        const float v = l2 * 0.30102999566398120f;  // log10(x) = log2(x) log10(2)
+        lmax = fmaxf(lmax, v);
+        static_cast<float *>(a.out)[o] = v;
+      } else if (a.out_f16) {
+        static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
+      } else {
+        static_cast<float *>(a.out)[o] = acc;
+      }
+    };
+    if constexpr (TF == 1) {
+      // One frame, filters hundreds of bins wide: a warp per band, lanes
+      // over taps, then a shuffle reduction.
+      const int lane = threadIdx.x & 31;
+      for (int m = threadIdx.x >> 5; m < a.n_mels; m += kWaveThreads / 32) {
         const int st = fstart[m], wd = fwidth[m];
         const float *w = fw + m * a.wmax;
-        const float *pr = pw + f * NFP + st;
         float acc = 0.f;
-        for (int t = 0; t < wd; ++t) acc = fmaf(w[t], pr[t], acc);
-        const int64_t o = (b * a.n_mels + m) * a.n_frames + t0 + f;
-        if (a.log_mel) {
-          float l2;
-          asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(fmaxf(acc, 1e-10f)));
-          const float v = l2 * 0.30102999566398120f;  // log10(x) = log2(x) log10(2)
-          lmax = fmaxf(lmax, v);
-          static_cast<float *>(a.out)[o] = v;
-        } else if (a.out_f16) {
-          static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
-        } else {
-          static_cast<float *>(a.out)[o] = acc;
+        for (int t = lane; t < wd; t += 32) acc = fmaf(w[t], pw[st + t], acc);
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+        if (lane == 0) emit(m, 0, acc);
+      }
+    } else {
+      // Lanes run over frames of one band.
+      for (int idx = threadIdx.x; idx < a.n_mels * TF; idx += blockDim.x) {
+        const int m = idx / TF;
+        const int f = idx - m * TF;
+        if (f < nf) {
+          const int st = fstart[m], wd = fwidth[m];
+          const float *w = fw + m * a.wmax;
+          const float *pr = pw + f * NFP + st;
+          float acc = 0.f;
+          for (int t = 0; t < wd; ++t) acc = fmaf(w[t], pr[t], acc);
+          emit(m, f, acc);
         }
       }
     }
@@ -325,13 +359,15 @@ bool pick_wave_kernel(int n_fft, int n_mels, int wmax, WaveKernel *k, size_t *sm
     case 1024: wave_entry<1024>(k, smem, tf, n_mels, wmax); return true;
     case 2048: wave_entry<2048>(k, smem, tf, n_mels, wmax); return true;
     case 4096: wave_entry<4096>(k, smem, tf, n_mels, wmax); return true;
+    case 8192: wave_entry<8192>(k, smem, tf, n_mels, wmax); return true;
+    case 16384: wave_entry<16384>(k, smem, tf, n_mels, wmax); return true;
     default: return false;
   }
 }
 
 bool supported_nfft(int n) {
   if (n == 400) return true;
-  if (n < 64 || n > 4096) return false;
+  if (n < 64 || n > 16384) return false;
   return (n & (n - 1)) == 0;
 }
 

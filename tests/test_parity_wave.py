@@ -70,6 +70,20 @@ def test_power_of_two_sizes(lm, oracle_mod, n_fft):
     _run(lm, oracle_mod, x, 16000, n_fft, n_fft // 4, 40 if n_fft <= 128 else 80, f_max=8000.0)
 
 
+@pytest.mark.parametrize("n_fft", [8192, 16384])
+def test_large_fft_sizes(lm, oracle_mod, n_fft):
+    # Past 4096 points the window, untangle twiddles and filterbank are read
+    # from global memory, one frame per tile, a warp per mel band.  8192 still
+    # stages aligned sample spans; 16384 always gathers.  Seven frames a clip
+    # keep the oracle's direct DFT to a few seconds.
+    T = 3 * n_fft + 77
+    x = workloads.wave_sines(2, T, 22050, seed=n_fft)
+    _run(lm, oracle_mod, x, 22050, n_fft, n_fft // 2, 128, f_max=11025.0, mel_scale="slaney", norm="slaney")
+    _run(lm, oracle_mod, x, 22050, n_fft, n_fft // 2, 80, f_max=8000.0, log_mel=True)
+    xi = workloads.wave_pcm16(2, T, seed=n_fft + 1)
+    _run(lm, oracle_mod, xi, 16000, n_fft, n_fft // 2, 256, f_max=8000.0, out_dtype="f16")
+
+
 @pytest.mark.parametrize("pad_mode", ["reflect", "constant", "replicate", "circular"])
 def test_pad_modes(lm, oracle_mod, pad_mode):
     x = workloads.wave_sines(2, 3333, 16000, seed=7)
