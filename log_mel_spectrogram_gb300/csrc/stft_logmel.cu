@@ -52,14 +52,14 @@
 namespace lm {
 namespace {
 
-constexpr int kLag = 12;         // resident mode: steps a tile's log values wait in shared memory
-constexpr int kResolveWindow = 4;  // steps whose clip maxima the resolver reads per round
-constexpr int kSlots = 32;       // ring of per-step handshake slots (> kLag + kResolveWindow)
+constexpr int kLag = 7;          // resident mode: steps a tile's log values wait in shared memory
+constexpr int kResolveSteps = 8;  // steps the resolver polls together
+constexpr int kSlots = 32;       // ring of per-step handshake slots (> kLag + kMaxStages)
 constexpr int kMaxStages = 8;
 constexpr int kRegTaps = 8;      // filter taps held in registers per band
 constexpr int kMaxBands = 512;
 constexpr int kMaxBins = 8193;
-constexpr int kStageTargetBytes = 48 * 1024;
+constexpr int kStageTargetBytes = 39 * 1024;
 
 constexpr int threads_for(int cw) { return (cw + 3) * 32; }
 
@@ -354,98 +354,118 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
   }
 
   if (warp == kResolverWarp) {
-    // ---- resolver: clip maxima for kResolveWindow steps per round ----
-    // A round serves steps q0 .. q0+W-1 once this CTA has published the last
-    // of them (which also keeps the resolver less than kSlots steps ahead of
-    // the consumers, so no handshake slot is reused before it was read).
-    // The whole warp reads each step's clip slots with 16-byte loads -- the
-    // loads of all W clips are in flight together -- and a step is handed to
-    // the consumers as soon as none of its clip's slots is zero.
+    // ---- resolver: clip maxima over a sliding window of steps ----
+    // Step q is served (its clip maximum handed to the consumers) once this
+    // CTA has published step q -- which also keeps the resolver less than
+    // kSlots steps ahead of the consumers, so no handshake slot is reused
+    // before it was read -- and every tile slot of its clip is nonzero.  Each
+    // pass polls the first kResolveSteps unserved steps that this CTA has
+    // published, with the loads of all of them in flight together (16-byte
+    // relaxed loads by the whole warp), so a step is served about one L2
+    // round trip after its clip completes, in any order.
     if (!kResident) return;
-    constexpr int W = kResolveWindow;
-    TileIter it;
-    it.init(blockIdx.x, a.tiles_per_clip);
+    constexpr int M = kResolveSteps;
     const int tpc = a.tiles_per_clip;
-    for (int64_t q0 = 0; q0 < my_tiles; q0 += W) {
-      const int64_t last = min(q0 + W - 1, my_tiles - 1);
-      mbar_wait(&aux.pub_bar[last & (kSlots - 1)], static_cast<uint32_t>((last / kSlots) & 1), abort_flag, a.err);
-      const uint32_t *base[W];
-      int head[W];
-      unsigned pending = 0;
+    TileIter it0;  // at step q_next
+    it0.init(blockIdx.x, tpc);
+    int64_t q_next = 0;  // lowest step not yet served
+    unsigned done = 0;   // bit w: step q_next + w already served
+    uint64_t t0 = 0;
+    // Polling step q starts once this CTA has published step q + span: the
+    // clip of q ends by that step on every CTA, and the CTAs run nearly in
+    // step, so earlier polls would mostly fail and only take issue slots
+    // from the consumers.
+    auto gate = [&](int64_t q) { return min(q + a.span, my_tiles - 1); };
+    while (q_next < my_tiles) {
+      const int64_t g0 = gate(q_next);
+      if (!mbar_wait(&aux.pub_bar[g0 & (kSlots - 1)], static_cast<uint32_t>((g0 / kSlots) & 1), abort_flag, a.err))
+        return;
+      // Lane w < M tests the gate of step q_next + w; the publisher goes in
+      // step order, so the open steps are a prefix.  A gate is fewer than
+      // kSlots steps past a published step, so its parity is unambiguous.
+      int open = 0;
+      if (lane < M) {
+        const int64_t q = q_next + lane;
+        if (q < my_tiles) {
+          const int64_t g = gate(q);
+          open = lane == 0 || mbar_test_wait(smem_u32(&aux.pub_bar[g & (kSlots - 1)]),
+                                             static_cast<uint32_t>((g / kSlots) & 1));
+        }
+      }
+      const unsigned openmask = __ballot_sync(0xffffffffu, open);
+      const unsigned poll = ((1u << (__ffs(~openmask) - 1)) - 1u) & ~done;
+      const uint32_t *base[M];
+      int head[M];
+      TileIter it = it0;
 #pragma unroll
-      for (int w = 0; w < W; ++w) {
+      for (int w = 0; w < M; ++w) {
         const uint32_t *slots = a.tile_key + it.b * tpc;
         head[w] = static_cast<int>((reinterpret_cast<uintptr_t>(slots) & 15) >> 2);  // slots before the clip's first
         base[w] = slots - head[w];                                                   // 16-byte aligned
-        if (q0 + w < my_tiles) pending |= 1u << w;
         it.next(a);
       }
-      uint64_t t0 = 0;
-      while (pending) {
-        uint32_t m[W];
-        bool ok[W];
+      uint32_t m[M];
+      bool ok[M];
 #pragma unroll
-        for (int w = 0; w < W; ++w) {
-          m[w] = 0;
-          ok[w] = true;
-          if (pending & (1u << w)) {
-            const int nvec = (head[w] + tpc + 3) >> 2;
-            for (int v = lane; v < nvec; v += 32) {
-              const uint4 x = ld_relaxed_gpu_v4(base[w] + 4 * v);
-              const uint32_t e[4] = {x.x, x.y, x.z, x.w};
+      for (int w = 0; w < M; ++w) {
+        m[w] = 0;
+        ok[w] = true;
+        if ((poll >> w) & 1u) {
+          const int nvec = (head[w] + tpc + 3) >> 2;
+          for (int v = lane; v < nvec; v += 32) {
+            const uint4 x = ld_relaxed_gpu_v4(base[w] + 4 * v);
+            const uint32_t e[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int slot = 4 * v + j - head[w];
-                if (slot >= 0 && slot < tpc) {
-                  ok[w] = ok[w] && (e[j] != 0u);
-                  m[w] = max(m[w], e[j]);
-                }
+            for (int j = 0; j < 4; ++j) {
+              const int slot = 4 * v + j - head[w];
+              if (slot >= 0 && slot < tpc) {
+                ok[w] = ok[w] && (e[j] != 0u);
+                m[w] = max(m[w], e[j]);
               }
             }
           }
         }
+      }
+      unsigned served = 0;
 #pragma unroll
-        for (int w = 0; w < W; ++w) {
-          if (pending & (1u << w)) {
-            const bool all = __all_sync(0xffffffffu, ok[w]);
-            const uint32_t mx = __reduce_max_sync(0xffffffffu, m[w]);
-            if (all) {
-              const int64_t q = q0 + w;
-              if (lane == 0) {
-                aux.hi_val[q & (kSlots - 1)] = ordered_to_float(mx);
-                mbar_arrive(&aux.hi_bar[q & (kSlots - 1)]);
-              }
-              pending &= ~(1u << w);
-            }
-          }
-        }
-        if (!pending) break;
-        int stop = 0;
-        if (lane == 0) {
-          const uint64_t now = global_timer_ns();
-          if (t0 == 0) t0 = now;
-          if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
-            *abort_flag = 1;
-            atomicOr(a.err, kErrClipTimeout);
-          }
-          stop = *abort_flag;
-        }
-        if (__shfl_sync(0xffffffffu, stop, 0)) {
-          // give up: hand over whatever was read so the consumers can drain
-#pragma unroll
-          for (int w = 0; w < W; ++w) {
-            if ((pending & (1u << w)) && lane == 0) {
-              const int64_t q = q0 + w;
-              aux.hi_val[q & (kSlots - 1)] = 0.f;
+      for (int w = 0; w < M; ++w) {
+        if ((poll >> w) & 1u) {
+          const bool all = __all_sync(0xffffffffu, ok[w]);
+          const uint32_t mx = __reduce_max_sync(0xffffffffu, m[w]);
+          if (all) {
+            const int64_t q = q_next + w;
+            if (lane == 0) {
+              aux.hi_val[q & (kSlots - 1)] = ordered_to_float(mx);
               mbar_arrive(&aux.hi_bar[q & (kSlots - 1)]);
             }
+            served |= 1u << w;
           }
-          pending = 0;
-          break;
         }
-        __nanosleep(64);
       }
-      __syncwarp();
+      done |= served;
+      const int adv = __ffs(~done) - 1;  // served prefix
+      if (adv > 0) {
+        q_next += adv;
+        done >>= adv;
+        for (int i = 0; i < adv; ++i) it0.next(a);
+      }
+      if (served) {
+        t0 = 0;
+        continue;
+      }
+      int stop = 0;
+      if (lane == 0) {
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) t0 = now;
+        if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
+          *abort_flag = 1;
+          atomicOr(a.err, kErrClipTimeout);
+        }
+        stop = *abort_flag;
+      }
+      // give up: the consumers' waits end on the abort flag
+      if (__shfl_sync(0xffffffffu, stop, 0)) return;
+      __nanosleep(64);
     }
     return;
   }
@@ -461,23 +481,23 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
   {
+    // 32-bit indices (NM * NF < 2^23): a 64-bit division here cost microseconds.
     constexpr int U = 8;
-    const int64_t total = static_cast<int64_t>(a.NM) * a.NF;
-    for (int64_t i0 = threadIdx.x; i0 < total; i0 += U * kConsumers) {
+    const int total = a.NM * a.NF;
+    for (int i0 = threadIdx.x; i0 < total; i0 += U * kConsumers) {
       float v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t i = i0 + u * kConsumers;
+        const int i = i0 + u * kConsumers;
         v[u] = i < total ? __ldg(a.filters + i) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (v[u] != 0.f) {
-          const int64_t i = i0 + u * kConsumers;
-          const int r = static_cast<int>(i / a.NF);
-          const int col = static_cast<int>(i - static_cast<int64_t>(r) * a.NF);
-          atomicMin(&aux.band_start[r], col);
-          atomicMax(&aux.band_width[r], col);
+          const int i = i0 + u * kConsumers;
+          const int r = i / a.NF;
+          atomicMin(&aux.band_start[r], i - r * a.NF);
+          atomicMax(&aux.band_width[r], i - r * a.NF);
         }
       }
     }
@@ -561,6 +581,7 @@ KernelFn pick_fpt(int fpt, bool resident) {
     case 1: return pick_variant<1, CW>(resident);
     case 2: return pick_variant<2, CW>(resident);
     case 4: return pick_variant<4, CW>(resident);
+    case 6: return pick_variant<6, CW>(resident);
     default: return pick_variant<8, CW>(resident);
   }
 }
@@ -588,7 +609,7 @@ void tile_height(int NF, int NM, int *CW, int *FG, int *FPT) {
   const int64_t frame_bytes = static_cast<int64_t>(NF) * 8;
   *FG = fg_max;
   *FPT = 0;
-  for (int fpt : {8, 4, 2, 1}) {
+  for (int fpt : {8, 6, 4, 2, 1}) {
     if (static_cast<int64_t>(fg_max) * fpt * frame_bytes <= kStageTargetBytes) {
       *FPT = fpt;
       break;
@@ -645,10 +666,11 @@ lm_status plan_launch(int64_t B, int64_t F, int32_t NF, int32_t NM, StftLaunch *
   const char *variant = env_or("LOGMEL_K1_VARIANT", "auto");
   const bool force_two = std::strcmp(variant, "twopass") == 0;
   const bool force_res = std::strcmp(variant, "resident") == 0;
-  // The resolver serves step q once this CTA published step q + W - 1, so
-  // resident mode needs every tile of that clip by step q + kLag - 1:
-  // span + W - 1 <= kLag - 1.
-  ln->resident = !force_two && ln->span + kResolveWindow <= kLag;
+  // Consumers wait for step q's clip maximum after computing step q + kLag,
+  // so every tile of that clip (steps <= q + span on every CTA) is computed
+  // by then if span < kLag; the resolver serves q as soon as they are all
+  // published.  One step of slack is kept for the hand-off itself.
+  ln->resident = !force_two && ln->span + 1 <= kLag;
   if (ln->resident) {
     ln->tp = plan_tiles(NF, NM, dev.max_smem_optin, true);
     if (ln->tp.S < 2) ln->resident = false;  // the output ring does not fit beside two stages
