@@ -63,8 +63,9 @@ def _traffic_record():
         return None
     try:
         d = json.loads(rec.read_text())
-        src = ROOT / "log_mel_spectrogram_gb300" / "csrc" / "stft_logmel.cu"
-        if hashlib.sha256(src.read_bytes()).hexdigest() != d.get("source_sha256"):
+        csrc = ROOT / "log_mel_spectrogram_gb300" / "csrc"
+        digest = hashlib.sha256((csrc / "stft_logmel.cu").read_bytes() + (csrc / "ptx.cuh").read_bytes())
+        if digest.hexdigest() != d.get("source_sha256"):
             return None
         return d
     except Exception:
