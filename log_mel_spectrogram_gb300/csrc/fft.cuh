@@ -24,6 +24,20 @@ __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
 __device__ __forceinline__ float2 mul_neg_i(float2 z) { return make_float2(z.y, -z.x); }
 __device__ __forceinline__ float2 cscale(float2 z, float s) { return make_float2(z.x * s, z.y * s); }
 
+// Frame buffers of power-of-two transforms hold element x at x + x / 32: one
+// padding slot every 32 elements, so the power-of-radix strides of the
+// passes do not land in the same banks (a radix-8 pass over 512 points
+// otherwise stores with a 64-byte stride, 16 lanes to one bank).  Mixed-radix
+// sizes (400) are laid out unpadded: their strides spread over the banks and
+// the extra index arithmetic measured slower.
+template <int M>
+struct Layout {
+  static constexpr bool kPad = (M & (M - 1)) == 0;
+  __host__ __device__ static constexpr int at(int x) { return kPad ? x + (x >> 5) : x; }
+  // slots a buffer of n logical elements occupies
+  __host__ __device__ static constexpr int size(int n) { return kPad ? n + (n >> 5) + 1 : n; }
+};
+
 template <int R>
 struct Dft;
 
@@ -94,28 +108,34 @@ struct Dft<5> {
   }
 };
 
-// One Stockham pass over `frames` frames of M points stored back to back.
-template <int M, int R, int P>
+// One Stockham pass over FRAMES frames of M points stored back to back (at
+// Layout<M> positions), by NT threads (the block size); every loop bound is
+// a compile-time constant.
+template <int M, int R, int P, int FRAMES, int NT>
 __device__ __forceinline__ void pass(const float2 *__restrict__ in, float2 *__restrict__ out,
-                                     const float2 *__restrict__ W, int frames) {
+                                     const float2 *__restrict__ W) {
   constexpr int T = M / R;
   constexpr int TW = M / (P * R);  // twiddle table stride
-  for (int g = threadIdx.x; g < frames * T; g += blockDim.x) {
+  constexpr int ITEMS = FRAMES * T;
+#pragma unroll
+  for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
+    const int g = static_cast<int>(threadIdx.x) + r * NT;
+    if (ITEMS % NT != 0 && g >= ITEMS) break;
     const int f = g / T;
     const int i = g - f * T;
     const int k = i % P;
-    const float2 *src = in + f * M + i;
+    const int base = f * M + i;
     float2 u[R];
 #pragma unroll
-    for (int j = 0; j < R; ++j) u[j] = src[j * T];
+    for (int j = 0; j < R; ++j) u[j] = in[Layout<M>::at(base + j * T)];
     if constexpr (P > 1) {
 #pragma unroll
       for (int j = 1; j < R; ++j) u[j] = cmul(u[j], W[j * k * TW]);
     }
     Dft<R>::run(u);
-    float2 *dst = out + f * M + (i - k) * R + k;
+    const int obase = f * M + (i - k) * R + k;
 #pragma unroll
-    for (int l = 0; l < R; ++l) dst[l * P] = u[l];
+    for (int l = 0; l < R; ++l) out[Layout<M>::at(obase + l * P)] = u[l];
   }
 }
 
@@ -137,17 +157,17 @@ __host__ __device__ constexpr int num_passes() {
   }
 }
 
-// Runs every pass, ping-ponging between a and b.  Returns true when the
-// result ends in b.
-template <int M, int P = 1>
-__device__ __forceinline__ bool run(float2 *a, float2 *b, const float2 *W, int frames) {
+// Runs every pass over FRAMES frames with NT threads, ping-ponging between a
+// and b.  Returns true when the result ends in b.
+template <int M, int FRAMES, int NT, int P = 1>
+__device__ __forceinline__ bool run(float2 *a, float2 *b, const float2 *W) {
   if constexpr (P == M) {
     return false;
   } else {
     constexpr int R = next_radix<M, P>();
-    pass<M, R, P>(a, b, W, frames);
+    pass<M, R, P, FRAMES, NT>(a, b, W);
     __syncthreads();
-    return !run<M, P * R>(b, a, W, frames);
+    return !run<M, FRAMES, NT, P * R>(b, a, W);
   }
 }
 

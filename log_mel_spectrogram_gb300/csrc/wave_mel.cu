@@ -107,15 +107,18 @@ struct WaveCfg {
   // The power tile (TF rows of NFP floats) lives in whichever FFT buffer does
   // not hold the transform's result; it needs at most half of it.
   static constexpr bool kResultInB = fft::num_passes<M>() % 2 == 1;
-  static_assert(TF * NFP * sizeof(float) <= TF * M * sizeof(float2), "power tile must fit an FFT buffer");
+  using L = fft::Layout<M>;
+  static constexpr int BUF = L::size(TF * M);  // float2 slots per FFT buffer
+  static_assert(TF * NFP * sizeof(float) <= BUF * sizeof(float2), "power tile must fit an FFT buffer");
 };
 
-// Shared memory: bufA, bufB [TF*M] float2 (the power tile reuses one) | tw_m [M] | tw_n [M+1]
+// Shared memory: bufA, bufB [BUF] float2 (TF frames of M points at Layout<M>
+// positions; the power tile reuses one) | tw_m [M] | tw_n [M+1]
 //                | window [NFFT] | fstart, fwidth [n_mels] | fw [n_mels*wmax] | keys
 template <int NFFT>
 size_t wave_smem_bytes(int n_mels, int wmax) {
   using C = WaveCfg<NFFT>;
-  size_t b = 2 * sizeof(float2) * C::TF * C::M;
+  size_t b = 2 * sizeof(float2) * C::BUF;
   b += sizeof(float2) * C::M;
   if (C::kSmallTables) {
     b += sizeof(float2) * (C::M + 1);
@@ -132,20 +135,19 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   constexpr int M = C::M, TF = C::TF, NFP = C::NFP;
   extern __shared__ __align__(16) unsigned char smem[];
   float2 *bufA = reinterpret_cast<float2 *>(smem);
-  float2 *bufB = bufA + TF * M;
+  float2 *bufB = bufA + C::BUF;
   float *pw = reinterpret_cast<float *>(C::kResultInB ? bufA : bufB);
-  float2 *twm = bufB + TF * M;
+  float2 *twm = bufB + C::BUF;
   float2 *twn_s = twm + M;
   float *win_s = reinterpret_cast<float *>(twn_s + M + 1);
-  int *fstart_s = reinterpret_cast<int *>(win_s + NFFT);
-  int *fwidth_s = fstart_s + a.n_mels;
-  float *fw_s = reinterpret_cast<float *>(fwidth_s + a.n_mels);
+  int2 *fsw_s = reinterpret_cast<int2 *>(win_s + NFFT);  // {first bin, width} per band
+  float *fw_s = reinterpret_cast<float *>(fsw_s + a.n_mels);
   uint32_t *blk_key = C::kSmallTables ? reinterpret_cast<uint32_t *>(fw_s + a.n_mels * a.wmax)
                                       : reinterpret_cast<uint32_t *>(twm + M);
   const float2 *twn = C::kSmallTables ? twn_s : a.tw_n;
   const float *win = C::kSmallTables ? win_s : a.window;
-  const int *fstart = C::kSmallTables ? fstart_s : a.fstart;
-  const int *fwidth = C::kSmallTables ? fwidth_s : a.fwidth;
+  const int *fstart = a.fstart;  // global: one-frame tiles only
+  const int *fwidth = a.fwidth;
   const float *fw = C::kSmallTables ? fw_s : a.fw;
   int *abort_flag_p = reinterpret_cast<int *>(blk_key + 1);
   volatile int *abort_flag = abort_flag_p;
@@ -194,10 +196,7 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   if constexpr (C::kSmallTables) {
     for (int i = threadIdx.x; i <= M; i += blockDim.x) twn_s[i] = a.tw_n[i];
     for (int i = threadIdx.x; i < NFFT; i += blockDim.x) win_s[i] = a.window[i];
-    for (int i = threadIdx.x; i < a.n_mels; i += blockDim.x) {
-      fstart_s[i] = a.fstart[i];
-      fwidth_s[i] = a.fwidth[i];
-    }
+    for (int i = threadIdx.x; i < a.n_mels; i += blockDim.x) fsw_s[i] = make_int2(a.fstart[i], a.fwidth[i]);
     for (int i = threadIdx.x; i < a.n_mels * a.wmax; i += blockDim.x) fw_s[i] = a.fw[i];
   }
 
@@ -231,7 +230,48 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
     const int64_t head = staged ? (static_cast<int64_t>(b * a.T + s_first) * es - static_cast<int64_t>(span_a0)) / es : 0;
     const float *segf = reinterpret_cast<const float *>(seg + buf * static_cast<size_t>(a.seg_bytes));
     const int16_t *segh = reinterpret_cast<const int16_t *>(segf);
-    for (int idx = threadIdx.x; idx < TF * M; idx += blockDim.x) {
+    // Staged tile whose sample pairs (2n, 2n+1) are aligned in the span
+    // buffer (even head and hop): one 8-byte (f32) or 4-byte (i16) load per
+    // complex point, the window as pairs too, compile-time trip count.
+    const bool paired = staged && ((static_cast<int>(head) | a.hop) & 1) == 0;
+    if (paired) {
+      // 32-bit shared addresses; thread idx handles point n of frame f.
+      constexpr int ITEMS = TF * M;
+      const uint32_t seg0 = smem_u32(segf) + static_cast<uint32_t>(head) * es;
+      // the window is in shared memory only with the small tables
+      const uint32_t win0 = C::kSmallTables ? smem_u32(win) : 0u;
+      const float2 *win_g = reinterpret_cast<const float2 *>(win);
+      const uint32_t dst0 = smem_u32(bufA);
+      const bool i16 = a.in_i16 != 0;
+#pragma unroll 4
+      for (int r = 0; r < (ITEMS + kWaveThreads - 1) / kWaveThreads; ++r) {
+        const int idx = static_cast<int>(threadIdx.x) + r * kWaveThreads;
+        if (ITEMS % kWaveThreads != 0 && idx >= ITEMS) break;
+        const int f = idx / M;
+        const int n = idx - f * M;
+        float2 z = make_float2(0.f, 0.f);
+        if (f < nf) {
+          const uint32_t e = static_cast<uint32_t>(f * a.hop + 2 * n);  // sample offset from head, even
+          float2 x;
+          if (i16) {
+            const int v = lds_s32(seg0 + 2u * e);
+            x = make_float2(static_cast<float>(static_cast<int16_t>(v & 0xffff)) * (1.0f / 32768.0f),
+                            static_cast<float>(static_cast<int16_t>(v >> 16)) * (1.0f / 32768.0f));
+          } else {
+            x = lds_f32x2(seg0 + 4u * e);
+          }
+          float2 w;
+          if constexpr (C::kSmallTables) {
+            w = lds_f32x2(win0 + 8u * static_cast<uint32_t>(n));
+          } else {
+            w = win_g[n];
+          }
+          z = make_float2(x.x * w.x, x.y * w.y);
+        }
+        sts_f32x2(dst0 + 8u * static_cast<uint32_t>(C::L::at(idx)), z);
+      }
+    }
+    for (int idx = paired ? TF * M : static_cast<int>(threadIdx.x); idx < TF * M; idx += blockDim.x) {
       const int f = idx / M;
       const int n = idx - f * M;
       float2 z = make_float2(0.f, 0.f);
@@ -262,35 +302,51 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
         }
         z = make_float2(x0 * win[2 * n], x1 * win[2 * n + 1]);
       }
-      bufA[idx] = z;
+      bufA[C::L::at(idx)] = z;
     }
     __syncthreads();
 
     // 2. N/2-point complex FFT of every frame
-    const bool in_b = fft::run<M>(bufA, bufB, twm, TF);
+    const bool in_b = fft::run<M, TF, kWaveThreads>(bufA, bufB, twm);
     const float2 *Z = in_b ? bufB : bufA;  // == kResultInB; pw is the other buffer
 
-    // 3. untangle the real spectrum and take |X|^power
-    for (int idx = threadIdx.x; idx < TF * (M + 1); idx += blockDim.x) {
-      const int f = idx / (M + 1);
-      const int k = idx - f * (M + 1);
-      const float2 A = Z[f * M + (k == M ? 0 : k)];
-      const float2 Bz = Z[f * M + (k == 0 ? 0 : M - k)];
-      const float2 Bc = make_float2(Bz.x, -Bz.y);
-      const float2 E = make_float2(0.5f * (A.x + Bc.x), 0.5f * (A.y + Bc.y));
-      // O = (A - Bc) / (2i) = -i (A - Bc) / 2
-      const float2 O = make_float2(0.5f * (A.y - Bc.y), -0.5f * (A.x - Bc.x));
-      const float2 X = fft::cadd(E, fft::cmul(twn[k], O));
-      float p = fmaf(X.x, X.x, X.y * X.y);
-      if (a.power_is_one) p = sqrtf(p);
-      pw[f * NFP + k] = p;
+    // 3. untangle the real spectrum and take |X|^power.  Bins k and M - k
+    // come from the same two values: with A = Z[k], B = Z[M-k],
+    // E = (A + conj B) / 2, O = (A - conj B) / (2i) and tw = exp(-2 pi i k / N),
+    // X[k] = E + tw O and X[M-k] = conj(E - tw O).  k = 0 gives X[0] and
+    // X[M]; k = M/2 is its own partner.
+    {
+      constexpr int KP = M / 2 + 1;  // pairs per frame (M is even)
+      constexpr int ITEMS = TF * KP;
+#pragma unroll 2
+      for (int r = 0; r < (ITEMS + kWaveThreads - 1) / kWaveThreads; ++r) {
+        const int idx = static_cast<int>(threadIdx.x) + r * kWaveThreads;
+        if (ITEMS % kWaveThreads != 0 && idx >= ITEMS) break;
+        const int f = idx / KP;
+        const int k = idx - f * KP;
+        const float2 A = Z[C::L::at(f * M + k)];
+        const float2 Bz = Z[C::L::at(f * M + (k == 0 ? 0 : M - k))];
+        const float2 E = make_float2(0.5f * (A.x + Bz.x), 0.5f * (A.y - Bz.y));
+        // O = (A - conj B) / (2i) = -i (A - conj B) / 2
+        const float2 O = make_float2(0.5f * (A.y + Bz.y), -0.5f * (A.x - Bz.x));
+        const float2 TO = fft::cmul(twn[k], O);
+        float p0 = fmaf(E.x + TO.x, E.x + TO.x, (E.y + TO.y) * (E.y + TO.y));
+        float p1 = fmaf(E.x - TO.x, E.x - TO.x, (E.y - TO.y) * (E.y - TO.y));
+        if (a.power_is_one) {
+          p0 = sqrtf(p0);
+          p1 = sqrtf(p1);
+        }
+        pw[f * NFP + k] = p0;
+        if (k != M / 2) pw[f * NFP + M - k] = p1;
+      }
     }
     __syncthreads();
 
     // 4. mel projection and store
     float lmax = -INFINITY;
+    const int64_t orow0 = b * a.n_mels * a.n_frames + t0;  // output index of (band 0, frame 0) of this tile
     auto emit = [&](int m, int f, float acc) {
-      const int64_t o = (b * a.n_mels + m) * a.n_frames + t0 + f;
+      const int64_t o = orow0 + static_cast<int64_t>(m) * a.n_frames + f;
       if (a.log_mel) {
         float l2;
         asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(fmaxf(acc, 1e-10f)));
@@ -317,16 +373,30 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
         if (lane == 0) emit(m, 0, acc);
       }
     } else {
-      // Lanes run over frames of one band.
-      for (int idx = threadIdx.x; idx < a.n_mels * TF; idx += blockDim.x) {
-        const int m = idx / TF;
-        const int f = idx - m * TF;
-        if (f < nf) {
-          const int st = fstart[m], wd = fwidth[m];
-          const float *w = fw + m * a.wmax;
-          const float *pr = pw + f * NFP + st;
+      // Thread = (frame f, band group): lanes run over the TF frames of one
+      // band, so each band's output row is written as a run of consecutive
+      // frames; the group walks bands m0, m0 + NG, ...  Shared memory is
+      // addressed with 32-bit offsets.
+      constexpr int NG = kWaveThreads / TF;
+      const int f = static_cast<int>(threadIdx.x) % TF;
+      if (f < nf) {
+        const uint32_t prow = smem_u32(pw) + static_cast<uint32_t>(f * NFP) * 4u;
+        const int m0 = static_cast<int>(threadIdx.x) / TF;
+        uint32_t fsw = smem_u32(fsw_s) + static_cast<uint32_t>(m0) * 8u;
+        uint32_t wa = smem_u32(fw_s) + static_cast<uint32_t>(m0 * a.wmax) * 4u;
+        const uint32_t wstep = static_cast<uint32_t>(NG * a.wmax) * 4u;
+        for (int m = m0; m < a.n_mels; m += NG, fsw += NG * 8, wa += wstep) {
+          const int2 sw = lds_s32x2(fsw);
+          const uint32_t pa = prow + static_cast<uint32_t>(sw.x) * 4u;
           float acc = 0.f;
-          for (int t = 0; t < wd; ++t) acc = fmaf(w[t], pr[t], acc);
+          int t = 0;
+          for (; t + 4 <= sw.y; t += 4) {
+            acc = fmaf(lds_f32(wa + 4 * t), lds_f32(pa + 4 * t), acc);
+            acc = fmaf(lds_f32(wa + 4 * t + 4), lds_f32(pa + 4 * t + 4), acc);
+            acc = fmaf(lds_f32(wa + 4 * t + 8), lds_f32(pa + 4 * t + 8), acc);
+            acc = fmaf(lds_f32(wa + 4 * t + 12), lds_f32(pa + 4 * t + 12), acc);
+          }
+          for (; t < sw.y; ++t) acc = fmaf(lds_f32(wa + 4 * t), lds_f32(pa + 4 * t), acc);
           emit(m, f, acc);
         }
       }
