@@ -98,8 +98,11 @@ struct WaveCfg {
   static constexpr int M = NFFT / 2;
   static constexpr int NF = NFFT / 2 + 1;
   static constexpr int NFP = NF | 1;  // odd power-tile row stride
-  // frames per tile: enough work for 256 threads, bounded by shared memory
-  static constexpr int TF = NFFT <= 512 ? 16 : (NFFT <= 1024 ? 8 : (NFFT <= 4096 ? 2 : 1));
+  // Frames per tile, bounded by shared memory.  Up to 1024 points, 8: at
+  // n_fft 400 two 16-frame CTAs per SM were 8% slower than eight-frame ones
+  // (more CTAs hide each other's barriers), and at 1024 four frames were 22%
+  // slower.
+  static constexpr int TF = NFFT <= 1024 ? 8 : (NFFT <= 4096 ? 2 : 1);
   // Up to 4096 every table sits in shared memory; beyond, only the FFT
   // twiddles do and the window, untangle twiddles and filterbank are read
   // through L1 from global memory.
