@@ -162,9 +162,10 @@ def cpu_baseline(stft_host, W_host, target_s: float = 12.0) -> dict:
 class StftJob:
     """log_mel_from_stft on the B=256, F=3000, NF=201, NM=128 batch (or --batch B)."""
 
-    def __init__(self, lm, workloads, dev, batch):
+    def __init__(self, lm, workloads, dev, batch, name="stft"):
         import torch
-        w = workloads.WHISPER_STFT_B256
+        w = {"stft": workloads.WHISPER_STFT_B256, "stft_small": workloads.WHISPER_STFT_SMALL,
+             "stft_b8": workloads.WHISPER_STFT}[name]
         if batch and batch != w.B:
             import dataclasses
             w = dataclasses.replace(w, B=batch, name=w.name.replace(f"b{w.B}_", f"b{batch}_"))
@@ -225,6 +226,7 @@ class WaveJob:
         self.out = self.mel(self.x)
         self.units = w.B
         self.bytes = w.canonical_bytes
+        self.flops = wave_flops(w)
         self.kernels = 2 if w.log_mel else 1
         self.flush_l2 = True  # 14-28 MB per step fits in L2
         self.inputs = [self.x]
@@ -245,6 +247,24 @@ class WaveJob:
 
     def kernel_note(self):
         return "wave_mel_kernel" + (" + logmel_clamp_kernel" if self.w.log_mel else "")
+
+
+# FP32 FMA peak of the GPU from its unit counts and clock: 152 SMs x 128
+# FP32 lanes x 2 flops per FMA x 2.07 GHz.
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def wave_flops(w) -> float:
+    """Algorithmic flops of one waveform step: per frame, the N/2-point
+    complex FFT at 5 (N/2) log2(N/2), the real-input untangle and power at 10
+    per bin, the window at 1 per sample, the mel projection at 2 per filter
+    tap (triangles overlap in pairs: about 2 taps per bin) and one log per
+    band on log plans."""
+    import math
+    M = w.n_fft // 2
+    nf = M + 1
+    per_frame = 5 * M * math.log2(M) + 10 * nf + w.n_fft + 2 * 2 * nf + (w.n_mels if w.log_mel else 0)
+    return w.B * w.n_frames * per_frame
 
 
 def run_ours(args, world, rank, local):
@@ -269,7 +289,7 @@ def run_ours(args, world, rank, local):
     barrier()
     import log_mel_spectrogram_gb300 as lm
 
-    job = StftJob(lm, workloads, dev, args.batch) if args.workload == "stft" else WaveJob(lm, workloads, dev,
+    job = StftJob(lm, workloads, dev, args.batch, args.workload) if args.workload.startswith("stft") else WaveJob(lm, workloads, dev,
                                                                                              args.workload, args.batch)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if job.flush_l2 else None
@@ -393,12 +413,20 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded, generated on the device; see workloads.py)",
         "achieved_hbm_gbs": achieved,
         "config": config,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": (trec["dram_bytes_per_launch"] if trec else None),
-                     "traffic_source": ("profiles/traffic.json" if trec else "stale or missing"),
-                     "kernel": job.kernel_note(),
-                     "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)},
+        "roofline": ({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                      "frac": achieved / peak, "peak_kind": peak_kind,
+                      "traffic": (trec["dram_bytes_per_launch"] if trec else None),
+                      "traffic_source": ("profiles/traffic.json" if trec else "stale or missing"),
+                      "kernel": job.kernel_note(),
+                      "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)}
+                     if not hasattr(job, "flops") else
+                     {"bound": "alu", "achieved": job.flops / mean_launch_s / 1e12, "peak": FP32_PEAK_TFLOPS,
+                      "unit": "TFLOP/s", "frac": job.flops / mean_launch_s / 1e12 / FP32_PEAK_TFLOPS,
+                      "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz",
+                      "traffic": None, "kernel": job.kernel_note(),
+                      "hbm_gbs": achieved, "hbm_frac_of_measured": achieved / peak,
+                      "flops_per_step": job.flops,
+                      "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)}),
         "e2e": {"value": e2e_value, "unit": "clips/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "host_latency_ms": {"median": lat[len(lat) // 2], "p90": lat[(9 * len(lat)) // 10], "samples": len(lat),
@@ -456,8 +484,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs on smaller cases)")
     ap.add_argument("--graph", action="store_true", help="replay one captured CUDA graph per step")
-    ap.add_argument("--workload", choices=["stft", "wave_whisper", "wave_pcm16"], default="stft",
-                    help="stft (default, the headline) or one of the waveform workloads")
+    ap.add_argument("--workload", choices=["stft", "stft_small", "stft_b8", "wave_whisper", "wave_pcm16"],
+                    default="stft",
+                    help="stft (default, the headline: B=256, F=3000, NM=128), stft_small (B=1, F=300, NM=80), "
+                         "stft_b8 (B=8, F=3000, NM=80) or one of the waveform workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
