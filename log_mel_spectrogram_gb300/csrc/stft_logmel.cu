@@ -774,8 +774,15 @@ lm_status launch_clip_clamp(float *out, const uint32_t *tile_key, int64_t B, int
                             int32_t tiles_per_clip, cudaStream_t stream) {
   const int vec4 = (per_clip % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
   const int64_t work = vec4 ? per_clip / 4 : per_clip;
-  const unsigned gx = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 1024)));
-  const unsigned gy = static_cast<unsigned>(std::min<int64_t>(B, 65535));
+  DeviceInfo dev;
+  if (lm_status st = current_device_info(&dev); st != LM_OK) return st;
+  // About four resident blocks per SM in all: every block first reduces its
+  // clip's tile slots, so one block per 256 items would repeat that
+  // reduction thousands of times for a few bytes of work each.
+  const int64_t gy64 = std::min<int64_t>(B, 65535);
+  const int64_t per_clip_blocks = (4 * static_cast<int64_t>(dev.sm_count) + gy64 - 1) / gy64;
+  const unsigned gx = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, per_clip_blocks)));
+  const unsigned gy = static_cast<unsigned>(gy64);
   logmel_clamp_kernel<<<dim3(gx, gy), 256, 0, stream>>>(out, tile_key, B, per_clip, tiles_per_clip, vec4);
   LM_CUDA_TRY(cudaGetLastError());
   return LM_OK;

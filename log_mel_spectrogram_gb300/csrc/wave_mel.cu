@@ -65,6 +65,7 @@ struct WaveArgs {
   int32_t pad_zero;                 // zeros added on both sides before centre padding
   int32_t n_mels, wmax, tiles_per_clip, TF;
   uint32_t *err;           // device error word (workspace header)
+  uint32_t *next_tile;     // tile counter (workspace header), zero at launch
   uint64_t total_bytes;    // B * T * sample size
   uint32_t seg_offset;     // shared-memory offset of the two sample-span buffers
   uint32_t seg_bytes;      // bytes per span buffer (multiple of 128)
@@ -203,20 +204,30 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
     for (int i = threadIdx.x; i < a.n_mels * a.wmax; i += blockDim.x) fw_s[i] = a.fw[i];
   }
 
+  // Tiles are handed out dynamically: a CTA's first tile is its index, each
+  // later one comes from a counter in the workspace header (zeroed per
+  // call), claimed at the start of the tile before it so its samples can be
+  // prefetched.  (Claiming two ahead measured slower: the last tiles go to
+  // CTAs that are not yet free.)
   const int64_t n_tiles = a.B * a.tiles_per_clip;
+  volatile int *next_s = reinterpret_cast<volatile int *>(blk_key + 2);  // n_tiles < 2^31 (host check)
   int it = 0;
-  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+  for (int64_t tile = blockIdx.x, nxt; tile < n_tiles; tile = nxt, ++it) {
     const int buf = it & 1;
     const int64_t b = tile / a.tiles_per_clip;
     const int tloc = static_cast<int>(tile - b * a.tiles_per_clip);
     const int64_t t0 = static_cast<int64_t>(tloc) * TF;
     const int64_t left = a.n_frames - t0;
     const int nf = left < TF ? static_cast<int>(left) : TF;
-    if (threadIdx.x == 0) *blk_key = 0u;
+    if (threadIdx.x == 0) {
+      *blk_key = 0u;
+      *next_s = static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
+    }
     __syncthreads();  // tables loaded / previous tile finished with every buffer
+    nxt = *next_s;
     // Prefetch the next tile's samples into the other span buffer; the
     // previous tile's framing, its last reader, finished before the barrier.
-    if (threadIdx.x == 0 && tile + gridDim.x < n_tiles) issue_span(tile + gridDim.x, buf ^ 1);
+    if (threadIdx.x == 0 && nxt < n_tiles) issue_span(nxt, buf ^ 1);
     uint64_t span_a0;
     uint32_t span_bytes;
     const bool staged = span_of(tile, &span_a0, &span_bytes);
@@ -713,11 +724,13 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   a.fwidth = plan->fwidth;
   a.fw = plan->fw;
   a.err = static_cast<uint32_t *>(workspace);
+  a.next_tile = static_cast<uint32_t *>(workspace) + 1;
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(T) * esize;
   a.seg_offset = static_cast<uint32_t>(seg_offset);
   a.seg_bytes = static_cast<uint32_t>(seg_used);
   a.use_seg = use_seg;
   const int64_t n_tiles = B * a.tiles_per_clip;
+  if (n_tiles > INT32_MAX / 2) return LM_ERR_UNSUPPORTED;  // tile indices and the counter are 32-bit
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_tiles, static_cast<int64_t>(di.sm_count) * per_sm));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Clears the device error word (and, for log plans, the tile slots).
