@@ -48,6 +48,8 @@ struct lm_mel_plan {
   int *fstart;   // [n_mels]
   int *fwidth;   // [n_mels]
   float *fw;     // [n_mels][wmax]
+  unsigned char *tables;  // n_fft <= 4096: tw_m | tw_n | window | {fstart, fwidth} | fw, the shared-memory image
+  uint32_t tables_bytes;  // its size, a multiple of 16
 };
 
 namespace lm {
@@ -76,6 +78,8 @@ struct WaveArgs {
   const int *fstart;
   const int *fwidth;
   const float *fw;
+  const unsigned char *tables;  // shared-memory image of the tables (n_fft <= 4096)
+  uint32_t tables_bytes;
 };
 
 __device__ __forceinline__ int64_t map_index(int64_t s, int64_t T, int mode, bool *zero) {
@@ -116,20 +120,29 @@ struct WaveCfg {
   static_assert(TF * NFP * sizeof(float) <= BUF * sizeof(float2), "power tile must fit an FFT buffer");
 };
 
+// Bytes of the table image up to 4096 points: tw_m [M] float2 | tw_n [M+1]
+// float2 | window [NFFT] | {fstart, fwidth} [n_mels] int2 | fw [n_mels*wmax],
+// rounded up to 16 (one bulk copy).
+inline uint32_t wave_tables_bytes(int n_fft, int n_mels, int wmax) {
+  const size_t M = n_fft / 2;
+  const size_t b = 8 * (2 * M + 1) + 4 * static_cast<size_t>(n_fft) + 8 * static_cast<size_t>(n_mels) +
+                   4 * static_cast<size_t>(n_mels) * wmax;
+  return static_cast<uint32_t>((b + 15) / 16 * 16);
+}
+
 // Shared memory: bufA, bufB [BUF] float2 (TF frames of M points at Layout<M>
-// positions; the power tile reuses one) | tw_m [M] | tw_n [M+1]
-//                | window [NFFT] | fstart, fwidth [n_mels] | fw [n_mels*wmax] | keys
+// positions; the power tile reuses one) | the table image (tw_m only above
+// 4096 points) | keys
 template <int NFFT>
 size_t wave_smem_bytes(int n_mels, int wmax) {
   using C = WaveCfg<NFFT>;
   size_t b = 2 * sizeof(float2) * C::BUF;
   b += sizeof(float2) * C::M;
   if (C::kSmallTables) {
-    b += sizeof(float2) * (C::M + 1);
-    b += sizeof(float) * NFFT;
-    b += sizeof(int) * 2 * n_mels + sizeof(float) * n_mels * wmax;
+    b -= sizeof(float2) * C::M;
+    b += wave_tables_bytes(NFFT, n_mels, wmax);
   }
-  b += 16;  // tile key and abort flag
+  b += 16;  // tile key, abort flag, next tile
   return (b + 127) / 128 * 128;  // the sample-span buffers follow, 128-byte aligned
 }
 
@@ -146,7 +159,7 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   float *win_s = reinterpret_cast<float *>(twn_s + M + 1);
   int2 *fsw_s = reinterpret_cast<int2 *>(win_s + NFFT);  // {first bin, width} per band
   float *fw_s = reinterpret_cast<float *>(fsw_s + a.n_mels);
-  uint32_t *blk_key = C::kSmallTables ? reinterpret_cast<uint32_t *>(fw_s + a.n_mels * a.wmax)
+  uint32_t *blk_key = C::kSmallTables ? reinterpret_cast<uint32_t *>(reinterpret_cast<unsigned char *>(twm) + a.tables_bytes)
                                       : reinterpret_cast<uint32_t *>(twm + M);
   const float2 *twn = C::kSmallTables ? twn_s : a.tw_n;
   const float *win = C::kSmallTables ? win_s : a.window;
@@ -156,7 +169,7 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   int *abort_flag_p = reinterpret_cast<int *>(blk_key + 1);
   volatile int *abort_flag = abort_flag_p;
   unsigned char *seg = smem + a.seg_offset;  // two buffers of seg_bytes
-  uint64_t *seg_bar = reinterpret_cast<uint64_t *>(seg + 2 * static_cast<size_t>(a.seg_bytes));
+  uint64_t *seg_bar = reinterpret_cast<uint64_t *>(seg + 2 * static_cast<size_t>(a.seg_bytes));  // [2]: tables
   const int es = a.in_i16 ? 2 : 4;
 
   // The contiguous samples an interior tile (no padding in play) reads:
@@ -190,18 +203,23 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
   if (threadIdx.x == 0) {
     mbar_init(&seg_bar[0], 1);
     mbar_init(&seg_bar[1], 1);
+    mbar_init(&seg_bar[2], 1);
     *abort_flag_p = 0;
     fence_mbar_init();
+    if constexpr (C::kSmallTables) {
+      // every table in one bulk copy of the plan's shared-memory image
+      mbar_arrive_expect_tx(&seg_bar[2], a.tables_bytes);
+      bulk_g2s_plain(twm, a.tables, a.tables_bytes, &seg_bar[2]);
+    }
     if (blockIdx.x < a.B * a.tiles_per_clip) issue_span(blockIdx.x, 0);
   }
   uint32_t fill0 = 0u, fill1 = 0u;  // completed span copies per buffer (the same in every thread)
 
-  for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
   if constexpr (C::kSmallTables) {
-    for (int i = threadIdx.x; i <= M; i += blockDim.x) twn_s[i] = a.tw_n[i];
-    for (int i = threadIdx.x; i < NFFT; i += blockDim.x) win_s[i] = a.window[i];
-    for (int i = threadIdx.x; i < a.n_mels; i += blockDim.x) fsw_s[i] = make_int2(a.fstart[i], a.fwidth[i]);
-    for (int i = threadIdx.x; i < a.n_mels * a.wmax; i += blockDim.x) fw_s[i] = a.fw[i];
+    __syncthreads();  // the barrier is initialised
+    mbar_wait(&seg_bar[2], 0, abort_flag, a.err);
+  } else {
+    for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
   }
 
   // Tiles are handed out dynamically: a CTA's first tile is its index, each
@@ -560,6 +578,7 @@ void free_plan(lm_mel_plan *pl) {
   cudaFree(pl->fstart);
   cudaFree(pl->fwidth);
   cudaFree(pl->fw);
+  cudaFree(pl->tables);
   delete pl;
 }
 
@@ -613,6 +632,25 @@ extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan
   if (st == LM_OK) st = lm::upload(t.fstart, &pl->fstart);
   if (st == LM_OK) st = lm::upload(t.fwidth, &pl->fwidth);
   if (st == LM_OK) st = lm::upload(t.fw, &pl->fw);
+  if (st == LM_OK && params->n_fft <= 4096) {
+    // the shared-memory image the kernel copies in one piece
+    pl->tables_bytes = lm::wave_tables_bytes(params->n_fft, params->n_mels, t.wmax);
+    std::vector<unsigned char> img(pl->tables_bytes, 0);
+    size_t o = 0;
+    auto put = [&](const void *src, size_t n) {
+      std::memcpy(img.data() + o, src, n);
+      o += n;
+    };
+    put(t.tw_m.data(), t.tw_m.size() * sizeof(float2));
+    put(t.tw_n.data(), t.tw_n.size() * sizeof(float2));
+    put(t.window.data(), t.window.size() * sizeof(float));
+    for (int m = 0; m < params->n_mels; ++m) {
+      const int sw[2] = {t.fstart[m], t.fwidth[m]};
+      put(sw, sizeof(sw));
+    }
+    put(t.fw.data(), t.fw.size() * sizeof(float));
+    st = lm::upload(img, &pl->tables);
+  }
   if (st != LM_OK) {
     lm::free_plan(pl);
     return st;
@@ -684,12 +722,12 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   lm::DeviceInfo di;
   if (lm_status st = lm::current_device_info(&di); st != LM_OK) return st;
   bool use_seg = (reinterpret_cast<uintptr_t>(wave) & 15) == 0 &&
-                 seg_offset + 2 * seg_bytes + 16 <= static_cast<size_t>(di.max_smem_optin);
+                 seg_offset + 2 * seg_bytes + 32 <= static_cast<size_t>(di.max_smem_optin);
   // Without staging (unaligned input, or a hop so long the spans do not fit)
   // every tile gathers its samples from global memory; the two mbarriers are
   // still reserved, right after the tables, since every CTA initialises them.
   const size_t seg_used = use_seg ? seg_bytes : 0;
-  smem = seg_offset + 2 * seg_used + 16;
+  smem = seg_offset + 2 * seg_used + 32;  // three mbarriers
   if (smem > static_cast<size_t>(di.max_smem_optin)) return LM_ERR_UNSUPPORTED;
   if (lm_status st = lm::ensure_smem_attribute(reinterpret_cast<const void *>(kern), static_cast<int>(smem));
       st != LM_OK)
@@ -723,6 +761,8 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   a.fstart = plan->fstart;
   a.fwidth = plan->fwidth;
   a.fw = plan->fw;
+  a.tables = plan->tables;
+  a.tables_bytes = plan->tables_bytes;
   a.err = static_cast<uint32_t *>(workspace);
   a.next_tile = static_cast<uint32_t *>(workspace) + 1;
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(T) * esize;
