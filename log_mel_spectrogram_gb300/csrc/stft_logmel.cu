@@ -539,6 +539,10 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
 __global__ void __launch_bounds__(256) logmel_clamp_kernel(float *out, const uint32_t *tile_key, int64_t B,
                                                            int64_t per_clip, int32_t tiles_per_clip, int vec4) {
   __shared__ uint32_t warp_keys[8];
+  // Launched as a programmatic dependent of the kernel that wrote the
+  // values: wait until that grid has finished and its writes are visible
+  // (a no-op for an ordinary launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
     uint32_t m = 0;
     for (int i = threadIdx.x; i < tiles_per_clip; i += blockDim.x) m = max(m, tile_key[b * tiles_per_clip + i]);
@@ -552,14 +556,28 @@ __global__ void __launch_bounds__(256) logmel_clamp_kernel(float *out, const uin
     float *o = out + b * per_clip;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (vec4) {
+      // Eight 16-byte loads in flight per thread before any store: the
+      // rewrite is in place, so one-at-a-time would wait an L2 round trip
+      // per vector.
+      constexpr int U = 8;
       float4 *o4 = reinterpret_cast<float4 *>(o);
-      for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < per_clip / 4; i += stride) {
-        float4 v = o4[i];
-        v.x = rescale(v.x, floor_v);
-        v.y = rescale(v.y, floor_v);
-        v.z = rescale(v.z, floor_v);
-        v.w = rescale(v.w, floor_v);
-        o4[i] = v;
+      const int64_t n4 = per_clip / 4;
+      for (int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i0 < n4; i0 += U * stride) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (i0 + u * stride < n4) v[u] = o4[i0 + u * stride];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (i0 + u * stride < n4) {
+            float4 w = v[u];
+            w.x = rescale(w.x, floor_v);
+            w.y = rescale(w.y, floor_v);
+            w.z = rescale(w.z, floor_v);
+            w.w = rescale(w.w, floor_v);
+            o4[i0 + u * stride] = w;
+          }
+        }
       }
     } else {
       for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < per_clip; i += stride)
@@ -783,8 +801,19 @@ lm_status launch_clip_clamp(float *out, const uint32_t *tile_key, int64_t B, int
   const int64_t per_clip_blocks = (4 * static_cast<int64_t>(dev.sm_count) + gy64 - 1) / gy64;
   const unsigned gx = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, per_clip_blocks)));
   const unsigned gy = static_cast<unsigned>(gy64);
-  logmel_clamp_kernel<<<dim3(gx, gy), 256, 0, stream>>>(out, tile_key, B, per_clip, tiles_per_clip, vec4);
-  LM_CUDA_TRY(cudaGetLastError());
+  // Programmatic dependent launch: the epilogue's blocks are staged while
+  // the previous kernel drains and start the moment it completes.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(gx, gy);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  LM_CUDA_TRY(cudaLaunchKernelEx(&cfg, logmel_clamp_kernel, out, tile_key, B, per_clip, tiles_per_clip, vec4));
   return LM_OK;
 }
 

@@ -440,6 +440,9 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
       if (threadIdx.x == 0) a.tile_key[tile] = *blk_key;
     }
   }
+  // This CTA is done: a programmatically dependent epilogue may be scheduled
+  // (it still waits for the whole grid before reading).
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 using WaveKernel = void (*)(WaveArgs);
