@@ -34,6 +34,7 @@ if str(ROOT) not in sys.path:
 METRIC = "log-mel clips/sec and achieved HBM GB/s vs GB300 peak (B=256 Whisper STFT)"
 L2_BYTES = 129 * 2 ** 20  # GB300 L2
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
 def _dist():
@@ -41,6 +42,25 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The largest of every rank's value (the slowest rank's time); the
+    identity with one rank.  Needs an initialised process group when world > 1
+    (NCCL with a CUDA device in the benchmark, gloo with "cpu" in the tests)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job units per second: every rank processes its own batch each
+    step (weak scaling) and the job takes the slowest rank's time."""
+    return world * units_per_rank * steps / (total_ms / 1e3)
 
 
 def _peaks():
@@ -348,13 +368,9 @@ def run_ours(args, world, rank, local):
         lat.append((time.perf_counter() - h0) * 1e3)
     lat.sort()
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * job.units * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, job.units, args.steps, total_ms)
 
     # end to end: pinned host input -> device -> library call -> host result
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 5))
@@ -382,13 +398,8 @@ def run_ours(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e_value = world * job.units * e2e_steps / (e2e_ms / 1e3)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e_value = job_throughput(world, job.units, e2e_steps, e2e_ms)
         del host_in, dev_in, out_h
 
     peak, peak_kind = _peaks()
@@ -415,6 +426,7 @@ def run_ours(args, world, rank, local):
         "config": config,
         "roofline": ({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                       "frac": achieved / peak, "peak_kind": peak_kind,
+                      "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                       "traffic": (trec["dram_bytes_per_launch"] if trec else None),
                       "traffic_source": ("profiles/traffic.json" if trec else "stale or missing"),
                       "kernel": job.kernel_note(),
