@@ -485,12 +485,55 @@ def run_reference(args, world, rank):
     }), flush=True)
 
 
+def run_torch_eager(args, world, rank, local):
+    """Context only: the per-clip definition composed from eager PyTorch ops
+    on the same GPU (power, dense projection, log10, clip max, clamp,
+    rescale), timed like the library call.  Not the reference arm."""
+    import torch
+
+    import workloads
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.WHISPER_STFT_B256
+    stft, W = workloads.stft_workload_inputs(w, device=dev)
+
+    def step():
+        mag = torch.view_as_real(stft).square().sum(-1)
+        mel = mag @ W.t()
+        ls = torch.log10(mel.clamp_min(1e-10))
+        hi = ls.amax(dim=(1, 2), keepdim=True)
+        return (torch.maximum(ls, hi - 8.0) + 4.0) / 4.0
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    achieved = w.canonical_bytes / (ms / 1e3) / 1e9
+    peak, peak_kind = _peaks()
+    print(json.dumps({"impl": "torch_eager", "metric": METRIC, "value": w.B / (ms / 1e3), "unit": "clips/s",
+                      "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                      "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+                      "config": {"workload": w.name, "B": w.B, "F": w.F, "NF": w.NF, "NM": w.NM},
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                                   "frac": achieved / peak, "peak_kind": peak_kind}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--impl", choices=["ours", "reference", "torch_eager"], default="ours",
+                    help="ours (the library), reference (the CPU oracle), or torch_eager (context: the "
+                         "definition as eager PyTorch ops on the GPU)")
     ap.add_argument("--reference-clips", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
@@ -506,6 +549,9 @@ def main():
     world, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.impl == "torch_eager":
+        run_torch_eager(args, world, rank, local)
         return
     run_ours(args, world, rank, local)
 
