@@ -106,6 +106,20 @@ def test_variants_agree(lm, oracle_mod, variant, monkeypatch):
     _compare(*_run(lm, oracle_mod, stft, W))
 
 
+def test_filters_only_four_byte_aligned(lm, oracle_mod):
+    # A filter view 4 bytes into its allocation: the prologue's scalar path.
+    stft, W = workloads.stft_inputs(3, 301, 201, 128, seed=31)
+    Wbig = torch.zeros(W.numel() + 1)
+    Wbig[1:] = W.flatten()
+    Wv = Wbig[1:].view(W.shape)
+    dev = torch.device("cuda")
+    Wd = torch.zeros(W.numel() + 1, device=dev)
+    Wd[1:] = W.flatten().to(dev)
+    out = lm.log_mel_from_stft(stft.to(dev), Wd[1:].view(W.shape))
+    ref = oracle_mod.log_mel_from_stft(stft.numpy(), Wv.numpy())
+    _compare(out.cpu().numpy(), ref)
+
+
 def test_deterministic_and_stream_aware(lm):
     stft, W = workloads.stft_inputs(4, 500, 201, 80, seed=2, device="cuda")
     a = lm.log_mel_from_stft(stft, W)

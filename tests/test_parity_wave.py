@@ -177,3 +177,27 @@ def test_full_torchaudio_argument_set(lm, oracle_mod, win_length, pad, normalize
     p = workloads.wave_pcm16(1, 4000, seed=pad)
     _run(lm, oracle_mod, p, 16000, n_fft, n_fft // 4, 48, mel_scale="slaney", norm="slaney", out_dtype="f16",
          win_length=win_length, pad=pad, normalized=normalized, center=center, pad_mode=pad_mode)
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "i16"])
+def test_odd_hop_and_odd_span_head(lm, oracle_mod, in_dtype):
+    # An odd hop makes every other frame's sample pairs unaligned in the span
+    # buffer (the scalar framing path); an odd leading pad offsets the whole
+    # span by one sample.
+    x = workloads.wave_sines(2, 9000, 16000, seed=41) if in_dtype == "f32" else workloads.wave_pcm16(2, 9000, seed=41)
+    _run(lm, oracle_mod, x, 16000, 400, 161, 80, f_max=8000.0)
+    _run(lm, oracle_mod, x, 16000, 512, 127, 64, f_max=8000.0, pad=3)
+
+
+def test_repeat_calls_are_bitwise_identical(lm):
+    # Tiles are claimed dynamically; the result must not depend on which CTA
+    # computed which tile.
+    x = workloads.wave_sines(4, 48000, 16000, seed=3).cuda()
+    for log_mel in (False, True):
+        m = lm.MelSpectrogram(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0,
+                              log_mel=log_mel)
+        a = m(x)
+        b = m(x)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+        m.close()
