@@ -141,6 +141,45 @@ typedef struct lm_stft_launch_info {
 lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM,
                                         lm_stft_launch_info *info);
 
+/* ---- Pre-packed filters (the "flashmel" page, "How it works": triangular
+ * filters packed as start / width / weights) ----
+ *
+ * lm_log_mel_from_stft derives each band's support (first..last nonzero bin of
+ * its row of the dense matrix) and first weights on every call; at kernel
+ * start that costs a sweep of the whole matrix plus a second round of loads,
+ * several microseconds that dominate small batches.  A caller that reuses
+ * one filter matrix can pack it once and pass the pack:
+ *
+ *   lm_mel_filters_pack_size(NF, NM, &bytes)   bytes of device memory a pack
+ *                                              needs (LM_ERR_INVALID_ARG /
+ *                                              LM_ERR_UNSUPPORTED as for the
+ *                                              shapes of lm_log_mel_from_stft).
+ *   lm_mel_filters_pack(mel_filters, NF, NM, packed, bytes, stream)
+ *       enqueues on `stream` the packing of the dense [NM][NF] f32 matrix
+ *       (device, 4-byte aligned, read-only) into `packed` (device, caller
+ *       owned, 16-byte aligned, >= the size above): a header with the shape,
+ *       then {first bin, width} per band, then each band's first 8 weights
+ *       from its first bin (zero past the width).  Errors:
+ *       LM_ERR_INVALID_ARG (null), LM_ERR_MISALIGNED, LM_ERR_WORKSPACE (too
+ *       small), LM_ERR_CUDA.
+ *   lm_log_mel_from_stft_packed(stft, mel_filters, packed, out, ...)
+ *       the same computation, arguments and results as lm_log_mel_from_stft,
+ *       reading supports and first weights from `packed` (which must be made
+ *       from this mel_filters, and be complete in stream order; bands wider
+ *       than 8 bins still read the rest from mel_filters).  A pack whose
+ *       header does not match NF, NM is not used: the call falls back to the
+ *       dense matrix and sets bit 4 of the device error word
+ *       (lm_workspace_error).  Errors: as lm_log_mel_from_stft, plus
+ *       LM_ERR_INVALID_ARG for a null pack and LM_ERR_MISALIGNED for one not
+ *       16-byte aligned.
+ */
+lm_status lm_mel_filters_pack_size(int32_t NF, int32_t NM, size_t *bytes);
+lm_status lm_mel_filters_pack(const float *mel_filters, int32_t NF, int32_t NM, void *packed,
+                              size_t packed_bytes, lm_stream_t stream);
+lm_status lm_log_mel_from_stft_packed(const void *stft, const float *mel_filters, const void *packed,
+                                      float *out, int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                      void *workspace, size_t workspace_bytes, lm_stream_t stream);
+
 /* ---- Allocation-free variant (the source pages have no counterpart) ----
  *
  * Same computation, arguments and results as lm_log_mel_from_stft, without

@@ -13,7 +13,9 @@ missing or the tensors are not on a CUDA device.
 """
 from __future__ import annotations
 
+import collections
 import ctypes
+import weakref
 
 import torch
 
@@ -21,6 +23,7 @@ from . import _native
 from ._native import LogmelError
 
 __all__ = ["log_mel_from_stft", "log_mel_from_stft_workspace_size", "workspace_error", "LogmelError",
+           "pack_mel_filters",
            "describe_log_mel_from_stft", "MelSpectrogram", "mel_spectrogram", "library_path",
            "log_mel_from_stft_op", "mel_spectrogram_op"]
 
@@ -57,9 +60,69 @@ def log_mel_from_stft_workspace_size(B: int, F: int, NF: int, NM: int) -> int:
     return int(n.value)
 
 
+def pack_mel_filters(mel_filters: torch.Tensor, stream=None) -> torch.Tensor:
+    """Packs a [NM, NF] float32 CUDA filter matrix once (each band's first
+    nonzero bin, width and first 8 weights; lm_mel_filters_pack) so that
+    log_mel_from_stft calls with it skip the per-call derivation.  Returns the
+    pack as a uint8 CUDA tensor, filled in stream order."""
+    _require_cuda(mel_filters, "mel_filters")
+    if mel_filters.dtype != torch.float32 or mel_filters.dim() != 2:
+        raise ValueError("mel_filters must be a [NM, NF] float32 tensor")
+    NM, NF = mel_filters.shape
+    n = ctypes.c_size_t()
+    _native.check(_native.lib().lm_mel_filters_pack_size(NF, NM, ctypes.byref(n)), "lm_mel_filters_pack_size")
+    packed = torch.empty(n.value, dtype=torch.uint8, device=mel_filters.device)
+    _native.check(_native.lib().lm_mel_filters_pack(mel_filters.data_ptr(), NF, NM, packed.data_ptr(), n.value,
+                                                    _stream_handle(stream)), "lm_mel_filters_pack")
+    return packed
+
+
+# Packs made on behalf of callers, one per live filter tensor and version
+# (torch bumps a tensor's version on every in-place write, views included);
+# an entry goes when its tensor is freed.  Never filled during graph capture.
+_PACKS: collections.OrderedDict = collections.OrderedDict()
+_PACKS_MAX = 32
+_PACK_FINALIZERS: set = set()
+
+
+def _drop_packs(tid: int) -> None:
+    _PACK_FINALIZERS.discard(tid)
+    for k in [k for k in _PACKS if k[0] == tid]:
+        del _PACKS[k]
+
+
+def _cached_pack(mel_filters: torch.Tensor, stream) -> torch.Tensor:
+    if torch.cuda.is_current_stream_capturing():
+        return pack_mel_filters(mel_filters, stream)
+    try:
+        version = mel_filters._version
+    except RuntimeError:  # inference tensors keep no version counter: no cache
+        return None
+    tid = id(mel_filters)
+    key = (tid, version, mel_filters.data_ptr(), tuple(mel_filters.shape), mel_filters.device.index)
+    hit = _PACKS.get(key)
+    if hit is not None:
+        _PACKS.move_to_end(key)
+        return hit
+    for k in [k for k in _PACKS if k[0] == tid]:
+        del _PACKS[k]
+    packed = pack_mel_filters(mel_filters, stream)
+    _PACKS[key] = packed
+    if tid not in _PACK_FINALIZERS:
+        weakref.finalize(mel_filters, _drop_packs, tid)
+        _PACK_FINALIZERS.add(tid)
+    while len(_PACKS) > _PACKS_MAX:
+        _PACKS.popitem(last=False)
+    return packed
+
+
 def log_mel_from_stft(stft: torch.Tensor, mel_filters: torch.Tensor, out: torch.Tensor | None = None,
-                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """stft [B,F,NF] complex64, mel_filters [NM,NF] float32 -> [B,F,NM] float32."""
+                      workspace: torch.Tensor | None = None, stream=None, packed=None) -> torch.Tensor:
+    """stft [B,F,NF] complex64, mel_filters [NM,NF] float32 -> [B,F,NM] float32.
+
+    packed: None (default) packs mel_filters once per tensor version and
+    reuses the pack; a tensor from pack_mel_filters(mel_filters) uses that
+    pack; False derives supports and weights from the dense matrix every call."""
     _no_grad_inputs(stft, mel_filters)
     _require_cuda(stft, "stft")
     _require_cuda(mel_filters, "mel_filters")
@@ -78,11 +141,22 @@ def log_mel_from_stft(stft: torch.Tensor, mel_filters: torch.Tensor, out: torch.
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=stft.device)
     elif workspace.numel() * workspace.element_size() < ws_bytes:
         raise ValueError(f"workspace needs {ws_bytes} bytes")
-    rc = _native.lib().lm_log_mel_from_stft(stft.data_ptr(), mel_filters.data_ptr(), out.data_ptr(), B, F, NF,
-                                            NM, workspace.data_ptr(),
-                                            workspace.numel() * workspace.element_size(),
-                                            _stream_handle(stream))
-    _native.check(rc, "lm_log_mel_from_stft")
+    ws_len = workspace.numel() * workspace.element_size()
+    if packed is None:
+        packed = _cached_pack(mel_filters, stream)
+        if packed is None:
+            packed = False
+    if packed is False:
+        rc = _native.lib().lm_log_mel_from_stft(stft.data_ptr(), mel_filters.data_ptr(), out.data_ptr(), B, F,
+                                                NF, NM, workspace.data_ptr(), ws_len, _stream_handle(stream))
+        _native.check(rc, "lm_log_mel_from_stft")
+        return out
+    if not isinstance(packed, torch.Tensor) or not packed.is_cuda:
+        raise ValueError("packed must be None, False or a tensor from pack_mel_filters")
+    rc = _native.lib().lm_log_mel_from_stft_packed(stft.data_ptr(), mel_filters.data_ptr(), packed.data_ptr(),
+                                                   out.data_ptr(), B, F, NF, NM, workspace.data_ptr(), ws_len,
+                                                   _stream_handle(stream))
+    _native.check(rc, "lm_log_mel_from_stft_packed")
     return out
 
 

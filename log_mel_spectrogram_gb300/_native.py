@@ -72,6 +72,12 @@ def lib() -> ctypes.CDLL:
         L.lm_log_mel_from_stft.restype = ctypes.c_int
         L.lm_log_mel_from_stft_describe.argtypes = [i64, i64, i32, i32, ctypes.POINTER(StftLaunchInfo)]
         L.lm_log_mel_from_stft_describe.restype = ctypes.c_int
+        L.lm_mel_filters_pack_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
+        L.lm_mel_filters_pack_size.restype = ctypes.c_int
+        L.lm_mel_filters_pack.argtypes = [vp, i32, i32, vp, sz, vp]
+        L.lm_mel_filters_pack.restype = ctypes.c_int
+        L.lm_log_mel_from_stft_packed.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, sz, vp]
+        L.lm_log_mel_from_stft_packed.restype = ctypes.c_int
         L.lm_workspace_error.argtypes = [vp, sz, ctypes.POINTER(u32), vp]
         L.lm_workspace_error.restype = ctypes.c_int
         L.lm_mel_plan_create.argtypes = [ctypes.POINTER(MelParams), ctypes.POINTER(vp)]

@@ -49,7 +49,8 @@ size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM);
 // Validated launch; arguments as in lm_log_mel_from_stft.
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
                           int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
-                          cudaStream_t stream);
+                          cudaStream_t stream,
+                          const void *packed = nullptr);
 
 // Per-clip floor and rescale in place: out[b] = (max(out[b], hi_b - 8) + 4) / 4,
 // hi_b = the largest of the clip's tiles_per_clip order-preserving keys.

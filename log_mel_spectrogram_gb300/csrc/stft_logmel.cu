@@ -56,7 +56,7 @@ constexpr int kLag = 7;          // resident mode: steps a tile's log values wai
 constexpr int kResolveSteps = 8;  // steps the resolver polls together
 constexpr int kSlots = 32;       // ring of per-step handshake slots (> kLag + kMaxStages)
 constexpr int kMaxStages = 8;
-constexpr int kRegTaps = 8;      // filter taps held in registers per band
+constexpr int kRegTaps = 8;      // filter taps held in registers per band (packed filters assume 8)
 constexpr int kMaxBands = 512;
 constexpr int kMaxBins = 8193;
 constexpr int kStageTargetBytes = 39 * 1024;
@@ -82,6 +82,25 @@ struct StftArgs {
   uint32_t stage_stride;   // bytes per stage, multiple of 128
   uint32_t aux_offset;     // shared-memory offset of SmemAux (after the stages and the ring)
   uint64_t total_bytes;    // B * F * NF * 8
+  const int32_t *packed;   // packed filter supports and first taps (see PackLayout), or null
+};
+
+// Packed filters: header {magic, NF, NM, widest support}, then {first bin,
+// width} per band, then the first kRegTaps weights of each band's support
+// (zero past its width).  Built once by mel_filters_pack_kernel so that a
+// call's prologue is one memory round trip instead of a sweep of the dense
+// matrix followed by the tap loads.
+struct PackLayout {
+  static constexpr int32_t kMagic = 0x464d4c50;  // "PLMF"
+  static constexpr size_t kHeader = 16;
+  __host__ __device__ static size_t sw_offset() { return kHeader; }
+  // the taps start 16-byte aligned (they are read as float4)
+  __host__ __device__ static size_t taps_offset(int32_t NM) {
+    return kHeader + (8 * static_cast<size_t>(NM) + 15) / 16 * 16;
+  }
+  __host__ __device__ static size_t bytes(int32_t NM) {
+    return taps_offset(NM) + 4 * static_cast<size_t>(kRegTaps) * NM;  // a multiple of 16: kRegTaps = 8
+  }
 };
 
 struct SmemAux {
@@ -471,61 +490,94 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
   }
 
   // ---------------------------- consumers ----------------------------
-  // Support of each filter row: first and last nonzero bin.  All consumer
-  // threads sweep the dense matrix together with eight independent loads in
-  // flight each, folding nonzeros into shared minima and maxima
-  // (band_width holds the last nonzero bin until the final pass).
-  for (int n = threadIdx.x; n < a.NM; n += kConsumers) {
-    aux.band_start[n] = INT_MAX;
-    aux.band_width[n] = -1;
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  {
-    // 32-bit indices (NM * NF < 2^23): a 64-bit division here cost microseconds.
-    constexpr int U = 8;
-    const int total = a.NM * a.NF;
-    for (int i0 = threadIdx.x; i0 < total; i0 += U * kConsumers) {
-      float v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * kConsumers;
-        v[u] = i < total ? __ldg(a.filters + i) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (v[u] != 0.f) {
-          const int i = i0 + u * kConsumers;
-          const int r = i / a.NF;
-          atomicMin(&aux.band_start[r], i - r * a.NF);
-          atomicMax(&aux.band_width[r], i - r * a.NF);
-        }
-      }
-    }
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  for (int n = threadIdx.x; n < a.NM; n += kConsumers) {
-    const int first = aux.band_start[n], last = aux.band_width[n];
-    const int width = last >= 0 ? last - first + 1 : 0;
-    aux.band_start[n] = last >= 0 ? first : 0;
-    aux.band_width[n] = width;
-    atomicMax(&aux.max_width, width);
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-
   Band band;
   band.n = threadIdx.x % a.NM;
   band.fg = threadIdx.x / a.NM;
   band.active = band.fg < a.FG;
-  band.st = band.active ? aux.band_start[band.n] : 0;
-  band.wd = band.active ? aux.band_width[band.n] : 0;
-  band.wrow = a.filters + static_cast<int64_t>(band.n) * a.NF + band.st;
-#pragma unroll
-  for (int t = 0; t < kRegTaps; ++t) {
-    const float wt = (t < band.wd) ? __ldg(band.wrow + t) : 0.f;
-    band.w2[t] = make_float2(wt, wt);
+  int maxw;
+  // Packed filters that match this call: supports and first taps in one
+  // round of loads.  Anything else (no pack, or one made for another shape)
+  // derives them from the dense matrix; a mismatched pack is reported.
+  bool use_pack = a.packed != nullptr;
+  int4 hdr = make_int4(0, 0, 0, 0);
+  if (use_pack) {
+    hdr = __ldg(reinterpret_cast<const int4 *>(a.packed));
+    use_pack = hdr.x == PackLayout::kMagic && hdr.y == a.NF && hdr.z == a.NM;
+    if (!use_pack && threadIdx.x == 0) atomicOr(a.err, kErrBadPack);
   }
+  if (use_pack) {
+    const int2 *sw = reinterpret_cast<const int2 *>(reinterpret_cast<const char *>(a.packed) + PackLayout::sw_offset());
+    const float4 *tw = reinterpret_cast<const float4 *>(reinterpret_cast<const char *>(a.packed) +
+                                                        PackLayout::taps_offset(a.NM)) +
+                       static_cast<int64_t>(band.n) * (kRegTaps / 4);
+    const int2 v = __ldg(sw + band.n);
+    float wt[kRegTaps];
+#pragma unroll
+    for (int q = 0; q < kRegTaps / 4; ++q) {
+      const float4 t4 = __ldg(tw + q);
+      wt[4 * q] = t4.x;
+      wt[4 * q + 1] = t4.y;
+      wt[4 * q + 2] = t4.z;
+      wt[4 * q + 3] = t4.w;
+    }
+    maxw = hdr.w;
+    band.st = band.active ? v.x : 0;
+    band.wd = band.active ? v.y : 0;
+#pragma unroll
+    for (int t = 0; t < kRegTaps; ++t) band.w2[t] = band.active ? make_float2(wt[t], wt[t]) : make_float2(0.f, 0.f);
+  } else {
+    // Support of each filter row: first and last nonzero bin.  All consumer
+    // threads sweep the dense matrix together with eight independent loads in
+    // flight each, folding nonzeros into shared minima and maxima
+    // (band_width holds the last nonzero bin until the final pass).
+    for (int n = threadIdx.x; n < a.NM; n += kConsumers) {
+      aux.band_start[n] = INT_MAX;
+      aux.band_width[n] = -1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+    {
+      // 32-bit indices (NM * NF < 2^23): a 64-bit division here cost microseconds.
+      constexpr int U = 8;
+      const int total = a.NM * a.NF;
+      for (int i0 = threadIdx.x; i0 < total; i0 += U * kConsumers) {
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * kConsumers;
+          v[u] = i < total ? __ldg(a.filters + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (v[u] != 0.f) {
+            const int i = i0 + u * kConsumers;
+            const int r = i / a.NF;
+            atomicMin(&aux.band_start[r], i - r * a.NF);
+            atomicMax(&aux.band_width[r], i - r * a.NF);
+          }
+        }
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+    for (int n = threadIdx.x; n < a.NM; n += kConsumers) {
+      const int first = aux.band_start[n], last = aux.band_width[n];
+      const int width = last >= 0 ? last - first + 1 : 0;
+      aux.band_start[n] = last >= 0 ? first : 0;
+      aux.band_width[n] = width;
+      atomicMax(&aux.max_width, width);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+
+    maxw = aux.max_width;
+    band.st = band.active ? aux.band_start[band.n] : 0;
+    band.wd = band.active ? aux.band_width[band.n] : 0;
+#pragma unroll
+    for (int t = 0; t < kRegTaps; ++t) {
+      const float wt = (t < band.wd) ? __ldg(a.filters + static_cast<int64_t>(band.n) * a.NF + band.st + t) : 0.f;
+      band.w2[t] = make_float2(wt, wt);
+    }
+  }
+  band.wrow = a.filters + static_cast<int64_t>(band.n) * a.NF + band.st;
   float *ring = reinterpret_cast<float *>(smem + static_cast<size_t>(a.n_stages) * a.stage_stride);
-  const int maxw = aux.max_width;
   if (maxw <= 4)
     consume<FPT, 4, kResident, CW>(a, smem, aux, ring, my_tiles, band, lane);
   else if (maxw <= kRegTaps)
@@ -584,6 +636,43 @@ __global__ void __launch_bounds__(256) logmel_clamp_kernel(float *out, const uin
         o[i] = rescale(o[i], floor_v);
     }
   }
+}
+
+// Packs the dense [NM, NF] filter matrix: a warp per row finds the first
+// and last nonzero bin with ballots (as the kernel's own sweep defines the
+// support) and stores {first, width} and the first kRegTaps weights from
+// `first` (zero past the width).  The header is zeroed before launch; block 0
+// writes the shape and the magic, and every row folds its width into the
+// widest.
+__global__ void __launch_bounds__(256) mel_filters_pack_kernel(const float *filters, int32_t NF, int32_t NM,
+                                                               int32_t *packed) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    packed[0] = PackLayout::kMagic;
+    packed[1] = NF;
+    packed[2] = NM;
+  }
+  if (n >= NM) return;
+  const float *row = filters + static_cast<int64_t>(n) * NF;
+  int first = INT_MAX, last = -1;
+  for (int k0 = 0; k0 < NF; k0 += 32) {
+    const int k = k0 + lane;
+    const unsigned m = __ballot_sync(0xffffffffu, k < NF && row[k] != 0.f);
+    if (m) {
+      if (first == INT_MAX) first = k0 + __ffs(m) - 1;
+      last = k0 + 31 - __clz(m);
+    }
+  }
+  const int st = last >= 0 ? first : 0;
+  const int wd = last >= 0 ? last - first + 1 : 0;
+  int2 *sw = reinterpret_cast<int2 *>(reinterpret_cast<char *>(packed) + PackLayout::sw_offset());
+  float *taps = reinterpret_cast<float *>(reinterpret_cast<char *>(packed) + PackLayout::taps_offset(NM));
+  if (lane == 0) {
+    sw[n] = make_int2(st, wd);
+    atomicMax(&packed[3], wd);
+  }
+  if (lane < kRegTaps) taps[static_cast<int64_t>(n) * kRegTaps + lane] = lane < wd ? row[st + lane] : 0.f;
 }
 
 using KernelFn = void (*)(StftArgs);
@@ -725,7 +814,7 @@ size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM) {
 
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
                           int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const void *packed) {
   if (B < 0 || F < 0 || NF < 1 || NM < 1) return LM_ERR_INVALID_ARG;
   if (NF > kMaxBins || NM > kMaxBands) return LM_ERR_UNSUPPORTED;
   if (B == 0 || F == 0) return LM_OK;
@@ -735,6 +824,7 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   if ((reinterpret_cast<uintptr_t>(stft) & 15) || (reinterpret_cast<uintptr_t>(filters) & 3) ||
       (reinterpret_cast<uintptr_t>(out) & 3) || (reinterpret_cast<uintptr_t>(workspace) & 3))
     return LM_ERR_MISALIGNED;
+  if (packed && (reinterpret_cast<uintptr_t>(packed) & 15)) return LM_ERR_MISALIGNED;
   const size_t ws_needed = stft_workspace_bytes(B, F, NF, NM);
   if (workspace_bytes < ws_needed) return LM_ERR_WORKSPACE;
   {  // the output may not overlap either input
@@ -769,6 +859,7 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(F) * static_cast<uint64_t>(NF) * 8ull;
   a.grid_q = ln.grid / ln.tpc;
   a.grid_r = static_cast<int32_t>(ln.grid % ln.tpc);
+  a.packed = static_cast<const int32_t *>(packed);
 
   LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, ws_needed, stream));
 
@@ -846,7 +937,7 @@ extern "C" lm_status lm_log_mel_from_stft(const void *stft, const float *mel_fil
                                           int64_t F, int32_t NF, int32_t NM, void *workspace,
                                           size_t workspace_bytes, lm_stream_t stream) {
   return lm::stft_logmel_run(stft, mel_filters, out, B, F, NF, NM, workspace, workspace_bytes,
-                             reinterpret_cast<cudaStream_t>(stream));
+                             reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 extern "C" lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM,
@@ -890,5 +981,37 @@ extern "C" lm_status lm_log_mel_from_stft_noalloc(const void *stft, const float 
   }
   // stft_logmel_run clears the scratch it uses before launching.
   return lm::stft_logmel_run(stft, mel_filters, out, B, F, NF, NM, scratch, LM_NOALLOC_SCRATCH_BYTES,
-                             reinterpret_cast<cudaStream_t>(stream));
+                             reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" lm_status lm_mel_filters_pack_size(int32_t NF, int32_t NM, size_t *bytes) {
+  if (!bytes) return LM_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (NF < 1 || NM < 1) return LM_ERR_INVALID_ARG;
+  if (NF > lm::kMaxBins || NM > lm::kMaxBands) return LM_ERR_UNSUPPORTED;
+  *bytes = lm::PackLayout::bytes(NM);
+  return LM_OK;
+}
+
+extern "C" lm_status lm_mel_filters_pack(const float *mel_filters, int32_t NF, int32_t NM, void *packed,
+                                         size_t packed_bytes, lm_stream_t stream) {
+  size_t need = 0;
+  if (lm_status st = lm_mel_filters_pack_size(NF, NM, &need); st != LM_OK) return st;
+  if (!mel_filters || !packed) return LM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(mel_filters) & 3) || (reinterpret_cast<uintptr_t>(packed) & 15))
+    return LM_ERR_MISALIGNED;
+  if (packed_bytes < need) return LM_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LM_CUDA_TRY(cudaMemsetAsync(packed, 0, lm::PackLayout::kHeader, s));
+  lm::mel_filters_pack_kernel<<<(NM + 7) / 8, 256, 0, s>>>(mel_filters, NF, NM, static_cast<int32_t *>(packed));
+  LM_CUDA_TRY(cudaGetLastError());
+  return LM_OK;
+}
+
+extern "C" lm_status lm_log_mel_from_stft_packed(const void *stft, const float *mel_filters, const void *packed,
+                                                 float *out, int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                                 void *workspace, size_t workspace_bytes, lm_stream_t stream) {
+  if (!packed) return LM_ERR_INVALID_ARG;
+  return lm::stft_logmel_run(stft, mel_filters, out, B, F, NF, NM, workspace, workspace_bytes,
+                             reinterpret_cast<cudaStream_t>(stream), packed);
 }

@@ -94,3 +94,22 @@ def test_mel_plan_validation(L):
     p = _native.MelParams(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, center=1,
                           power=2.0)
     assert L.lm_mel_plan_create(ctypes.byref(p), None) == 1
+
+
+def test_filter_pack_validation_needs_no_gpu(L):
+    n = ctypes.c_size_t()
+    assert L.lm_mel_filters_pack_size(201, 128, ctypes.byref(n)) == 0
+    # header, {first, width} per band (padded to 16 bytes), 8 weights per band
+    assert n.value == 16 + 1024 + 32 * 128 and n.value % 16 == 0
+    assert L.lm_mel_filters_pack_size(201, 81, ctypes.byref(n)) == 0
+    assert n.value == 16 + 656 + 32 * 81
+    assert L.lm_mel_filters_pack_size(0, 80, ctypes.byref(n)) == 1
+    assert L.lm_mel_filters_pack_size(201, 600, ctypes.byref(n)) == 2
+    assert L.lm_mel_filters_pack(None, 201, 80, 0x10000, 1 << 20, None) == 1
+    assert L.lm_mel_filters_pack(0x20000, 201, 80, 0x10008, 1 << 20, None) == 3   # pack not 16-byte aligned
+    assert L.lm_mel_filters_pack(0x20000, 201, 80, 0x10000, 64, None) == 7        # pack too small
+    # the packed call validates like the dense one, plus a null or misaligned pack
+    assert L.lm_log_mel_from_stft_packed(0x10000, 0x20000, None, 0x30000000, 2, 3, 201, 80, 0x40000, 1 << 20,
+                                         None) == 1
+    assert L.lm_log_mel_from_stft_packed(0x10000, 0x20000, 0x50008, 0x30000000, 2, 3, 201, 80, 0x40000,
+                                         1 << 20, None) == 3

@@ -120,6 +120,51 @@ def test_filters_only_four_byte_aligned(lm, oracle_mod):
     _compare(out.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("shape", [(3, 301, 201, 128), (2, 100, 201, 81), (2, 50, 65, 7), (1, 40, 3, 2),
+                                   (2, 90, 201, 64)], ids=str)
+def test_packed_filters_match_dense(lm, oracle_mod, shape):
+    # Supports and first taps from a pack, from the per-call cache, or from
+    # the dense matrix: the same bits.  Odd NM exercises the pack's padding;
+    # the last case has dense random rows (every band wider than 8 taps).
+    B, F, NF, NM = shape
+    stft, W = workloads.stft_inputs(B, F, NF, NM, seed=60 + NM)
+    if NM == 64:
+        W = torch.rand(NM, NF, generator=torch.Generator().manual_seed(4))
+        W[5] = 0
+    dev = torch.device("cuda")
+    s, w = stft.to(dev), W.to(dev)
+    dense = lm.log_mel_from_stft(s, w, packed=False)
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(B, F, NF, NM), dtype=torch.uint8, device=dev)
+    explicit = lm.log_mel_from_stft(s, w, packed=lm.pack_mel_filters(w), workspace=ws)
+    assert lm.workspace_error(ws) == 0
+    cached = lm.log_mel_from_stft(s, w)
+    cached2 = lm.log_mel_from_stft(s, w)
+    assert torch.equal(dense, explicit) and torch.equal(dense, cached) and torch.equal(dense, cached2)
+    _compare(dense.cpu().numpy(), oracle_mod.log_mel_from_stft(stft.numpy(), W.numpy()))
+
+
+def test_pack_follows_in_place_filter_changes(lm, oracle_mod):
+    stft, W = workloads.stft_inputs(2, 120, 201, 80, seed=71)
+    s, w = stft.cuda(), W.cuda()
+    a = lm.log_mel_from_stft(s, w)
+    w.mul_(3.0)                        # bumps the tensor's version: a new pack
+    b = lm.log_mel_from_stft(s, w)
+    _compare(b.cpu().numpy(), oracle_mod.log_mel_from_stft(stft.numpy(), (W * 3.0).numpy()))
+    assert not torch.equal(a, b)
+
+
+def test_mismatched_pack_is_reported_and_not_used(lm, oracle_mod):
+    stft, W = workloads.stft_inputs(2, 100, 201, 80, seed=72)
+    _, W2 = workloads.stft_inputs(1, 1, 201, 64, seed=73)
+    dev = torch.device("cuda")
+    s, w = stft.to(dev), W.to(dev)
+    wrong = lm.pack_mel_filters(W2.to(dev))              # a pack made for 64 bands
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(2, 100, 201, 80), dtype=torch.uint8, device=dev)
+    out = lm.log_mel_from_stft(s, w, packed=wrong, workspace=ws)
+    assert lm.workspace_error(ws) == 4                  # bit 4: the pack did not match; dense matrix used
+    _compare(out.cpu().numpy(), oracle_mod.log_mel_from_stft(stft.numpy(), W.numpy()))
+
+
 def test_deterministic_and_stream_aware(lm):
     stft, W = workloads.stft_inputs(4, 500, 201, 80, seed=2, device="cuda")
     a = lm.log_mel_from_stft(stft, W)
