@@ -300,19 +300,22 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
   const int64_t my_tiles = (a.n_tiles - 1 - blockIdx.x) / G + 1;
   const int S = a.n_stages;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&aux.full[s], 1);
-      mbar_init(&aux.empty[s], CW);
+  // Warp 0 initialises the barriers, a lane per handshake slot (kSlots =
+  // 32), each lane fencing its own initialisations.
+  static_assert(kSlots == 32 && kMaxStages <= 32, "one lane per slot");
+  if (warp == 0) {
+    if (lane < S) {
+      mbar_init(&aux.full[lane], 1);
+      mbar_init(&aux.empty[lane], CW);
     }
-    for (int r = 0; r < kSlots; ++r) {
-      mbar_init(&aux.tmax_bar[r], CW);
-      mbar_init(&aux.pub_bar[r], 1);
-      mbar_init(&aux.hi_bar[r], 1);
-      aux.tmax_key[r] = 0u;
+    mbar_init(&aux.tmax_bar[lane], CW);
+    mbar_init(&aux.pub_bar[lane], 1);
+    mbar_init(&aux.hi_bar[lane], 1);
+    aux.tmax_key[lane] = 0u;
+    if (lane == 0) {
+      aux.max_width = 0;
+      aux.abort_flag = 0;
     }
-    aux.max_width = 0;
-    aux.abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
