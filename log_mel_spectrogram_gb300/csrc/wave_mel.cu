@@ -112,6 +112,12 @@ struct WaveCfg {
   // twiddles do and the window, untangle twiddles and filterbank are read
   // through L1 from global memory.
   static constexpr bool kSmallTables = NFFT <= 4096;
+  // CTAs per SM that shared memory allows at these sizes; registers are
+  // capped to match so they do not lower the occupancy further.  400 points
+  // gets no minimum (0): the compiler's own choice there is 64 registers,
+  // while an explicit 4 made it spill and 1 let it take 104.
+  static constexpr int kMinBlocks = NFFT == 400 ? 0 : (NFFT <= 512 ? 4 : (NFFT <= 1024 ? 2 : 1));
+  static constexpr bool kFuseFirst = (M & (M - 1)) == 0;
   // The power tile (TF rows of NFP floats) lives in whichever FFT buffer does
   // not hold the transform's result; it needs at most half of it.
   static constexpr bool kResultInB = fft::num_passes<M>() % 2 == 1;
@@ -147,7 +153,7 @@ size_t wave_smem_bytes(int n_mels, int wmax) {
 }
 
 template <int NFFT>
-__global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a) {
+__global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_mel_kernel(const WaveArgs a) {
   using C = WaveCfg<NFFT>;
   constexpr int M = C::M, TF = C::TF, NFP = C::NFP;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -266,11 +272,13 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
     // buffer (even head and hop): one 8-byte (f32) or 4-byte (i16) load per
     // complex point, the window as pairs too, compile-time trip count.
     const bool paired = staged && ((static_cast<int>(head) | a.hop) & 1) == 0;
-    if (paired) {
+    // Power-of-two sizes fuse the framing into the first FFT pass; at 400
+    // points the fused radix-5 pass measured slower than framing on its own.
+    const bool fused = paired && C::kFuseFirst;
+    if (paired && !fused) {
       // 32-bit shared addresses; thread idx handles point n of frame f.
       constexpr int ITEMS = TF * M;
       const uint32_t seg0 = smem_u32(segf) + static_cast<uint32_t>(head) * es;
-      // the window is in shared memory only with the small tables
       const uint32_t win0 = C::kSmallTables ? smem_u32(win) : 0u;
       const float2 *win_g = reinterpret_cast<const float2 *>(win);
       const uint32_t dst0 = smem_u32(bufA);
@@ -301,6 +309,56 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
           z = make_float2(x.x * w.x, x.y * w.y);
         }
         sts_f32x2(dst0 + 8u * static_cast<uint32_t>(C::L::at(idx)), z);
+      }
+    }
+    if constexpr (C::kFuseFirst) if (fused) {
+      // Framing fused into the first FFT pass (span P = 1, radix R0): the
+      // thread of butterfly i of frame f loads its R0 complex points
+      // n = i + j M/R0 straight from the span buffer (one 8-byte f32 or
+      // 4-byte i16 load per point), windows them, transforms and stores to
+      // bufB -- one shared-memory round trip and one barrier fewer.
+      constexpr int R0 = fft::next_radix<M, 1>();
+      constexpr int T = M / R0;
+      constexpr int ITEMS = TF * T;
+      const uint32_t seg0 = smem_u32(segf) + static_cast<uint32_t>(head) * es;
+      const uint32_t win0 = C::kSmallTables ? smem_u32(win) : 0u;  // the window is in shared memory only with the small tables
+      const float2 *win_g = reinterpret_cast<const float2 *>(win);
+      const uint32_t dst0 = smem_u32(bufB);
+      const bool i16 = a.in_i16 != 0;
+#pragma unroll 2
+      for (int r = 0; r < (ITEMS + kWaveThreads - 1) / kWaveThreads; ++r) {
+        const int g = static_cast<int>(threadIdx.x) + r * kWaveThreads;
+        if (ITEMS % kWaveThreads != 0 && g >= ITEMS) break;
+        const int f = g / T;
+        const int i = g - f * T;
+        float2 u[R0];
+#pragma unroll
+        for (int j = 0; j < R0; ++j) {
+          const int n = i + j * T;
+          u[j] = make_float2(0.f, 0.f);
+          if (f < nf) {
+            const uint32_t e = static_cast<uint32_t>(f * a.hop + 2 * n);  // sample offset from head, even
+            float2 x;
+            if (i16) {
+              const int v = lds_s32(seg0 + 2u * e);
+              x = make_float2(static_cast<float>(static_cast<int16_t>(v & 0xffff)) * (1.0f / 32768.0f),
+                              static_cast<float>(static_cast<int16_t>(v >> 16)) * (1.0f / 32768.0f));
+            } else {
+              x = lds_f32x2(seg0 + 4u * e);
+            }
+            float2 w;
+            if constexpr (C::kSmallTables) {
+              w = lds_f32x2(win0 + 8u * static_cast<uint32_t>(n));
+            } else {
+              w = win_g[n];
+            }
+            u[j] = make_float2(x.x * w.x, x.y * w.y);
+          }
+        }
+        fft::Dft<R0>::run(u);
+#pragma unroll
+        for (int l = 0; l < R0; ++l)
+          sts_f32x2(dst0 + 8u * static_cast<uint32_t>(C::L::at(f * M + i * R0 + l)), u[l]);
       }
     }
     for (int idx = paired ? TF * M : static_cast<int>(threadIdx.x); idx < TF * M; idx += blockDim.x) {
@@ -338,8 +396,18 @@ __global__ void __launch_bounds__(kWaveThreads) wave_mel_kernel(const WaveArgs a
     }
     __syncthreads();
 
-    // 2. N/2-point complex FFT of every frame
-    const bool in_b = fft::run<M, TF, kWaveThreads>(bufA, bufB, twm);
+    // 2. N/2-point complex FFT of every frame (its first pass already done
+    // for aligned staged tiles, whose result is then in bufB)
+    bool in_b;
+    if constexpr (C::kFuseFirst) {
+      if (fused) {
+        in_b = !fft::run<M, TF, kWaveThreads, fft::next_radix<M, 1>()>(bufB, bufA, twm);
+      } else {
+        in_b = fft::run<M, TF, kWaveThreads>(bufA, bufB, twm);
+      }
+    } else {
+      in_b = fft::run<M, TF, kWaveThreads>(bufA, bufB, twm);
+    }
     const float2 *Z = in_b ? bufB : bufA;  // == kResultInB; pw is the other buffer
 
     // 3. untangle the real spectrum and take |X|^power.  Bins k and M - k
