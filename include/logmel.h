@@ -193,8 +193,8 @@ lm_status lm_log_mel_from_stft_packed(const void *stft, const float *mel_filters
  * into the library; every GPU that loads the library holds that array until
  * the process exits.  The call allocates and frees nothing.
  *  - A problem needing more scratch than that (16 bytes plus 4 bytes per
- *    tile of frames; for NF = 201, NM = 128 a tile is 24 frames, so up to
- *    about 262,000 tiles, e.g. 256 clips of up to 24,552 frames) returns
+ *    tile of frames; for NF = 201, NM = 128 a tile is 25 frames, so up to
+ *    about 262,000 tiles, e.g. 256 clips of up to 25,575 frames) returns
  *    LM_ERR_WORKSPACE and enqueues nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call

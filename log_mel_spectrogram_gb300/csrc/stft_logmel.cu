@@ -59,7 +59,7 @@ constexpr int kMaxStages = 8;
 constexpr int kRegTaps = 8;      // filter taps held in registers per band (packed filters assume 8)
 constexpr int kMaxBands = 512;
 constexpr int kMaxBins = 8193;
-constexpr int kStageTargetBytes = 39 * 1024;
+constexpr int kStageTargetBytes = 41 * 1024;
 
 constexpr int threads_for(int cw) { return (cw + 3) * 32; }
 
@@ -697,7 +697,7 @@ KernelFn pick_fpt(int fpt, bool resident) {
 }
 
 KernelFn pick_kernel(int cw, int fpt, bool resident) {
-  (void)cw;
+  if (cw == 20) return fpt == 5 ? pick_variant<5, 20>(resident) : pick_variant<4, 20>(resident);
   return pick_fpt<16>(fpt, resident);
 }
 
@@ -710,9 +710,12 @@ struct TilePlan {
 };
 
 // Consumer warps CW, frame groups FG of NM threads, FPT frames per thread,
-// with a stage of roughly kStageTargetBytes.  Sixteen consumer warps: the
-// loop is latency-bound, and halving the warps (with twice the frames per
-// thread) measured 37% slower.
+// with a stage of at most about kStageTargetBytes.  Sixteen consumer warps,
+// or twenty where NM divides 640 and that gives a tile at least as tall with
+// 4 or 5 frames per thread (NM = 128: 5 x 5 = 25 frames against 4 x 6).  The
+// loop is latency-bound: twenty warps were 3% faster at NM = 128, and halving
+// the warps (with twice the frames per thread) was 37% slower.  A function
+// of the shape alone: the workspace size depends on it.
 void tile_height(int NF, int NM, int *CW, int *FG, int *FPT) {
   *CW = 16;
   const int fg_max = (*CW * 32) / NM;
@@ -728,6 +731,18 @@ void tile_height(int NF, int NM, int *CW, int *FG, int *FPT) {
   if (*FPT == 0) {
     *FPT = 1;
     *FG = std::max<int>(1, std::min<int64_t>(fg_max, kStageTargetBytes / frame_bytes));
+    return;
+  }
+  if (NM <= 640 && 640 % NM == 0) {
+    const int fg20 = 640 / NM;
+    for (int fpt : {5, 4}) {
+      if (static_cast<int64_t>(fg20) * fpt * frame_bytes <= kStageTargetBytes && fg20 * fpt >= *FG * *FPT) {
+        *CW = 20;
+        *FG = fg20;
+        *FPT = fpt;
+        return;
+      }
+    }
   }
 }
 

@@ -58,8 +58,8 @@ def test_status_strings(L):
 def test_workspace_size(L):
     n = ctypes.c_size_t()
     assert L.lm_log_mel_from_stft_workspace_size(256, 3000, 201, 128, ctypes.byref(n)) == 0
-    # header + one u32 per 24-frame tile (125 per clip)
-    assert n.value >= 16 + 4 * 256 * 125 and n.value % 256 == 0
+    # header + one u32 per 25-frame tile (120 per clip; 20 consumer warps x 5 frames)
+    assert n.value >= 16 + 4 * 256 * 120 and n.value % 256 == 0
     assert L.lm_log_mel_from_stft_workspace_size(-1, 10, 201, 128, ctypes.byref(n)) == 1
     assert L.lm_log_mel_from_stft_workspace_size(2, 10, 201, 600, ctypes.byref(n)) == 2
 
