@@ -280,6 +280,68 @@ lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wave, int32_t 
                              int64_t T, void *out, int32_t out_dtype, void *workspace,
                              size_t workspace_bytes, lm_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* 3. host buffers in and out (the source pages have no counterpart)        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The same computations as lm_log_mel_from_stft(_packed) and
+ * lm_mel_spectrogram, for inputs and results in host memory.  The library
+ * cuts the batch into chunks of whole clips and pipelines them through
+ * three staging slots in the workspace: the copy in of one chunk, the
+ * kernels of the previous one and the copy out of the one before run at
+ * the same time, on two internal streams of the library and `stream`.
+ * Results equal those of the device entry points bit for bit (clips are
+ * independent; the per-clip maximum never crosses a chunk).
+ *
+ *   stft_host / wave_host  host, laid out as the device entry point's input.
+ *   out_host               host, laid out as the device entry point's output;
+ *                          must not overlap the input.
+ *                          Both should be page-locked (cudaHostAlloc or
+ *                          cudaHostRegister) for the copies to overlap;
+ *                          pageable memory gives the same results, with the
+ *                          copies serialised and the call blocking the host.
+ *   mel_filters, packed    device, as for lm_log_mel_from_stft_packed;
+ *                          packed may be NULL (dense filters).
+ *   chunk_clips            clips per chunk; 0 = the library's choice: whole
+ *                          clips filling about 32 MB of input, and at most a
+ *                          third of the batch (rounded up).
+ *   workspace              device, 256-byte aligned, >= the matching
+ *                          *_host_workspace_size (a 256-byte header whose
+ *                          first u32 is the device error word of every
+ *                          chunk, the operation's workspace for one chunk,
+ *                          then three input and three output slots).
+ *   stream                 the call is ordered on it: the copy streams
+ *                          start after its earlier work, and it waits for
+ *                          the last copy out.  out_host is complete once
+ *                          `stream` reaches that point (e.g. after
+ *                          cudaStreamSynchronize(stream)).
+ *
+ * The first call on a device, and each further call that overlaps in time
+ * with the others, creates two streams and twelve events that the library
+ * keeps for reuse until the process exits; no memory is allocated.
+ *
+ * Errors: as the device entry points, plus LM_ERR_INVALID_ARG when the host
+ * buffers overlap, and LM_ERR_UNSUPPORTED when `stream` is capturing a
+ * CUDA graph (the pipeline is not capturable).  Argument errors are found
+ * before anything is enqueued; lm_workspace_error reads the error word.
+ * Calls that overlap in time need distinct workspaces.
+ */
+lm_status lm_log_mel_from_stft_host_workspace_size(int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                                   int64_t chunk_clips, size_t *bytes);
+lm_status lm_log_mel_from_stft_host(const void *stft_host, const float *mel_filters, const void *packed,
+                                    float *out_host, int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                    int64_t chunk_clips, void *workspace, size_t workspace_bytes,
+                                    lm_stream_t stream);
+
+lm_status lm_mel_spectrogram_host_workspace_size(const lm_mel_plan *plan, int64_t B, int64_t T,
+                                                 int32_t in_dtype, int32_t out_dtype, int64_t chunk_clips,
+                                                 size_t *bytes);
+lm_status lm_mel_spectrogram_host(const lm_mel_plan *plan, const void *wave_host, int32_t in_dtype,
+                                  int64_t B, int64_t T, void *out_host, int32_t out_dtype,
+                                  int64_t chunk_clips, void *workspace, size_t workspace_bytes,
+                                  lm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

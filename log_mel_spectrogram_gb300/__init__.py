@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import collections
 import ctypes
+import threading
 import weakref
 
 import torch
@@ -23,7 +24,7 @@ from . import _native
 from ._native import LogmelError
 
 __all__ = ["log_mel_from_stft", "log_mel_from_stft_workspace_size", "workspace_error", "LogmelError",
-           "pack_mel_filters",
+           "pack_mel_filters", "log_mel_from_stft_host", "log_mel_from_stft_host_workspace_size",
            "describe_log_mel_from_stft", "MelSpectrogram", "mel_spectrogram", "library_path",
            "log_mel_from_stft_op", "mel_spectrogram_op"]
 
@@ -83,12 +84,14 @@ def pack_mel_filters(mel_filters: torch.Tensor, stream=None) -> torch.Tensor:
 _PACKS: collections.OrderedDict = collections.OrderedDict()
 _PACKS_MAX = 32
 _PACK_FINALIZERS: set = set()
+_PACKS_LOCK = threading.RLock()  # host threads may call concurrently
 
 
 def _drop_packs(tid: int) -> None:
-    _PACK_FINALIZERS.discard(tid)
-    for k in [k for k in _PACKS if k[0] == tid]:
-        del _PACKS[k]
+    with _PACKS_LOCK:
+        _PACK_FINALIZERS.discard(tid)
+        for k in [k for k in _PACKS if k[0] == tid]:
+            del _PACKS[k]
 
 
 def _cached_pack(mel_filters: torch.Tensor, stream) -> torch.Tensor:
@@ -100,19 +103,20 @@ def _cached_pack(mel_filters: torch.Tensor, stream) -> torch.Tensor:
         return None
     tid = id(mel_filters)
     key = (tid, version, mel_filters.data_ptr(), tuple(mel_filters.shape), mel_filters.device.index)
-    hit = _PACKS.get(key)
-    if hit is not None:
-        _PACKS.move_to_end(key)
-        return hit
-    for k in [k for k in _PACKS if k[0] == tid]:
-        del _PACKS[k]
-    packed = pack_mel_filters(mel_filters, stream)
-    _PACKS[key] = packed
-    if tid not in _PACK_FINALIZERS:
-        weakref.finalize(mel_filters, _drop_packs, tid)
-        _PACK_FINALIZERS.add(tid)
-    while len(_PACKS) > _PACKS_MAX:
-        _PACKS.popitem(last=False)
+    with _PACKS_LOCK:
+        hit = _PACKS.get(key)
+        if hit is not None:
+            _PACKS.move_to_end(key)
+            return hit
+        for k in [k for k in _PACKS if k[0] == tid]:
+            del _PACKS[k]
+        packed = pack_mel_filters(mel_filters, stream)
+        _PACKS[key] = packed
+        if tid not in _PACK_FINALIZERS:
+            weakref.finalize(mel_filters, _drop_packs, tid)
+            _PACK_FINALIZERS.add(tid)
+        while len(_PACKS) > _PACKS_MAX:
+            _PACKS.popitem(last=False)
     return packed
 
 
@@ -157,6 +161,72 @@ def log_mel_from_stft(stft: torch.Tensor, mel_filters: torch.Tensor, out: torch.
                                                    out.data_ptr(), B, F, NF, NM, workspace.data_ptr(), ws_len,
                                                    _stream_handle(stream))
     _native.check(rc, "lm_log_mel_from_stft_packed")
+    return out
+
+
+def _require_host(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _host_output(shape, dtype, like: torch.Tensor, out: torch.Tensor | None) -> torch.Tensor:
+    if out is None:
+        return torch.empty(shape, dtype=dtype, pin_memory=like.is_pinned())
+    _require_host(out, "out")
+    if tuple(out.shape) != tuple(shape) or out.dtype != dtype:
+        raise ValueError(f"out must be a contiguous {tuple(shape)} {dtype} CPU tensor")
+    return out
+
+
+def log_mel_from_stft_host_workspace_size(B: int, F: int, NF: int, NM: int, chunk_clips: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _native.check(_native.lib().lm_log_mel_from_stft_host_workspace_size(int(B), int(F), int(NF), int(NM),
+                                                                         int(chunk_clips), ctypes.byref(n)),
+                  "lm_log_mel_from_stft_host_workspace_size")
+    return int(n.value)
+
+
+def log_mel_from_stft_host(stft: torch.Tensor, mel_filters: torch.Tensor, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None, packed=None, chunk_clips: int = 0,
+                           synchronize: bool = True) -> torch.Tensor:
+    """log_mel_from_stft for a batch in host memory: stft [B,F,NF] complex64
+    on the CPU (pinned, for the copies to overlap the kernels), mel_filters
+    [NM,NF] float32 on the GPU that computes -> [B,F,NM] float32 on the CPU.
+
+    The library pipelines chunks of whole clips through device staging slots
+    (lm_log_mel_from_stft_host).  With synchronize=False the result is
+    complete only once the stream reaches the end of the call's work."""
+    _no_grad_inputs(stft, mel_filters)
+    _require_host(stft, "stft")
+    _require_cuda(mel_filters, "mel_filters")
+    if stft.dtype != torch.complex64 or stft.dim() != 3:
+        raise ValueError("stft must be a [B, F, NF] complex64 tensor")
+    if mel_filters.dtype != torch.float32 or mel_filters.dim() != 2 or mel_filters.shape[1] != stft.shape[2]:
+        raise ValueError("mel_filters must be a [NM, NF] float32 tensor")
+    B, F, NF = stft.shape
+    NM = mel_filters.shape[0]
+    out = _host_output((B, F, NM), torch.float32, stft, out)
+    with torch.cuda.device(mel_filters.device):
+        ws_bytes = log_mel_from_stft_host_workspace_size(B, F, NF, NM, chunk_clips)
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=mel_filters.device)
+        elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < ws_bytes:
+            raise ValueError(f"workspace must be a CUDA tensor of at least {ws_bytes} bytes")
+        if packed is None:
+            packed = _cached_pack(mel_filters, stream)
+        if packed is False:
+            packed = None
+        if packed is not None and (not isinstance(packed, torch.Tensor) or not packed.is_cuda):
+            raise ValueError("packed must be None, False or a tensor from pack_mel_filters")
+        rc = _native.lib().lm_log_mel_from_stft_host(
+            stft.data_ptr(), mel_filters.data_ptr(), packed.data_ptr() if packed is not None else None,
+            out.data_ptr(), B, F, NF, NM, int(chunk_clips), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        _native.check(rc, "lm_log_mel_from_stft_host")
+        if synchronize:
+            (stream or torch.cuda.current_stream()).synchronize()
     return out
 
 
@@ -252,6 +322,50 @@ class MelSpectrogram:
                                                   workspace.numel() * workspace.element_size(),
                                                   _stream_handle(stream))
             _native.check(rc, "lm_mel_spectrogram")
+        return out.reshape(*lead, self.n_mels, nfr.value)
+
+    def host(self, wave: torch.Tensor, device=None, out: torch.Tensor | None = None,
+             workspace: torch.Tensor | None = None, stream=None, chunk_clips: int = 0,
+             synchronize: bool = True) -> torch.Tensor:
+        """The same transform for waveforms in host memory (pinned, for the
+        copies to overlap the kernels), computed on `device` (default: the
+        current CUDA device) and returned in host memory
+        (lm_mel_spectrogram_host).  With synchronize=False the result is
+        complete only once the stream reaches the end of the call's work."""
+        _no_grad_inputs(wave)
+        _require_host(wave, "wave")
+        if wave.dtype == torch.int16:
+            in_code = _native.DTYPES["i16"]
+        elif wave.dtype == torch.float32:
+            in_code = _native.DTYPES["f32"]
+        else:
+            raise ValueError("wave must be float32 or int16")
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        lead = wave.shape[:-1]
+        T = wave.shape[-1]
+        w2 = wave.reshape(-1, T)
+        B = w2.shape[0]
+        with torch.cuda.device(dev):
+            plan = self._plan(dev)
+            nfr = ctypes.c_int64()
+            _native.check(_native.lib().lm_mel_n_frames(plan, T, ctypes.byref(nfr)), "lm_mel_n_frames")
+            out = _host_output((B, self.n_mels, nfr.value), self.dtype, wave, out)
+            out_code = _native.DTYPES["f16" if self.dtype == torch.float16 else "f32"]
+            need = ctypes.c_size_t()
+            _native.check(_native.lib().lm_mel_spectrogram_host_workspace_size(
+                plan, B, T, in_code, out_code, int(chunk_clips), ctypes.byref(need)),
+                "lm_mel_spectrogram_host_workspace_size")
+            if workspace is None:
+                workspace = torch.empty(need.value, dtype=torch.uint8, device=dev)
+            elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need.value:
+                raise ValueError(f"workspace must be a CUDA tensor of at least {need.value} bytes")
+            rc = _native.lib().lm_mel_spectrogram_host(plan, w2.data_ptr(), in_code, B, T, out.data_ptr(), out_code,
+                                                       int(chunk_clips), workspace.data_ptr(),
+                                                       workspace.numel() * workspace.element_size(),
+                                                       _stream_handle(stream))
+            _native.check(rc, "lm_mel_spectrogram_host")
+            if synchronize:
+                (stream or torch.cuda.current_stream()).synchronize()
         return out.reshape(*lead, self.n_mels, nfr.value)
 
     def close(self) -> None:

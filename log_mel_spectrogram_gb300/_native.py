@@ -90,6 +90,14 @@ def lib() -> ctypes.CDLL:
         L.lm_mel_workspace_size.restype = ctypes.c_int
         L.lm_mel_spectrogram.argtypes = [vp, vp, i32, i64, i64, vp, i32, vp, sz, vp]
         L.lm_mel_spectrogram.restype = ctypes.c_int
+        L.lm_log_mel_from_stft_host_workspace_size.argtypes = [i64, i64, i32, i32, i64, ctypes.POINTER(sz)]
+        L.lm_log_mel_from_stft_host_workspace_size.restype = ctypes.c_int
+        L.lm_log_mel_from_stft_host.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i64, vp, sz, vp]
+        L.lm_log_mel_from_stft_host.restype = ctypes.c_int
+        L.lm_mel_spectrogram_host_workspace_size.argtypes = [vp, i64, i64, i32, i32, i64, ctypes.POINTER(sz)]
+        L.lm_mel_spectrogram_host_workspace_size.restype = ctypes.c_int
+        L.lm_mel_spectrogram_host.argtypes = [vp, vp, i32, i64, i64, vp, i32, i64, vp, sz, vp]
+        L.lm_mel_spectrogram_host.restype = ctypes.c_int
         _lib = L
         return _lib
 

@@ -46,11 +46,13 @@ const char *env_or(const char *name, const char *fallback);
 // Workspace bytes of lm_log_mel_from_stft for this shape.
 size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM);
 
-// Validated launch; arguments as in lm_log_mel_from_stft.
+// Validated launch; arguments as in lm_log_mel_from_stft.  `err_word`, when
+// set, receives the kernel's error bits instead of the workspace header (a
+// device u32 the caller clears).
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
                           int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
                           cudaStream_t stream,
-                          const void *packed = nullptr);
+                          const void *packed = nullptr, uint32_t *err_word = nullptr);
 
 // Per-clip floor and rescale in place: out[b] = (max(out[b], hi_b - 8) + 4) / 4,
 // hi_b = the largest of the clip's tiles_per_clip order-preserving keys.
@@ -58,5 +60,20 @@ lm_status launch_clip_clamp(float *out, const uint32_t *tile_key, int64_t B, int
                             int32_t tiles_per_clip, cudaStream_t stream);
 
 lm_status stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM, lm_stft_launch_info *info);
+
+// --- mel_spectrogram ----------------------------------------------------------
+
+// Argument rules of lm_mel_spectrogram that need no pointers.
+lm_status mel_spectrogram_check(const lm_mel_plan *plan, int32_t in_dtype, int64_t B, int64_t T,
+                                int32_t out_dtype);
+
+// The plan's number of mel bands.
+lm_status mel_plan_n_mels(const lm_mel_plan *plan, int32_t *n_mels);
+
+// Validated launch; arguments as in lm_mel_spectrogram, plus `err_word` as
+// for stft_logmel_run.
+lm_status mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int32_t in_dtype, int64_t B,
+                              int64_t T, void *out, int32_t out_dtype, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream, uint32_t *err_word = nullptr);
 
 }  // namespace lm

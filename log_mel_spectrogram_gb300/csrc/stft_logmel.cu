@@ -832,7 +832,7 @@ size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM) {
 
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
                           int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
-                          cudaStream_t stream, const void *packed) {
+                          cudaStream_t stream, const void *packed, uint32_t *err_word) {
   if (B < 0 || F < 0 || NF < 1 || NM < 1) return LM_ERR_INVALID_ARG;
   if (NF > kMaxBins || NM > kMaxBands) return LM_ERR_UNSUPPORTED;
   if (B == 0 || F == 0) return LM_OK;
@@ -860,7 +860,7 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   a.stft = static_cast<const float2 *>(stft);
   a.filters = filters;
   a.out = out;
-  a.err = static_cast<uint32_t *>(workspace);
+  a.err = err_word ? err_word : static_cast<uint32_t *>(workspace);
   a.tile_key = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + tile_key_offset());
   a.B = B;
   a.F = F;

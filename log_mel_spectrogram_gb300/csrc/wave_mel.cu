@@ -756,9 +756,14 @@ extern "C" lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, i
   return LM_OK;
 }
 
-extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wave, int32_t in_dtype, int64_t B,
-                                        int64_t T, void *out, int32_t out_dtype, void *workspace,
-                                        size_t workspace_bytes, lm_stream_t stream) {
+lm_status lm::mel_plan_n_mels(const lm_mel_plan *plan, int32_t *n_mels) {
+  if (!plan || !n_mels) return LM_ERR_INVALID_ARG;
+  *n_mels = plan->p.n_mels;
+  return LM_OK;
+}
+
+lm_status lm::mel_spectrogram_check(const lm_mel_plan *plan, int32_t in_dtype, int64_t B, int64_t T,
+                                    int32_t out_dtype) {
   if (!plan || B < 0 || T < 0) return LM_ERR_INVALID_ARG;
   if (in_dtype != LM_F32 && in_dtype != LM_I16) return LM_ERR_UNSUPPORTED;
   if (out_dtype != LM_F32 && out_dtype != LM_F16) return LM_ERR_UNSUPPORTED;
@@ -769,6 +774,16 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   if (T < 1 || nfr < 1) return LM_ERR_INVALID_ARG;
   if (p.center && p.pad_mode == LM_PAD_REFLECT && T + 2 * static_cast<int64_t>(p.pad) <= p.n_fft / 2)
     return LM_ERR_INVALID_ARG;
+  return LM_OK;
+}
+
+lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int32_t in_dtype, int64_t B,
+                                  int64_t T, void *out, int32_t out_dtype, void *workspace,
+                                  size_t workspace_bytes, cudaStream_t stream, uint32_t *err_word) {
+  if (lm_status st = mel_spectrogram_check(plan, in_dtype, B, T, out_dtype); st != LM_OK) return st;
+  if (B == 0) return LM_OK;
+  const lm_mel_params &p = plan->p;
+  const int64_t nfr = lm::frames_for(p, T);
   if (!wave || !out || !workspace) return workspace ? LM_ERR_INVALID_ARG : LM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(wave) & 3) || (reinterpret_cast<uintptr_t>(out) & 3) ||
       (reinterpret_cast<uintptr_t>(workspace) & 3))
@@ -834,7 +849,7 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   a.fw = plan->fw;
   a.tables = plan->tables;
   a.tables_bytes = plan->tables_bytes;
-  a.err = static_cast<uint32_t *>(workspace);
+  a.err = err_word ? err_word : static_cast<uint32_t *>(workspace);
   a.next_tile = static_cast<uint32_t *>(workspace) + 1;
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(T) * esize;
   a.seg_offset = static_cast<uint32_t>(seg_offset);
@@ -843,7 +858,7 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
   const int64_t n_tiles = B * a.tiles_per_clip;
   if (n_tiles > INT32_MAX / 2) return LM_ERR_UNSUPPORTED;  // tile indices and the counter are 32-bit
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_tiles, static_cast<int64_t>(di.sm_count) * per_sm));
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t s = stream;
   // Clears the device error word (and, for log plans, the tile slots).
   LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, a.log_mel ? need : lm::kWorkspaceHeaderBytes, s));
   kern<<<grid, lm::kWaveThreads, smem, s>>>(a);
@@ -855,4 +870,11 @@ extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wav
       return st;
   }
   return LM_OK;
+}
+
+extern "C" lm_status lm_mel_spectrogram(const lm_mel_plan *plan, const void *wave, int32_t in_dtype, int64_t B,
+                                        int64_t T, void *out, int32_t out_dtype, void *workspace,
+                                        size_t workspace_bytes, lm_stream_t stream) {
+  return lm::mel_spectrogram_run(plan, wave, in_dtype, B, T, out, out_dtype, workspace, workspace_bytes,
+                                 reinterpret_cast<cudaStream_t>(stream), nullptr);
 }

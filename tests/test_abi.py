@@ -113,3 +113,54 @@ def test_filter_pack_validation_needs_no_gpu(L):
                                          None) == 1
     assert L.lm_log_mel_from_stft_packed(0x10000, 0x20000, 0x50008, 0x30000000, 2, 3, 201, 80, 0x40000,
                                          1 << 20, None) == 3
+
+
+def _host_ws(L, B, F, NF, NM, chunk=0):
+    n = ctypes.c_size_t()
+    st = L.lm_log_mel_from_stft_host_workspace_size(B, F, NF, NM, chunk, ctypes.byref(n))
+    return st, n.value
+
+
+def test_host_pipeline_workspace_size(L):
+    # default chunk: whole clips filling about 32 MB of input, here 6 Whisper clips
+    in_clip, out_clip = 3000 * 201 * 8, 3000 * 128 * 4
+    st, n = _host_ws(L, 256, 3000, 201, 128)
+    assert st == 0 and n % 256 == 0
+    assert n >= 3 * 6 * (in_clip + out_clip) and n < 3 * 7 * (in_clip + out_clip)
+    st, n1 = _host_ws(L, 256, 3000, 201, 128, 1)
+    assert st == 0 and 3 * (in_clip + out_clip) <= n1 < n
+    st, nb = _host_ws(L, 2, 3000, 201, 128, 64)   # a chunk never exceeds the batch
+    assert st == 0 and nb < n
+    # a small batch runs in at least three chunks: 8 clips -> 3 per chunk
+    st, n8 = _host_ws(L, 8, 3000, 201, 128)
+    _, n3 = _host_ws(L, 8, 3000, 201, 128, 3)
+    assert st == 0 and n8 == n3
+    assert _host_ws(L, -1, 10, 201, 128)[0] == 1
+    assert _host_ws(L, 2, 10, 201, 128, -1)[0] == 1
+    assert _host_ws(L, 2, 10, 201, 600)[0] == 2
+    assert L.lm_log_mel_from_stft_host_workspace_size(2, 10, 201, 128, 0, None) == 1
+    n = ctypes.c_size_t()
+    assert L.lm_mel_spectrogram_host_workspace_size(None, 2, 1000, 0, 0, 0, ctypes.byref(n)) == 1
+
+
+def _host_call(L, stft=0x10000, filt=0x20000, packed=None, out=0x30000000, B=2, F=3, NF=201, NM=80, chunk=0,
+               ws=0x40000, ws_bytes=1 << 26):
+    return L.lm_log_mel_from_stft_host(stft, filt, packed, out, B, F, NF, NM, chunk, ws, ws_bytes, None)
+
+
+def test_host_pipeline_validation_needs_no_gpu(L):
+    # rejected before any CUDA call: the pointers are never dereferenced
+    assert _host_call(L, B=-1) == 1
+    assert _host_call(L, NM=600) == 2
+    assert _host_call(L, chunk=-2) == 1
+    assert _host_call(L, stft=0) == 1
+    assert _host_call(L, out=0) == 1
+    assert _host_call(L, ws=0) == 7
+    assert _host_call(L, ws=0x40010) == 3        # workspace must be 256-byte aligned
+    assert _host_call(L, filt=0x20002) == 3
+    assert _host_call(L, packed=0x50008) == 3
+    assert _host_call(L, ws_bytes=1024) == 7
+    assert _host_call(L, out=0x10000 + 8) == 1   # host output overlapping the host input
+    assert _host_call(L, B=0) == 0
+    assert _host_call(L, F=0) == 0
+    assert L.lm_mel_spectrogram_host(None, 0x10000, 0, 2, 1000, 0x30000000, 0, 0, 0x40000, 1 << 26, None) == 1
