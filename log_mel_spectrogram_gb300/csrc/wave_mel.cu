@@ -55,8 +55,6 @@ struct lm_mel_plan {
 namespace lm {
 namespace {
 
-constexpr int kWaveThreads = 256;
-
 struct WaveArgs {
   const void *wave;
   void *out;
@@ -108,6 +106,12 @@ struct WaveCfg {
   // (more CTAs hide each other's barriers), and at 1024 four frames were 22%
   // slower.
   static constexpr int TF = NFFT <= 1024 ? 8 : (NFFT <= 4096 ? 2 : 1);
+  // Threads per CTA (a multiple of TF: the mel phase maps a thread to one
+  // frame of a band group).  256 with 8-frame tiles beat every other pairing
+  // tried at 400 points (160-640 threads, 8 or 16 frames: 50-79 us against
+  // 48) and at 1024 (128-512 threads, 4-16 frames: 101-129 us against 95).
+  static constexpr int NT = 256;
+  static_assert(NT % 32 == 0 && NT % TF == 0, "thread count");
   // Up to 4096 every table sits in shared memory; beyond, only the FFT
   // twiddles do and the window, untangle twiddles and filterbank are read
   // through L1 from global memory.
@@ -153,9 +157,9 @@ size_t wave_smem_bytes(int n_mels, int wmax) {
 }
 
 template <int NFFT>
-__global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_mel_kernel(const WaveArgs a) {
+__global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) wave_mel_kernel(const WaveArgs a) {
   using C = WaveCfg<NFFT>;
-  constexpr int M = C::M, TF = C::TF, NFP = C::NFP;
+  constexpr int M = C::M, TF = C::TF, NFP = C::NFP, NT = C::NT;
   extern __shared__ __align__(16) unsigned char smem[];
   float2 *bufA = reinterpret_cast<float2 *>(smem);
   float2 *bufB = bufA + C::BUF;
@@ -284,9 +288,9 @@ __global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_
       const uint32_t dst0 = smem_u32(bufA);
       const bool i16 = a.in_i16 != 0;
 #pragma unroll 4
-      for (int r = 0; r < (ITEMS + kWaveThreads - 1) / kWaveThreads; ++r) {
-        const int idx = static_cast<int>(threadIdx.x) + r * kWaveThreads;
-        if (ITEMS % kWaveThreads != 0 && idx >= ITEMS) break;
+      for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
+        const int idx = static_cast<int>(threadIdx.x) + r * NT;
+        if (ITEMS % NT != 0 && idx >= ITEMS) break;
         const int f = idx / M;
         const int n = idx - f * M;
         float2 z = make_float2(0.f, 0.f);
@@ -326,9 +330,9 @@ __global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_
       const uint32_t dst0 = smem_u32(bufB);
       const bool i16 = a.in_i16 != 0;
 #pragma unroll 2
-      for (int r = 0; r < (ITEMS + kWaveThreads - 1) / kWaveThreads; ++r) {
-        const int g = static_cast<int>(threadIdx.x) + r * kWaveThreads;
-        if (ITEMS % kWaveThreads != 0 && g >= ITEMS) break;
+      for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
+        const int g = static_cast<int>(threadIdx.x) + r * NT;
+        if (ITEMS % NT != 0 && g >= ITEMS) break;
         const int f = g / T;
         const int i = g - f * T;
         float2 u[R0];
@@ -401,12 +405,12 @@ __global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_
     bool in_b;
     if constexpr (C::kFuseFirst) {
       if (fused) {
-        in_b = !fft::run<M, TF, kWaveThreads, fft::next_radix<M, 1>()>(bufB, bufA, twm);
+        in_b = !fft::run<M, TF, NT, fft::next_radix<M, 1>()>(bufB, bufA, twm);
       } else {
-        in_b = fft::run<M, TF, kWaveThreads>(bufA, bufB, twm);
+        in_b = fft::run<M, TF, NT>(bufA, bufB, twm);
       }
     } else {
-      in_b = fft::run<M, TF, kWaveThreads>(bufA, bufB, twm);
+      in_b = fft::run<M, TF, NT>(bufA, bufB, twm);
     }
     const float2 *Z = in_b ? bufB : bufA;  // == kResultInB; pw is the other buffer
 
@@ -419,9 +423,9 @@ __global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_
       constexpr int KP = M / 2 + 1;  // pairs per frame (M is even)
       constexpr int ITEMS = TF * KP;
 #pragma unroll 2
-      for (int r = 0; r < (ITEMS + kWaveThreads - 1) / kWaveThreads; ++r) {
-        const int idx = static_cast<int>(threadIdx.x) + r * kWaveThreads;
-        if (ITEMS % kWaveThreads != 0 && idx >= ITEMS) break;
+      for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
+        const int idx = static_cast<int>(threadIdx.x) + r * NT;
+        if (ITEMS % NT != 0 && idx >= ITEMS) break;
         const int f = idx / KP;
         const int k = idx - f * KP;
         const float2 A = Z[C::L::at(f * M + k)];
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_
       // One frame, filters hundreds of bins wide: a warp per band, lanes
       // over taps, then a shuffle reduction.
       const int lane = threadIdx.x & 31;
-      for (int m = threadIdx.x >> 5; m < a.n_mels; m += kWaveThreads / 32) {
+      for (int m = threadIdx.x >> 5; m < a.n_mels; m += NT / 32) {
         const int st = fstart[m], wd = fwidth[m];
         const float *w = fw + m * a.wmax;
         float acc = 0.f;
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_
       // band, so each band's output row is written as a run of consecutive
       // frames; the group walks bands m0, m0 + NG, ...  Shared memory is
       // addressed with 32-bit offsets.
-      constexpr int NG = kWaveThreads / TF;
+      constexpr int NG = NT / TF;
       const int f = static_cast<int>(threadIdx.x) % TF;
       if (f < nf) {
         const uint32_t prow = smem_u32(pw) + static_cast<uint32_t>(f * NFP) * 4u;
@@ -516,24 +520,25 @@ __global__ void __launch_bounds__(kWaveThreads, WaveCfg<NFFT>::kMinBlocks) wave_
 using WaveKernel = void (*)(WaveArgs);
 
 template <int NFFT>
-void wave_entry(WaveKernel *k, size_t *smem, int *tf, int n_mels, int wmax) {
+void wave_entry(WaveKernel *k, size_t *smem, int *tf, int *nt, int n_mels, int wmax) {
   *k = wave_mel_kernel<NFFT>;
   *smem = wave_smem_bytes<NFFT>(n_mels, wmax);
   *tf = WaveCfg<NFFT>::TF;
+  *nt = WaveCfg<NFFT>::NT;
 }
 
-bool pick_wave_kernel(int n_fft, int n_mels, int wmax, WaveKernel *k, size_t *smem, int *tf) {
+bool pick_wave_kernel(int n_fft, int n_mels, int wmax, WaveKernel *k, size_t *smem, int *tf, int *nt) {
   switch (n_fft) {
-    case 64: wave_entry<64>(k, smem, tf, n_mels, wmax); return true;
-    case 128: wave_entry<128>(k, smem, tf, n_mels, wmax); return true;
-    case 256: wave_entry<256>(k, smem, tf, n_mels, wmax); return true;
-    case 400: wave_entry<400>(k, smem, tf, n_mels, wmax); return true;
-    case 512: wave_entry<512>(k, smem, tf, n_mels, wmax); return true;
-    case 1024: wave_entry<1024>(k, smem, tf, n_mels, wmax); return true;
-    case 2048: wave_entry<2048>(k, smem, tf, n_mels, wmax); return true;
-    case 4096: wave_entry<4096>(k, smem, tf, n_mels, wmax); return true;
-    case 8192: wave_entry<8192>(k, smem, tf, n_mels, wmax); return true;
-    case 16384: wave_entry<16384>(k, smem, tf, n_mels, wmax); return true;
+    case 64: wave_entry<64>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 128: wave_entry<128>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 256: wave_entry<256>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 400: wave_entry<400>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 512: wave_entry<512>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 1024: wave_entry<1024>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 2048: wave_entry<2048>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 4096: wave_entry<4096>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 8192: wave_entry<8192>(k, smem, tf, nt, n_mels, wmax); return true;
+    case 16384: wave_entry<16384>(k, smem, tf, nt, n_mels, wmax); return true;
     default: return false;
   }
 }
@@ -675,8 +680,8 @@ int64_t frames_for(const lm_mel_params &p, int64_t T) {
 int tile_frames(int n_fft) {
   WaveKernel k;
   size_t smem;
-  int tf = 1;
-  pick_wave_kernel(n_fft, 1, 1, &k, &smem, &tf);
+  int tf = 1, nt = 0;
+  pick_wave_kernel(n_fft, 1, 1, &k, &smem, &tf, &nt);
   return tf;
 }
 
@@ -798,7 +803,8 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   lm::WaveKernel kern;
   size_t smem = 0;
   int tf = 1;
-  lm::pick_wave_kernel(p.n_fft, p.n_mels, plan->wmax, &kern, &smem, &tf);
+  int nt = 0;
+  lm::pick_wave_kernel(p.n_fft, p.n_mels, plan->wmax, &kern, &smem, &tf, &nt);
   // Two buffers for the contiguous samples of one tile of frames (plus 32
   // bytes of alignment slack), then two mbarriers.
   const int esize = in_dtype == LM_I16 ? 2 : 4;
@@ -819,7 +825,7 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
       st != LM_OK)
     return st;
   int per_sm = 0;
-  LM_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, lm::kWaveThreads, smem));
+  LM_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nt, smem));
   if (per_sm < 1) return LM_ERR_UNSUPPORTED;
 
   lm::WaveArgs a{};
@@ -861,7 +867,7 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   cudaStream_t s = stream;
   // Clears the device error word (and, for log plans, the tile slots).
   LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, a.log_mel ? need : lm::kWorkspaceHeaderBytes, s));
-  kern<<<grid, lm::kWaveThreads, smem, s>>>(a);
+  kern<<<grid, static_cast<unsigned>(nt), smem, s>>>(a);
   LM_CUDA_TRY(cudaGetLastError());
   if (a.log_mel) {
     if (lm_status st = lm::launch_clip_clamp(static_cast<float *>(out), a.tile_key, B, p.n_mels * nfr,
