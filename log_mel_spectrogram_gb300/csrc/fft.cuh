@@ -6,8 +6,8 @@
 // i + j*M/R (j < R) of every frame, multiplies it by exp(-2 pi i j k / (P R))
 // with k = i mod P, applies an R-point DFT and writes output l to position
 // (i - k) R + k + l P.  After the last pass (P = M) the result is in natural
-// order, so no bit reversal is needed.  Twiddles come from a table
-// W[t] = exp(-2 pi i t / M), t < M, built on the host in double precision.
+// order, so no bit reversal is needed.  The twiddle factors are built on the
+// host in double precision and laid out pass by pass (see rows_offset).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -108,6 +108,37 @@ struct Dft<5> {
   }
 };
 
+// Radix of the pass that follows span P: 5 while M/P has a factor 5, then 8
+// while possible, then the leftover 4 or 2.
+template <int M, int P>
+__host__ __device__ constexpr int next_radix() {
+  return ((M / P) % 5 == 0) ? 5 : ((M / P) % 8 == 0) ? 8 : ((M / P) % 4 == 0) ? 4 : 2;
+}
+
+// Twiddle table layout.  The pass with span P > 1 and radix R multiplies
+// input j of a butterfly with k = i mod P by exp(-2 pi i j k / (P R)); its
+// factors for j = 1..R-1 form row k, rows of row_stride<R>() values, P rows
+// per pass, passes back to back in order (the first pass, P = 1, needs
+// none).  A thread reads its R - 1 factors from one row at fixed offsets,
+// and the stride (7, 3 or 1 for radix 8, 4 or 2; radix 5 padded to 5) is
+// odd, so the rows of 16 consecutive butterflies fall in 16 distinct 8-byte
+// bank slots.  The rows take fewer than M entries for every supported M.
+template <int R>
+__host__ __device__ constexpr int row_stride() {
+  return R == 5 ? 5 : R - 1;
+}
+
+// Offset of the rows of the pass with span Q.
+template <int M, int Q, int P = 1>
+__host__ __device__ constexpr int rows_offset() {
+  if constexpr (P >= Q) {
+    return 0;
+  } else {
+    constexpr int R = next_radix<M, P>();
+    return (P > 1 ? P * row_stride<R>() : 0) + rows_offset<M, Q, P * R>();
+  }
+}
+
 // One Stockham pass over FRAMES frames of M points stored back to back (at
 // Layout<M> positions), by NT threads (the block size); every loop bound is
 // a compile-time constant.
@@ -115,7 +146,6 @@ template <int M, int R, int P, int FRAMES, int NT>
 __device__ __forceinline__ void pass(const float2 *__restrict__ in, float2 *__restrict__ out,
                                      const float2 *__restrict__ W) {
   constexpr int T = M / R;
-  constexpr int TW = M / (P * R);  // twiddle table stride
   constexpr int ITEMS = FRAMES * T;
 #pragma unroll
   for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
@@ -129,21 +159,15 @@ __device__ __forceinline__ void pass(const float2 *__restrict__ in, float2 *__re
 #pragma unroll
     for (int j = 0; j < R; ++j) u[j] = in[Layout<M>::at(base + j * T)];
     if constexpr (P > 1) {
+      const float2 *row = W + rows_offset<M, P>() + k * row_stride<R>();
 #pragma unroll
-      for (int j = 1; j < R; ++j) u[j] = cmul(u[j], W[j * k * TW]);
+      for (int j = 1; j < R; ++j) u[j] = cmul(u[j], row[j - 1]);
     }
     Dft<R>::run(u);
     const int obase = f * M + (i - k) * R + k;
 #pragma unroll
     for (int l = 0; l < R; ++l) out[Layout<M>::at(obase + l * P)] = u[l];
   }
-}
-
-// Radix of the pass that follows span P: 5 while M/P has a factor 5, then 8
-// while possible, then the leftover 4 or 2.
-template <int M, int P>
-__host__ __device__ constexpr int next_radix() {
-  return ((M / P) % 5 == 0) ? 5 : ((M / P) % 8 == 0) ? 8 : ((M / P) % 4 == 0) ? 4 : 2;
 }
 
 // Number of passes for an M-point transform (the result ends in the second

@@ -43,7 +43,7 @@ struct lm_mel_plan {
   int n_freqs;   // n_fft / 2 + 1
   int wmax;      // widest filter row, in bins
   float *window; // [n_fft]
-  float2 *tw_m;  // [n_fft/2]      exp(-2 pi i t / (n_fft/2))
+  float2 *tw_m;  // [n_fft/2]      FFT twiddles, per-pass rows (fft::rows_offset)
   float2 *tw_n;  // [n_fft/2 + 1]  exp(-2 pi i k / n_fft)
   int *fstart;   // [n_mels]
   int *fwidth;   // [n_mels]
@@ -586,10 +586,29 @@ void build_tables(const lm_mel_params &p, HostTables *t) {
   const double norm = p.normalized ? 1.0 / std::sqrt(energy) : 1.0;
   t->window.resize(N);
   for (int j = 0; j < N; ++j) t->window[j] = static_cast<float>(w[j] * norm);
-  t->tw_m.resize(M);
-  for (int i = 0; i < M; ++i) {
-    const double ang = -2.0 * M_PI * i / M;
-    t->tw_m[i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+  // FFT twiddles in the per-pass row layout of fft::rows_offset: for each
+  // pass after the first (span P, radix R, the radix rule of
+  // fft::next_radix), row k holds exp(-2 pi i j k / (P R)) for j = 1..R-1
+  // at stride R - 1 (radix 5: 5).  The rows fill fewer than M entries.
+  t->tw_m.assign(M, make_float2(0.f, 0.f));
+  {
+    size_t off = 0;
+    for (int P = 1; P < M;) {
+      const int q = M / P;
+      const int R = q % 5 == 0 ? 5 : q % 8 == 0 ? 8 : q % 4 == 0 ? 4 : 2;
+      if (P > 1) {
+        const int stride = R == 5 ? 5 : R - 1;
+        for (int k = 0; k < P; ++k) {
+          for (int j = 1; j < R; ++j) {
+            const double ang = -2.0 * M_PI * static_cast<double>(j) * k / (static_cast<double>(P) * R);
+            t->tw_m[off + static_cast<size_t>(k) * stride + j - 1] =
+                make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+          }
+        }
+        off += static_cast<size_t>(P) * stride;
+      }
+      P *= R;
+    }
   }
   t->tw_n.resize(M + 1);
   for (int k = 0; k <= M; ++k) {
