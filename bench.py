@@ -415,24 +415,28 @@ def run_ours(args, world, rank, local):
     # the timed region (the library overlaps the two directions and the
     # kernels chunk by chunk).  Inputs stay in host memory; the filter matrix
     # is a device-resident parameter, as in a serving process.
-    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 10))
+    # The value is the whole run's throughput; per-step times are reported
+    # beside it, since one host stall on a shared machine can weigh on a
+    # short run.
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 60))
     e2e_value = None
     h2d = d2h = 0
     e2e_ok = None
+    e2e_steps_ms = []
     if e2e_steps:
         h2d, d2h = job.host_setup()
         job.host_step()  # warm-up: creates the library's copy streams
         torch.cuda.synchronize(dev)
         barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+        marks[0].record(stream)
+        for i in range(e2e_steps):
             job.host_step()
-        e1.record(stream)
+            marks[i + 1].record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e_steps_ms = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(e2e_steps))
+        e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), world, dev)
         e2e_value = job_throughput(world, job.units, e2e_steps, e2e_ms)
         e2e_ok = job.host_check()
         if not e2e_ok:
@@ -478,7 +482,11 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": "clips/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": job.host_api() if e2e_steps else None,
-                "equals_device_result": e2e_ok},
+                "equals_device_result": e2e_ok,
+                "step_ms": ({"min": e2e_steps_ms[0], "median": e2e_steps_ms[len(e2e_steps_ms) // 2],
+                             "max": e2e_steps_ms[-1]} if e2e_steps_ms else None),
+                "value_at_median_step": (world * job.units / (e2e_steps_ms[len(e2e_steps_ms) // 2] / 1e3)
+                                         if e2e_steps_ms else None)},
         "host_latency_ms": {"median": lat[len(lat) // 2], "p90": lat[(9 * len(lat)) // 10], "samples": len(lat),
                             "launch": "cuda graph replay" if args.graph else "eager library call"},
         "gpu_launches": args.steps * job.kernels,
