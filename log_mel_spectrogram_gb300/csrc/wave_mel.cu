@@ -131,12 +131,14 @@ struct WaveCfg {
 };
 
 // Bytes of the table image up to 4096 points: tw_m [M] float2 | tw_n [M+1]
-// float2 | window [NFFT] | {fstart, fwidth} [n_mels] int2 | fw [n_mels*wmax],
-// rounded up to 16 (one bulk copy).
+// float2 and one float2 of padding | fw [n_mels*wmax] | window [NFFT] |
+// {fstart, fwidth} [n_mels] int2, rounded up to 16 (one bulk copy).  fw
+// starts 16-byte aligned (M is even) and wmax is a multiple of 4, so the
+// mel phase reads four weights with one 16-byte load.
 inline uint32_t wave_tables_bytes(int n_fft, int n_mels, int wmax) {
   const size_t M = n_fft / 2;
-  const size_t b = 8 * (2 * M + 1) + 4 * static_cast<size_t>(n_fft) + 8 * static_cast<size_t>(n_mels) +
-                   4 * static_cast<size_t>(n_mels) * wmax;
+  const size_t b = 8 * (2 * M + 2) + 4 * static_cast<size_t>(n_mels) * wmax + 4 * static_cast<size_t>(n_fft) +
+                   8 * static_cast<size_t>(n_mels);
   return static_cast<uint32_t>((b + 15) / 16 * 16);
 }
 
@@ -166,9 +168,9 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
   float *pw = reinterpret_cast<float *>(C::kResultInB ? bufA : bufB);
   float2 *twm = bufB + C::BUF;
   float2 *twn_s = twm + M;
-  float *win_s = reinterpret_cast<float *>(twn_s + M + 1);
+  float *fw_s = reinterpret_cast<float *>(twn_s + M + 2);  // 16-byte aligned
+  float *win_s = fw_s + a.n_mels * a.wmax;
   int2 *fsw_s = reinterpret_cast<int2 *>(win_s + NFFT);  // {first bin, width} per band
-  float *fw_s = reinterpret_cast<float *>(fsw_s + a.n_mels);
   uint32_t *blk_key = C::kSmallTables ? reinterpret_cast<uint32_t *>(reinterpret_cast<unsigned char *>(twm) + a.tables_bytes)
                                       : reinterpret_cast<uint32_t *>(twm + M);
   const float2 *twn = C::kSmallTables ? twn_s : a.tw_n;
@@ -494,13 +496,21 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
           const uint32_t pa = prow + static_cast<uint32_t>(sw.x) * 4u;
           float acc = 0.f;
           int t = 0;
+          // Weight rows start 16-byte aligned (wmax is a multiple of 4): four
+          // weights per load; the power row has no such alignment.
           for (; t + 4 <= sw.y; t += 4) {
-            acc = fmaf(lds_f32(wa + 4 * t), lds_f32(pa + 4 * t), acc);
-            acc = fmaf(lds_f32(wa + 4 * t + 4), lds_f32(pa + 4 * t + 4), acc);
-            acc = fmaf(lds_f32(wa + 4 * t + 8), lds_f32(pa + 4 * t + 8), acc);
-            acc = fmaf(lds_f32(wa + 4 * t + 12), lds_f32(pa + 4 * t + 12), acc);
+            const float4 w4 = lds_f32x4(wa + 4 * t);
+            acc = fmaf(w4.x, lds_f32(pa + 4 * t), acc);
+            acc = fmaf(w4.y, lds_f32(pa + 4 * t + 4), acc);
+            acc = fmaf(w4.z, lds_f32(pa + 4 * t + 8), acc);
+            acc = fmaf(w4.w, lds_f32(pa + 4 * t + 12), acc);
           }
-          for (; t < sw.y; ++t) acc = fmaf(lds_f32(wa + 4 * t), lds_f32(pa + 4 * t), acc);
+          if (t < sw.y) {
+            const float4 w4 = lds_f32x4(wa + 4 * t);
+            acc = fmaf(w4.x, lds_f32(pa + 4 * t), acc);
+            if (t + 1 < sw.y) acc = fmaf(w4.y, lds_f32(pa + 4 * t + 4), acc);
+            if (t + 2 < sw.y) acc = fmaf(w4.z, lds_f32(pa + 4 * t + 8), acc);
+          }
           emit(m, f, acc);
         }
       }
@@ -645,7 +655,9 @@ void build_tables(const lm_mel_params &p, HostTables *t) {
     }
     t->wmax = std::max(t->wmax, t->fwidth[m]);
   }
-  t->wmax = std::max(t->wmax, 1);
+  // Rows at a stride of a multiple of 4 taps (zero-padded): the kernel reads
+  // four weights at a time from 16-byte aligned rows.
+  t->wmax = (std::max(t->wmax, 1) + 3) / 4 * 4;
   t->fw.assign(static_cast<size_t>(p.n_mels) * t->wmax, 0.f);
   for (int m = 0; m < p.n_mels; ++m)
     for (int j = 0; j < t->fwidth[m]; ++j) t->fw[static_cast<size_t>(m) * t->wmax + j] = static_cast<float>(rows[m][j]);
@@ -738,12 +750,13 @@ extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan
     };
     put(t.tw_m.data(), t.tw_m.size() * sizeof(float2));
     put(t.tw_n.data(), t.tw_n.size() * sizeof(float2));
+    o += sizeof(float2);  // padding: fw starts 16-byte aligned
+    put(t.fw.data(), t.fw.size() * sizeof(float));
     put(t.window.data(), t.window.size() * sizeof(float));
     for (int m = 0; m < params->n_mels; ++m) {
       const int sw[2] = {t.fstart[m], t.fwidth[m]};
       put(sw, sizeof(sw));
     }
-    put(t.fw.data(), t.fw.size() * sizeof(float));
     st = lm::upload(img, &pl->tables);
   }
   if (st != LM_OK) {
