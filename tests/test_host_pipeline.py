@@ -109,6 +109,7 @@ def test_stft_host_concurrent_callers(lm):
         assert torch.equal(results[i], _device_result(lm, inputs[i][0], inputs[i][1], None))
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty:UserWarning")  # the refusal enqueues nothing
 def test_stft_host_refuses_graph_capture(lm):
     stft, W = workloads.stft_inputs(2, 50, 201, 80, seed=74)
     Wd = W.cuda()
