@@ -17,8 +17,8 @@
 //    below and the consumers index from the remainder.
 //  * CW consumer warps compute the tile.  Thread (n, g) owns mel band n and
 //    frames g, g+FG, ...; its band's support (first..last nonzero of the
-//    dense filter row, read from a filter pack or found by a sweep of the
-//    dense matrix once per CTA) and up to kRegTaps weights sit in registers.  Each tap is one 8-byte shared load and two packed f32x2
+//    dense filter row, found once per CTA) and up to kRegTaps weights sit in
+//    registers.  Each tap is one 8-byte shared load and two packed f32x2
 //    operations: acc += (w*re, w*im) * (re, im), so power and projection are
 //    formed together and the two halves are summed once per output.
 //  * Per-clip maximum without a second HBM pass: each warp reduces its tile
