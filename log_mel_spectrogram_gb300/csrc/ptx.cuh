@@ -124,13 +124,6 @@ __device__ __forceinline__ float2 lds_f32x2(uint32_t addr) {
   return v;
 }
 
-// 16-byte aligned address
-__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-  return v;
-}
-
 __device__ __forceinline__ void sts_f32x2(uint32_t addr, float2 v) {
   asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y));
 }

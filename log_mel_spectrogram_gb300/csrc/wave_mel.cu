@@ -55,6 +55,13 @@ struct lm_mel_plan {
 namespace lm {
 namespace {
 
+// Four floats from a 16-byte aligned shared-memory address.
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
 struct WaveArgs {
   const void *wave;
   void *out;
