@@ -96,7 +96,9 @@ lm_status lm_log_mel_from_stft_workspace_size(int64_t B, int64_t F, int32_t NF, 
  * spec: reference function, per-clip definition and I/O contract).
  *
  *   stft        device, [B][F][NF] complex64 = interleaved (re, im) f32
- *               pairs, contiguous, 16-byte aligned.            (read-only)
+ *               pairs, contiguous, 8-byte aligned (the alignment of a
+ *               complex64 element; any contiguous view of a complex64
+ *               tensor qualifies).                             (read-only)
  *   mel_filters device, [NM][NF] f32 row-major, 4-byte aligned; any dense
  *               matrix (only the span between the first and the last
  *               nonzero of each row is read).                  (read-only)
@@ -108,9 +110,10 @@ lm_status lm_log_mel_from_stft_workspace_size(int64_t B, int64_t F, int32_t NF, 
  *               4-byte aligned; its contents are overwritten.
  *
  * Errors: LM_ERR_INVALID_ARG (null pointer with B*F > 0, negative sizes),
- * LM_ERR_UNSUPPORTED (NF or NM out of range), LM_ERR_MISALIGNED,
- * LM_ERR_WORKSPACE, LM_ERR_CUDA.  B == 0 or F == 0 returns LM_OK and
- * enqueues nothing.  Concurrent calls must use distinct workspaces.
+ * LM_ERR_UNSUPPORTED (NF or NM out of range), LM_ERR_MISALIGNED (stft not
+ * 8-byte aligned, out or workspace not 4-byte aligned), LM_ERR_WORKSPACE,
+ * LM_ERR_CUDA.  B == 0 or F == 0 returns LM_OK and enqueues nothing.
+ * Concurrent calls must use distinct workspaces.
  */
 lm_status lm_log_mel_from_stft(const void *stft, const float *mel_filters, float *out, int64_t B,
                                int64_t F, int32_t NF, int32_t NM, void *workspace,
@@ -192,20 +195,24 @@ lm_status lm_log_mel_from_stft_packed(const void *stft, const float *mel_filters
  * Scratch comes from one fixed array of LM_NOALLOC_SCRATCH_BYTES compiled
  * into the library; every GPU that loads the library holds that array until
  * the process exits.  The call allocates and frees nothing.
- *  - A problem needing more scratch than that (16 bytes plus 4 bytes per
- *    tile of frames; for NF = 201, NM = 128 a tile is 25 frames, so up to
- *    about 262,000 tiles, e.g. 256 clips of up to 25,575 frames) returns
- *    LM_ERR_WORKSPACE and enqueues nothing.
+ *  - Its first LM_NOALLOC_SCRATCH_BYTES - 256 bytes stand in for the
+ *    workspace.  A problem needing more than that (about 16 bytes plus 4
+ *    bytes per tile of frames; for NF = 201, NM = 128 a tile is 25 frames,
+ *    so up to about 262,000 tiles, e.g. 256 clips of up to 25,500 frames)
+ *    returns LM_ERR_WORKSPACE and enqueues nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: after a cudaDeviceReset of that device it is stale, so do not
+ *    call these entry points after one.
  *  - Every call uses the same array, which keeps the previous call's
  *    contents; each call clears the part it needs before its kernel runs.
  *    Calls whose work can overlap on the GPU (different streams, or host
  *    threads without ordering between them) race on the array: the caller
  *    must order them.
- *  - The device error word of these calls lives in the shared array and is
- *    not readable through lm_workspace_error.
+ *  - The kernels' device error bits go to a word in the array's last 256
+ *    bytes, which no call clears: bits accumulate over calls until
+ *    lm_log_mel_from_stft_noalloc_error reads and clears them.
  */
 #define LM_NOALLOC_SCRATCH_BYTES (1u << 20)
 
@@ -213,12 +220,48 @@ lm_status lm_log_mel_from_stft_noalloc(const void *stft, const float *mel_filter
                                        int64_t B, int64_t F, int32_t NF, int32_t NM,
                                        lm_stream_t stream);
 
+/* Synchronises `stream`, then reads the accumulated device error word of
+ * lm_log_mel_from_stft_noalloc calls on the current device (0 = no kernel
+ * reported a problem) into *device_error, and clears it when `clear` is
+ * nonzero (the clearing is ordered on `stream`).  Allocates nothing.
+ * Returns LM_ERR_DEVICE_FAULT when the word was nonzero, LM_ERR_INVALID_ARG
+ * for a null pointer, LM_ERR_CUDA when a CUDA call failed. */
+lm_status lm_log_mel_from_stft_noalloc_error(uint32_t *device_error, int32_t clear, lm_stream_t stream);
+
 /* Synchronises `stream`, then reads the device error word of a workspace
  * used by lm_log_mel_from_stft or lm_mel_spectrogram.  *device_error = 0
- * means no kernel reported a problem.  Returns LM_ERR_DEVICE_FAULT when it
- * is nonzero. */
+ * means no kernel reported a problem; otherwise it holds bit flags:
+ *   1  an mbarrier wait inside a kernel ran out (2 s)
+ *   2  waiting for a clip's maximum ran out
+ *   4  a filter pack did not match the call (the dense matrix was used)
+ * Returns LM_ERR_DEVICE_FAULT when it is nonzero. */
 lm_status lm_workspace_error(const void *workspace, size_t workspace_bytes, uint32_t *device_error,
                              lm_stream_t stream);
+
+/* ---- Fault injection for tests of the bounded waits (the source pages
+ * have no counterpart) ----
+ *
+ * Runs lm_log_mel_from_stft (same arguments, results and errors) with two
+ * changes that make one of its cross-CTA waits run out on purpose, so that
+ * a test can check that the kernel gives up cleanly instead of hanging:
+ *   withheld_tile  the maximum of this tile of frames is never published
+ *                  (tiles are numbered clip by clip; a clip has
+ *                  ceil(F / frames_per_tile) of them, see
+ *                  lm_log_mel_from_stft_describe); >= 0.
+ *   clip_wait_ns   how long a CTA waits for a clip's maximum before giving
+ *                  up (the regular calls wait 2 s); 1e5 .. 2e9.
+ * When a wait gives up, the CTA sets bit 2 of the workspace's device error
+ * word, its warps stop without further stores, and it exits once its
+ * in-flight copies have landed.  The outputs of the clip whose tile was
+ * withheld (and, where a CTA ran tiles of several clips, of the clips it
+ * had not finished) are left incomplete.  Only single-kernel (resident)
+ * launches wait across CTAs; for two-launch shapes the tile's slot stays
+ * zero and the epilogue reduces the clip maximum over the other tiles.
+ * Returns LM_ERR_INVALID_ARG for arguments out of range. */
+lm_status lm_debug_log_mel_from_stft_withhold(const void *stft, const float *mel_filters, float *out,
+                                              int64_t B, int64_t F, int32_t NF, int32_t NM, void *workspace,
+                                              size_t workspace_bytes, int64_t withheld_tile,
+                                              uint64_t clip_wait_ns, lm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* 2. waveform -> mel spectrogram                                            */
@@ -250,7 +293,11 @@ typedef struct lm_mel_plan lm_mel_plan;
 /* Validates `params`, builds the window, filterbank and FFT tables on the
  * host in double and uploads them (rounded to f32) to the current device.
  * Errors: LM_ERR_INVALID_ARG, LM_ERR_UNSUPPORTED, LM_ERR_OUT_OF_MEMORY,
- * LM_ERR_CUDA.  The plan is immutable and may be shared by streams. */
+ * LM_ERR_CUDA; on any error *plan is NULL and nothing stays allocated.
+ * The plan is immutable and may be shared by streams.
+ * For tests of that error path, the environment variable
+ * LOGMEL_FAULT=plan_alloc (or plan_alloc:k) makes the first (k-th) of the
+ * plan's device allocations fail as if the device were out of memory. */
 lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan **plan);
 
 /* Frees the plan's device tables (synchronises the device first). */

@@ -80,6 +80,13 @@ def lib() -> ctypes.CDLL:
         L.lm_log_mel_from_stft_packed.restype = ctypes.c_int
         L.lm_workspace_error.argtypes = [vp, sz, ctypes.POINTER(u32), vp]
         L.lm_workspace_error.restype = ctypes.c_int
+        L.lm_log_mel_from_stft_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
+        L.lm_log_mel_from_stft_noalloc.restype = ctypes.c_int
+        L.lm_log_mel_from_stft_noalloc_error.argtypes = [ctypes.POINTER(u32), i32, vp]
+        L.lm_log_mel_from_stft_noalloc_error.restype = ctypes.c_int
+        L.lm_debug_log_mel_from_stft_withhold.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, sz, i64,
+                                                          ctypes.c_uint64, vp]
+        L.lm_debug_log_mel_from_stft_withhold.restype = ctypes.c_int
         L.lm_mel_plan_create.argtypes = [ctypes.POINTER(MelParams), ctypes.POINTER(vp)]
         L.lm_mel_plan_create.restype = ctypes.c_int
         L.lm_mel_plan_destroy.argtypes = [vp]

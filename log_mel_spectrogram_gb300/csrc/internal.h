@@ -46,13 +46,22 @@ const char *env_or(const char *name, const char *fallback);
 // Workspace bytes of lm_log_mel_from_stft for this shape.
 size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM);
 
+// Fault injection for tests of the bounded waits: the maximum of tile
+// `withhold_tile` is never published, and the resolver gives up waiting for
+// a clip maximum after `clip_wait_ns`.
+struct StftFault {
+  uint64_t clip_wait_ns;
+  int64_t withhold_tile;
+};
+
 // Validated launch; arguments as in lm_log_mel_from_stft.  `err_word`, when
 // set, receives the kernel's error bits instead of the workspace header (a
-// device u32 the caller clears).
+// device u32 the caller clears).  `fault` is null outside tests.
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
                           int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
                           cudaStream_t stream,
-                          const void *packed = nullptr, uint32_t *err_word = nullptr);
+                          const void *packed = nullptr, uint32_t *err_word = nullptr,
+                          const StftFault *fault = nullptr);
 
 // Per-clip floor and rescale in place: out[b] = (max(out[b], hi_b - 8) + 4) / 4,
 // hi_b = the largest of the clip's tiles_per_clip order-preserving keys.

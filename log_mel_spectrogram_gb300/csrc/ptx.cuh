@@ -103,6 +103,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   return mbar_wait_slow(addr, parity, abort_flag, err_word);
 }
 
+// Waits for a phase that a bulk copy this thread issued completes: used
+// before a CTA exits, so that no copy into its shared memory outlives it.
+// Ignores the abort flag (the copy lands whatever the other warps did);
+// bounded all the same, reporting kErrMbarTimeout if it ever ran out.
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint32_t *err_word) {
+  const uint32_t addr = smem_u32(bar);
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((it & 63u) == 0u) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitTimeoutNs) {
+        atomicOr(err_word, kErrMbarTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy (bulk copy) accesses to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory loads and stores by 32-bit shared-window address.  Volatile,
 // so the compiler keeps them in program order with the barriers and
 // mbarrier waits around them.

@@ -83,6 +83,8 @@ struct StftArgs {
   uint32_t aux_offset;     // shared-memory offset of SmemAux (after the stages and the ring)
   uint64_t total_bytes;    // B * F * NF * 8
   const int32_t *packed;   // packed filter supports and first taps (see PackLayout), or null
+  uint64_t clip_wait_ns;   // how long the resolver waits for a clip's maximum before giving up
+  int64_t withhold_tile;   // fault injection (tests only): this tile's maximum is never published; -1 = none
 };
 
 // Packed filters: header {magic, NF, NM, widest support}, then {first bin,
@@ -214,9 +216,12 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
   // Final values of step q from this thread's own ring entries.  The tile
   // descriptor of step q is still in its slot: the producer runs at most
   // n_stages (< kSlots - kLag) steps ahead of the consumers.
-  auto store_final = [&](int64_t q) {
+  // Returns false, storing nothing, when the wait for the clip maximum gave
+  // up (the CTA is aborting).
+  auto store_final = [&](int64_t q) -> bool {
     const int d = static_cast<int>(q & (kSlots - 1));
-    mbar_wait(&aux.hi_bar[d], static_cast<uint32_t>((q / kSlots) & 1), abort_flag, a.err);
+    const bool ok = mbar_wait(&aux.hi_bar[d], static_cast<uint32_t>((q / kSlots) & 1), abort_flag, a.err);
+    if (!__all_sync(0xffffffffu, ok)) return false;
     const float floor_v = aux.hi_val[d] - 8.0f;
     const int nf = aux.desc_nf[d];
     const float *r = ring + sslot * slot_stride + own;
@@ -227,6 +232,7 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
         if (c.fg + j * a.FG < nf) __stcs(o + j * ostep, rescale(r[j * ostep], floor_v));
     }
     if (++sslot == kLag + 1) sslot = 0;
+    return true;
   };
 
   for (int64_t k = 0; k < my_tiles; ++k) {
@@ -236,10 +242,15 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
       // reused before the publisher has read it.
       if (k >= kSlots / 2) {
         const int64_t j = k - kSlots / 2;
-        mbar_wait(&aux.pub_bar[j & (kSlots - 1)], static_cast<uint32_t>((j / kSlots) & 1), abort_flag, a.err);
+        const bool ok =
+            mbar_wait(&aux.pub_bar[j & (kSlots - 1)], static_cast<uint32_t>((j / kSlots) & 1), abort_flag, a.err);
+        if (!__all_sync(0xffffffffu, ok)) return;
       }
     }
-    mbar_wait(&aux.full[s], ph, abort_flag, a.err);
+    // A wait that gave up means the CTA is aborting: the warp leaves without
+    // touching the stage (the producer may never have filled it) or global
+    // memory.  The vote keeps the lanes together.
+    if (!__all_sync(0xffffffffu, mbar_wait(&aux.full[s], ph, abort_flag, a.err))) return;
     const int d = static_cast<int>(k & (kSlots - 1));
     const int64_t frame0 = aux.desc_frame0[d];
     const int nf = aux.desc_nf[d];
@@ -272,7 +283,7 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
       mbar_arrive(&aux.tmax_bar[d]);
     }
     if constexpr (kResident) {
-      if (k >= kLag) store_final(k - kLag);
+      if (k >= kLag && !store_final(k - kLag)) return;
       if (++slot == kLag + 1) slot = 0;
     }
     if (++s == S) {
@@ -281,7 +292,8 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
     }
   }
   if constexpr (kResident) {
-    for (int64_t q = my_tiles > kLag ? my_tiles - kLag : 0; q < my_tiles; ++q) store_final(q);
+    for (int64_t q = my_tiles > kLag ? my_tiles - kLag : 0; q < my_tiles; ++q)
+      if (!store_final(q)) return;
   }
 }
 
@@ -322,40 +334,64 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
 
   if (warp == kProducerWarp) {
     // ---------------- producer: bulk copies of frame tiles ----------------
+    // Addresses are absolute: the tensor need only be 8-byte aligned.  A
+    // tile's copy covers the 16-byte aligned range around it; where that
+    // range would start before the tensor (its first value sits 8 bytes past
+    // a boundary) or end after it, the one complex value concerned is copied
+    // by hand and the bulk copy shrinks to the aligned part.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const char *src = reinterpret_cast<const char *>(a.stft);
+      const uint64_t base = reinterpret_cast<uint64_t>(a.stft);
+      const uint64_t limit = base + a.total_bytes;
       TileIter it;
       it.init(blockIdx.x, a.tiles_per_clip);
       int s = 0;
       uint32_t ph = 0;
+      uint32_t generic_written = 0;  // stages holding a hand-copied value
+      int64_t issued = 0;
       for (int64_t k = 0; k < my_tiles; ++k) {
         if (k >= S && !mbar_wait(&aux.empty[s], ph ^ 1u, abort_flag, a.err)) break;
-        const uint64_t start = static_cast<uint64_t>(it.first_frame(a)) * a.NF * 8ull;
+        const uint64_t start = base + static_cast<uint64_t>(it.first_frame(a)) * a.NF * 8ull;
         const uint64_t end = start + static_cast<uint64_t>(it.frames(a)) * a.NF * 8ull;
-        const uint64_t a0 = start & ~15ull;
-        uint64_t a1 = (end + 15ull) & ~15ull;
+        const uint64_t a0 = start & ~15ull;  // the address stage byte 0 stands for
+        uint64_t lo = a0;
+        uint64_t hi = (end + 15ull) & ~15ull;
         unsigned char *dst = smem + static_cast<size_t>(s) * a.stage_stride;
-        if (a1 > a.total_bytes) {
-          // The tensor ends 8 bytes past a 16-byte boundary: copy its last
-          // complex value by hand; the bulk copy stops at the boundary.
-          a1 = end & ~15ull;
-          *reinterpret_cast<float2 *>(dst + (end - 8 - a0)) =
-              *reinterpret_cast<const float2 *>(src + end - 8);
+        if ((generic_written >> s) & 1u) {
+          // the bulk copy below may overwrite bytes written by hand earlier
+          fence_proxy_async_smem();
+          generic_written &= ~(1u << s);
         }
-        const uint32_t bytes = static_cast<uint32_t>(a1 - a0);
+        if (lo < base) {
+          // the first tile of a tensor that starts 8 bytes past a boundary
+          *reinterpret_cast<float2 *>(dst + (start - a0)) = *reinterpret_cast<const float2 *>(start);
+          lo += 16;
+          generic_written |= 1u << s;
+        }
+        if (hi > limit) {
+          // the last tile of a tensor that ends 8 bytes past a boundary
+          *reinterpret_cast<float2 *>(dst + (end - 8 - a0)) = *reinterpret_cast<const float2 *>(end - 8);
+          hi = end & ~15ull;
+          generic_written |= 1u << s;
+        }
+        const uint32_t bytes = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
         const int d = static_cast<int>(k & (kSlots - 1));
         aux.desc_frame0[d] = it.first_frame(a);
         aux.desc_nf[d] = it.frames(a);
         aux.desc_head[d] = static_cast<int32_t>(start - a0);
         mbar_arrive_expect_tx(&aux.full[s], bytes);
-        if (bytes > 0) bulk_g2s(dst, src + a0, bytes, &aux.full[s], pol);
+        if (bytes > 0) bulk_g2s(dst + (lo - a0), reinterpret_cast<const void *>(lo), bytes, &aux.full[s], pol);
+        ++issued;
         it.next(a);
         if (++s == S) {
           s = 0;
           ph ^= 1u;
         }
       }
+      // Every copy issued lands before the CTA may exit: wait for the last
+      // phase of each stage in use (immediate unless the CTA is aborting).
+      for (int64_t k = issued > S ? issued - S : 0; k < issued; ++k)
+        mbar_wait_drain(&aux.full[k % S], static_cast<uint32_t>((k / S) & 1), a.err);
     }
     return;
   }
@@ -366,10 +402,11 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
     volatile uint32_t *tkey = aux.tmax_key;
     for (int64_t k = 0; k < my_tiles; ++k) {
       const int r = static_cast<int>(k & (kSlots - 1));
-      mbar_wait(&aux.tmax_bar[r], static_cast<uint32_t>((k / kSlots) & 1), abort_flag, a.err);
+      if (!mbar_wait(&aux.tmax_bar[r], static_cast<uint32_t>((k / kSlots) & 1), abort_flag, a.err)) return;
       const uint32_t key = tkey[r];
       tkey[r] = 0u;
-      st_relaxed_gpu(a.tile_key + blockIdx.x + k * G, key);
+      const int64_t tile = blockIdx.x + k * G;
+      if (tile != a.withhold_tile) st_relaxed_gpu(a.tile_key + tile, key);
       mbar_arrive(&aux.pub_bar[r]);
     }
     return;
@@ -400,7 +437,10 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
     auto gate = [&](int64_t q) { return min(q + a.span, my_tiles - 1); };
     while (q_next < my_tiles) {
       const int64_t g0 = gate(q_next);
-      if (!mbar_wait(&aux.pub_bar[g0 & (kSlots - 1)], static_cast<uint32_t>((g0 / kSlots) & 1), abort_flag, a.err))
+      // Every lane waits; the vote keeps the warp together for the
+      // warp-wide operations below when some lane's wait gave up.
+      if (!__all_sync(0xffffffffu, mbar_wait(&aux.pub_bar[g0 & (kSlots - 1)],
+                                             static_cast<uint32_t>((g0 / kSlots) & 1), abort_flag, a.err)))
         return;
       // Lane w < M tests the gate of step q_next + w; the publisher goes in
       // step order, so the open steps are a prefix.  A gate is fewer than
@@ -479,7 +519,7 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
       if (lane == 0) {
         const uint64_t now = global_timer_ns();
         if (t0 == 0) t0 = now;
-        if (!*abort_flag && now - t0 > kWaitTimeoutNs) {
+        if (!*abort_flag && now - t0 > a.clip_wait_ns) {
           *abort_flag = 1;
           atomicOr(a.err, kErrClipTimeout);
         }
@@ -832,14 +872,14 @@ size_t stft_workspace_bytes(int64_t B, int64_t F, int32_t NF, int32_t NM) {
 
 lm_status stft_logmel_run(const void *stft, const float *filters, float *out, int64_t B, int64_t F,
                           int32_t NF, int32_t NM, void *workspace, size_t workspace_bytes,
-                          cudaStream_t stream, const void *packed, uint32_t *err_word) {
+                          cudaStream_t stream, const void *packed, uint32_t *err_word, const StftFault *fault) {
   if (B < 0 || F < 0 || NF < 1 || NM < 1) return LM_ERR_INVALID_ARG;
   if (NF > kMaxBins || NM > kMaxBands) return LM_ERR_UNSUPPORTED;
   if (B == 0 || F == 0) return LM_OK;
   if (!stft || !filters || !out || !workspace) return workspace ? LM_ERR_INVALID_ARG : LM_ERR_WORKSPACE;
   if (F > (int64_t{1} << 40) || B > (int64_t{1} << 40) || (B * F) > (int64_t{1} << 50) / NF)
     return LM_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(stft) & 15) || (reinterpret_cast<uintptr_t>(filters) & 3) ||
+  if ((reinterpret_cast<uintptr_t>(stft) & 7) || (reinterpret_cast<uintptr_t>(filters) & 3) ||
       (reinterpret_cast<uintptr_t>(out) & 3) || (reinterpret_cast<uintptr_t>(workspace) & 3))
     return LM_ERR_MISALIGNED;
   if (packed && (reinterpret_cast<uintptr_t>(packed) & 15)) return LM_ERR_MISALIGNED;
@@ -878,6 +918,8 @@ lm_status stft_logmel_run(const void *stft, const float *filters, float *out, in
   a.grid_q = ln.grid / ln.tpc;
   a.grid_r = static_cast<int32_t>(ln.grid % ln.tpc);
   a.packed = static_cast<const int32_t *>(packed);
+  a.clip_wait_ns = fault ? fault->clip_wait_ns : kWaitTimeoutNs;
+  a.withhold_tile = fault ? fault->withhold_tile : -1;
 
   LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, ws_needed, stream));
 
@@ -958,6 +1000,17 @@ extern "C" lm_status lm_log_mel_from_stft(const void *stft, const float *mel_fil
                              reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
+extern "C" lm_status lm_debug_log_mel_from_stft_withhold(const void *stft, const float *mel_filters, float *out,
+                                                         int64_t B, int64_t F, int32_t NF, int32_t NM,
+                                                         void *workspace, size_t workspace_bytes,
+                                                         int64_t withheld_tile, uint64_t clip_wait_ns,
+                                                         lm_stream_t stream) {
+  if (withheld_tile < 0 || clip_wait_ns < 100000ull || clip_wait_ns > lm::kWaitTimeoutNs) return LM_ERR_INVALID_ARG;
+  const lm::StftFault fault{clip_wait_ns, withheld_tile};
+  return lm::stft_logmel_run(stft, mel_filters, out, B, F, NF, NM, workspace, workspace_bytes,
+                             reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, &fault);
+}
+
 extern "C" lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM,
                                                    lm_stft_launch_info *info) {
   return lm::stft_describe(B, F, NF, NM, info);
@@ -968,13 +1021,34 @@ extern "C" lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t
 // present on every GPU that loads this library until the process exits.  Host
 // code may not pass `g_noalloc_scratch` itself to a kernel (in host code the
 // name is a host-side stand-in, not a device address); its device address is
-// looked up once per device below.
+// looked up once per device below.  The first LM_NOALLOC_SCRATCH_BYTES - 256
+// bytes serve as the call's workspace and are cleared by every call; the
+// last 256 bytes hold a sticky device error word that no call clears.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LM_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 constexpr int kNoallocMaxDevices = 64;
+constexpr size_t kNoallocWorkspaceBytes = LM_NOALLOC_SCRATCH_BYTES - 256;
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[kNoallocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current).  The cache outlives a
+// cudaDeviceReset, after which the address is stale: the entry points that
+// use it document that.
+lm_status noalloc_scratch(void **scratch) {
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return lm::cuda_fail(e);
+  if (dev < 0 || dev >= kNoallocMaxDevices) return LM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    if (cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch); e != cudaSuccess) return lm::cuda_fail(e);
+    g_noalloc_addr[dev] = p;
+  }
+  *scratch = g_noalloc_addr[dev];
+  return LM_OK;
+}
 }  // namespace
 
 extern "C" lm_status lm_log_mel_from_stft_noalloc(const void *stft, const float *mel_filters, float *out,
@@ -983,23 +1057,29 @@ extern "C" lm_status lm_log_mel_from_stft_noalloc(const void *stft, const float 
   if (B < 0 || F < 0 || NF < 1 || NM < 1) return LM_ERR_INVALID_ARG;
   if (NF > 8193 || NM > 512) return LM_ERR_UNSUPPORTED;
   if (B == 0 || F == 0) return LM_OK;
-  if (lm::stft_workspace_bytes(B, F, NF, NM) > LM_NOALLOC_SCRATCH_BYTES) return LM_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return lm::cuda_fail(e);
-  if (dev < 0 || dev >= kNoallocMaxDevices) return LM_ERR_UNSUPPORTED;
+  if (lm::stft_workspace_bytes(B, F, NF, NM) > kNoallocWorkspaceBytes) return LM_ERR_WORKSPACE;
   void *scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-      void *p = nullptr;
-      if (cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch); e != cudaSuccess) return lm::cuda_fail(e);
-      g_noalloc_addr[dev] = p;
-    }
-    scratch = g_noalloc_addr[dev];
-  }
-  // stft_logmel_run clears the scratch it uses before launching.
-  return lm::stft_logmel_run(stft, mel_filters, out, B, F, NF, NM, scratch, LM_NOALLOC_SCRATCH_BYTES,
-                             reinterpret_cast<cudaStream_t>(stream), nullptr);
+  if (lm_status st = noalloc_scratch(&scratch); st != LM_OK) return st;
+  uint32_t *sticky_err = reinterpret_cast<uint32_t *>(static_cast<char *>(scratch) + kNoallocWorkspaceBytes);
+  // stft_logmel_run clears the workspace part it uses before launching; the
+  // kernel's error bits go to the sticky word past it.
+  return lm::stft_logmel_run(stft, mel_filters, out, B, F, NF, NM, scratch, kNoallocWorkspaceBytes,
+                             reinterpret_cast<cudaStream_t>(stream), nullptr, sticky_err);
+}
+
+extern "C" lm_status lm_log_mel_from_stft_noalloc_error(uint32_t *device_error, int32_t clear, lm_stream_t stream) {
+  if (!device_error) return LM_ERR_INVALID_ARG;
+  *device_error = 0;
+  void *scratch = nullptr;
+  if (lm_status st = noalloc_scratch(&scratch); st != LM_OK) return st;
+  uint32_t *sticky_err = reinterpret_cast<uint32_t *>(static_cast<char *>(scratch) + kNoallocWorkspaceBytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  LM_CUDA_TRY(cudaMemcpyAsync(&v, sticky_err, sizeof(v), cudaMemcpyDeviceToHost, s));
+  if (clear) LM_CUDA_TRY(cudaMemsetAsync(sticky_err, 0, sizeof(uint32_t), s));
+  LM_CUDA_TRY(cudaStreamSynchronize(s));
+  *device_error = v;
+  return v ? LM_ERR_DEVICE_FAULT : LM_OK;
 }
 
 extern "C" lm_status lm_mel_filters_pack_size(int32_t NF, int32_t NM, size_t *bytes) {

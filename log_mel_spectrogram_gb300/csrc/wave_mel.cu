@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     *bytes = static_cast<uint32_t>(a1 - *a0);
     return true;
   };
+  uint32_t issued[2] = {0u, 0u};  // span copies issued per buffer (thread 0)
   auto issue_span = [&](int64_t tile, int buf) {
     uint64_t a0;
     uint32_t bytes;
@@ -217,7 +218,16 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       mbar_arrive_expect_tx(&seg_bar[buf], bytes);
       bulk_g2s(seg + buf * static_cast<size_t>(a.seg_bytes), static_cast<const char *>(a.wave) + a0, bytes,
                &seg_bar[buf], policy_evict_first());
+      ++issued[buf];
     }
+  };
+  // Before the CTA exits, thread 0 waits until every copy it issued has
+  // landed (immediate unless a wait gave up and the loop was left early).
+  auto drain = [&](bool tables) {
+    if (threadIdx.x != 0) return;
+    if (tables) mbar_wait_drain(&seg_bar[2], 0u, a.err);
+    for (int b = 0; b < 2; ++b)
+      if (issued[b] > 0) mbar_wait_drain(&seg_bar[b], (issued[b] - 1u) & 1u, a.err);
   };
   if (threadIdx.x == 0) {
     mbar_init(&seg_bar[0], 1);
@@ -236,7 +246,13 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
 
   if constexpr (C::kSmallTables) {
     __syncthreads();  // the barrier is initialised
-    mbar_wait(&seg_bar[2], 0, abort_flag, a.err);
+    // Without the tables every later shared-memory index is meaningless:
+    // if any thread's wait gave up, the whole CTA stops here.
+    const bool ok = mbar_wait(&seg_bar[2], 0, abort_flag, a.err);
+    if (__syncthreads_or(!ok)) {
+      drain(true);
+      return;
+    }
   } else {
     for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
   }
@@ -260,7 +276,10 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       *blk_key = 0u;
       *next_s = static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
     }
-    __syncthreads();  // tables loaded / previous tile finished with every buffer
+    // Tables loaded / previous tile finished with every buffer.  A wait that
+    // gave up in the previous tile (its values are then wrong, but every
+    // index stayed in bounds) ends the loop in every thread together.
+    if (__syncthreads_or(*abort_flag != 0)) break;
     nxt = *next_s;
     // Prefetch the next tile's samples into the other span buffer; the
     // previous tile's framing, its last reader, finished before the barrier.
@@ -529,6 +548,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       if (threadIdx.x == 0) a.tile_key[tile] = *blk_key;
     }
   }
+  drain(false);
   // This CTA is done: a programmatically dependent epilogue may be scheduled
   // (it still waits for the whole grid before reading).
   asm volatile("griddepcontrol.launch_dependents;");
@@ -670,10 +690,26 @@ void build_tables(const lm_mel_params &p, HostTables *t) {
     for (int j = 0; j < t->fwidth[m]; ++j) t->fw[static_cast<size_t>(m) * t->wmax + j] = static_cast<float>(rows[m][j]);
 }
 
+// Host-side fault injection for tests: with LOGMEL_FAULT=plan_alloc (or
+// plan_alloc:k) the first (k-th, counting from 1) device allocation of a plan
+// creation fails as if the device were out of memory, before any CUDA call
+// is made for it.  Unset, nothing changes.
+bool plan_alloc_fault(int index) {
+  const char *v = env_or("LOGMEL_FAULT", "");
+  const char *key = "plan_alloc";
+  const size_t n = std::strlen(key);
+  if (std::strncmp(v, key, n) != 0) return false;
+  int k = 1;
+  if (v[n] == ':') k = std::atoi(v + n + 1);
+  else if (v[n] != '\0') return false;
+  return index == k;
+}
+
 template <typename T>
-lm_status upload(const std::vector<T> &h, T **d) {
+lm_status upload(const std::vector<T> &h, T **d, int *n_alloc) {
   *d = nullptr;
   if (h.empty()) return LM_OK;
+  if (plan_alloc_fault(++*n_alloc)) return LM_ERR_OUT_OF_MEMORY;
   cudaError_t e = cudaMalloc(reinterpret_cast<void **>(d), h.size() * sizeof(T));
   if (e == cudaErrorMemoryAllocation) {
     (void)cudaGetLastError();
@@ -686,13 +722,10 @@ lm_status upload(const std::vector<T> &h, T **d) {
 
 void free_plan(lm_mel_plan *pl) {
   if (!pl) return;
-  cudaFree(pl->window);
-  cudaFree(pl->tw_m);
-  cudaFree(pl->tw_n);
-  cudaFree(pl->fstart);
-  cudaFree(pl->fwidth);
-  cudaFree(pl->fw);
-  cudaFree(pl->tables);
+  for (void *ptr : {static_cast<void *>(pl->window), static_cast<void *>(pl->tw_m), static_cast<void *>(pl->tw_n),
+                    static_cast<void *>(pl->fstart), static_cast<void *>(pl->fwidth), static_cast<void *>(pl->fw),
+                    static_cast<void *>(pl->tables)})
+    if (ptr) cudaFree(ptr);
   delete pl;
 }
 
@@ -736,16 +769,14 @@ extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan
   pl->p = *params;
   pl->n_freqs = params->n_fft / 2 + 1;
   pl->wmax = t.wmax;
-  if (cudaError_t e = cudaGetDevice(&pl->device); e != cudaSuccess) {
-    delete pl;
-    return lm::cuda_fail(e);
-  }
-  lm_status st = lm::upload(t.window, &pl->window);
-  if (st == LM_OK) st = lm::upload(t.tw_m, &pl->tw_m);
-  if (st == LM_OK) st = lm::upload(t.tw_n, &pl->tw_n);
-  if (st == LM_OK) st = lm::upload(t.fstart, &pl->fstart);
-  if (st == LM_OK) st = lm::upload(t.fwidth, &pl->fwidth);
-  if (st == LM_OK) st = lm::upload(t.fw, &pl->fw);
+  // The tables go to the current device, which the plan records.
+  int n_alloc = 0;
+  lm_status st = lm::upload(t.window, &pl->window, &n_alloc);
+  if (st == LM_OK) st = lm::upload(t.tw_m, &pl->tw_m, &n_alloc);
+  if (st == LM_OK) st = lm::upload(t.tw_n, &pl->tw_n, &n_alloc);
+  if (st == LM_OK) st = lm::upload(t.fstart, &pl->fstart, &n_alloc);
+  if (st == LM_OK) st = lm::upload(t.fwidth, &pl->fwidth, &n_alloc);
+  if (st == LM_OK) st = lm::upload(t.fw, &pl->fw, &n_alloc);
   if (st == LM_OK && params->n_fft <= 4096) {
     // the shared-memory image the kernel copies in one piece
     pl->tables_bytes = lm::wave_tables_bytes(params->n_fft, params->n_mels, t.wmax);
@@ -764,7 +795,10 @@ extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan
       const int sw[2] = {t.fstart[m], t.fwidth[m]};
       put(sw, sizeof(sw));
     }
-    st = lm::upload(img, &pl->tables);
+    st = lm::upload(img, &pl->tables, &n_alloc);
+  }
+  if (st == LM_OK) {
+    if (cudaError_t e = cudaGetDevice(&pl->device); e != cudaSuccess) st = lm::cuda_fail(e);
   }
   if (st != LM_OK) {
     lm::free_plan(pl);

@@ -79,7 +79,8 @@ def test_argument_validation_needs_no_gpu(L):
     assert _call(L, NF=9000) == 2
     assert _call(L, stft=0) == 1
     assert _call(L, ws=0) == 7
-    assert _call(L, stft=0x10008) == 3      # complex64 source must be 16-byte aligned
+    assert _call(L, stft=0x10004) == 3      # complex64 source must be 8-byte aligned
+    assert _call(L, stft=0x10002) == 3
     assert _call(L, out=0x30000002) == 3
     assert _call(L, ws_bytes=8) == 7
     assert _call(L, out=0x10000 + 64) == 1  # output overlapping the input
@@ -164,3 +165,46 @@ def test_host_pipeline_validation_needs_no_gpu(L):
     assert _host_call(L, B=0) == 0
     assert _host_call(L, F=0) == 0
     assert L.lm_mel_spectrogram_host(None, 0x10000, 0, 2, 1000, 0x30000000, 0, 0, 0x40000, 1 << 26, None) == 1
+
+
+def test_eight_byte_aligned_source_passes_validation(L):
+    # A complex64 view one element into its allocation is 8 bytes off a
+    # 16-byte boundary: validation accepts it, and without a GPU the call
+    # then stops at the first CUDA call (LM_ERR_CUDA), never at alignment.
+    assert _call(L, stft=0x10008) not in (1, 3, 7)
+
+
+def test_fault_injection_entry_validation_needs_no_gpu(L):
+    f = L.lm_debug_log_mel_from_stft_withhold
+    args = (0x10000, 0x20000, 0x30000000, 2, 3, 201, 80, 0x40000, 1 << 20)
+    assert f(*args, -1, 1000000, None) == 1            # no tile to withhold
+    assert f(*args, 0, 10, None) == 1                  # wait limit below 100 us
+    assert f(*args, 0, 10 ** 10, None) == 1            # above the regular 2 s
+    assert f(0x10004, *args[1:], 0, 1000000, None) == 3  # validated like the regular call
+    assert f(*args[:3], -1, 3, 201, 80, 0x40000, 1 << 20, 0, 1000000, None) == 1
+
+
+def test_noalloc_validation_needs_no_gpu(L):
+    assert L.lm_log_mel_from_stft_noalloc(None, None, None, -1, 10, 201, 80, None) == 1
+    assert L.lm_log_mel_from_stft_noalloc(None, None, None, 2, 10, 201, 600, None) == 2
+    assert L.lm_log_mel_from_stft_noalloc(None, None, None, 0, 10, 201, 80, None) == 0
+    # larger than the scratch the library holds: refused before any pointer is used
+    assert L.lm_log_mel_from_stft_noalloc(None, None, None, 512, 20000, 201, 128, None) == 7
+    assert L.lm_log_mel_from_stft_noalloc_error(None, 0, None) == 1
+
+
+def test_forced_plan_allocation_failure_needs_no_gpu(L, monkeypatch):
+    # LOGMEL_FAULT=plan_alloc: the plan's first device allocation fails as if
+    # the device were out of memory, before any CUDA call is made for it.
+    from log_mel_spectrogram_gb300 import _native
+    p = _native.MelParams(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, center=1,
+                          power=2.0)
+    plan = ctypes.c_void_p(1234)
+    monkeypatch.setenv("LOGMEL_FAULT", "plan_alloc")
+    assert L.lm_mel_plan_create(ctypes.byref(p), ctypes.byref(plan)) == 5   # LM_ERR_OUT_OF_MEMORY
+    assert plan.value is None
+    monkeypatch.setenv("LOGMEL_FAULT", "plan_alloc:1")
+    assert L.lm_mel_plan_create(ctypes.byref(p), ctypes.byref(plan)) == 5
+    # invalid parameters are still reported first
+    bad = _native.MelParams(sample_rate=16000, n_fft=401, hop_length=160, n_mels=128, center=1, power=2.0)
+    assert L.lm_mel_plan_create(ctypes.byref(bad), ctypes.byref(plan)) == 2

@@ -274,3 +274,49 @@ def test_pad_changes_frame_count(oracle_mod):
     x = workloads.wave_sines(1, 1000, 16000, 2).numpy()
     out = oracle_mod.mel_spectrogram(x, 16000, 400, 160, 40, pad=80)
     assert out.shape == (1, 40, 1 + (1000 + 160) // 160)
+
+
+@pytest.mark.parametrize("center,normalized,win_length,pad_mode",
+                         [(True, False, None, "reflect"), (False, False, None, "reflect"),
+                          (True, True, None, "constant"), (True, True, 300, "reflect"),
+                          (False, False, 256, "reflect"), (True, False, None, "circular")])
+def test_magnitude_spectrogram_matches_torch_stft(oracle_mod, center, normalized, win_length, pad_mode):
+    # power = 1 is the magnitude |X| (torchaudio's Spectrogram with power=1),
+    # not the power and not its square root taken twice: torch.stft in
+    # float64, its .abs(), pins the oracle's power != 2 branch for the plain
+    # and the full-argument entry points alike.
+    rng = np.random.default_rng(17 + (win_length or 0))
+    n_fft, hop, T = 400, 100, 3 * 400 + 51
+    x = rng.standard_normal(T)
+    spec = oracle_mod.power_spectrogram(x, n_fft, hop, center=center, pad_mode=pad_mode, power=1.0,
+                                        win_length=win_length, normalized=normalized)
+    wl = win_length or n_fft
+    win = torch.hann_window(wl, periodic=True, dtype=torch.float64)
+    X = torch.stft(torch.from_numpy(x), n_fft, hop_length=hop, win_length=wl, window=win, center=center,
+                   pad_mode=pad_mode, return_complex=True, onesided=True)
+    if normalized:
+        X = X / win.pow(2).sum().sqrt()
+    ref = X.abs().T.numpy()
+    assert spec.shape == ref.shape
+    np.testing.assert_allclose(spec, ref, rtol=1e-9, atol=1e-9)
+    # the power-2 result is the square of the magnitude, element by element
+    spec2 = oracle_mod.power_spectrogram(x, n_fft, hop, center=center, pad_mode=pad_mode, power=2.0,
+                                         win_length=win_length, normalized=normalized)
+    np.testing.assert_allclose(spec2, ref ** 2, rtol=1e-9, atol=1e-9)
+
+
+def test_mel_spectrogram_power_one_is_filterbank_times_magnitude(oracle_mod):
+    # The magnitude branch end to end, in the configuration the GPU parity
+    # test uses it (center=False, f_min=60, f_max=7600, hop 100): the
+    # filterbank (pinned above on its own) applied to torch.stft's |X|.
+    x = workloads.wave_sines(1, 5000, 16000, seed=9)
+    got = oracle_mod.mel_spectrogram(x.numpy(), 16000, 400, 100, 80, f_min=60.0, f_max=7600.0, center=False,
+                                     power=1.0)
+    fb = oracle_mod.mel_filterbank(201, 60.0, 7600.0, 80, 16000, scale="htk")
+    win = torch.hann_window(400, periodic=True, dtype=torch.float64)
+    X = torch.stft(x[0].double(), 400, hop_length=100, window=win, center=False, return_complex=True,
+                   onesided=True)
+    ref = fb @ X.abs().numpy()
+    assert got.shape == (1,) + ref.shape
+    # the oracle rounds its output to f32 once
+    np.testing.assert_allclose(got[0].astype(np.float64), ref, rtol=2 ** -23, atol=1e-12)

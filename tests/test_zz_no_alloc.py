@@ -3,10 +3,12 @@
 Some callers cannot allocate device memory: a real-time audio thread where
 cudaMalloc may block or synchronise the device, or an application that owns
 all device memory.  This entry point runs the same kernel with its scratch in
-a fixed array inside the library.  These checks call it through the C ABI and
-compare it with the regular entry point (which takes a caller workspace),
-on two calls in a row with different shapes and inputs, so a second call
-that saw the first call's leftover scratch would show up.
+a fixed array inside the library.  These checks call it through the C ABI on
+calls in a row with different shapes: a large one, a smaller one (whose clip
+maxima would read the larger call's leftover tile slots if the scratch were
+not cleared), then the large one again.  Each result is compared with the
+CPU oracle at the f32 gate and, bit for bit, with the regular entry point
+(which takes a caller workspace).  The sticky error word must read zero.
 
 The file is named so that pytest collects it last.
 """
@@ -29,11 +31,7 @@ def L():
     import __graft_entry__
     __graft_entry__.build()
     from log_mel_spectrogram_gb300 import _native
-    lib = _native.lib()
-    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
-    lib.lm_log_mel_from_stft_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
-    lib.lm_log_mel_from_stft_noalloc.restype = ctypes.c_int
-    return lib
+    return _native.lib()
 
 
 def _stream():
@@ -62,17 +60,27 @@ def _noalloc(L, stft, W):
     return out
 
 
-def test_noalloc_matches_regular_on_two_calls_in_a_row(L):
-    cases = (((3, 301, 201, 128), 31), ((5, 777, 201, 80), 32))
+def _error_word(L, clear=1):
+    v = ctypes.c_uint32(0xffffffff)
+    rc = L.lm_log_mel_from_stft_noalloc_error(ctypes.byref(v), clear, _stream())
+    assert rc == (0 if v.value == 0 else 6)
+    return v.value
+
+
+def test_noalloc_matches_oracle_and_regular_on_calls_in_a_row(L, oracle_mod):
+    cases = (((7, 777, 201, 128), 32), ((3, 301, 201, 80), 31), ((7, 777, 201, 128), 33))
     for (B, F, NF, NM), seed in cases:
-        stft, W = workloads.stft_inputs(B, F, NF, NM, seed=seed, device="cuda")
+        stft, W = workloads.stft_inputs(B, F, NF, NM, seed=seed)
         stft[1, F // 2:] *= 1e-6  # make the clip floor matter
-        ref = _regular(L, stft, W)
-        got = _noalloc(L, stft, W)
+        s, w = stft.cuda(), W.cuda()
+        got = _noalloc(L, s, w)
+        ref_dev = _regular(L, s, w)
         torch.cuda.synchronize()
-        ref = ref.cpu().numpy().astype(np.float64)
-        got = got.cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+        assert _error_word(L) == 0
+        ref = oracle_mod.log_mel_from_stft(stft.numpy(), W.numpy()).astype(np.float64)
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(g - ref) <= ATOL + RTOL * np.abs(ref)), (B, F, NF, NM)
+        assert torch.equal(got, ref_dev)
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch(L):
