@@ -94,76 +94,126 @@ def _traffic_record():
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """Samples the SM clock, its maximum, the board power and the active
+    clock-event reasons of one GPU while the timed regions run.
 
-    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML (the driver's libnvidia-ml, read-only queries) is polled every 2 ms
+    from a thread, so even a region of a few milliseconds gets samples;
+    where NVML cannot be loaded, nvidia-smi samples every 200 ms instead.
+    Nothing here changes a setting of the GPU."""
 
-    def __init__(self, gpu_index: int):
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, pci_bus_id: str | None = None, interval_s: float = 0.002):
         self.gpu = gpu_index
+        self.pci = pci_bus_id
+        self.interval = interval_s
+        self.rows = []
+        self.windows = []
+        self.source = None
         self.proc = None
+        self.thread = None
+
+    def _nvml_open(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.pci:
+            ok = nv.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(h)) == 0
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        try:
+            reasons_fn = nv.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            reasons_fn = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return nv, h, reasons_fn
+
+    def _poll(self, nv, h, reasons_fn):
+        import ctypes
+        sm, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            t = time.time()
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and \
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+                reasons_fn(h, ctypes.byref(rs))
+                self.rows.append({"t": t, "sm": float(sm.value), "max": float(mx.value),
+                                  "power": mw.value / 1000.0,
+                                  "reasons": [n for bit, n in self.REASONS.items() if rs.value & bit]})
+            time.sleep(self.interval)
 
     def __enter__(self):
-        self.window = None
+        import threading
+        self._stop = False
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            nv, h, reasons_fn = self._nvml_open()
+            self.thread = threading.Thread(target=self._poll, args=(nv, h, reasons_fn), daemon=True)
+            self.thread.start()
+            self.source = "nvml, every 2 ms"
         except Exception:
-            self.proc = None
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.SMI_FIELDS}",
+                                              "--format=csv,noheader,nounits", "-lms", "200"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi, every 200 ms"
+            except Exception:
+                self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        self._stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=5)
         if self.proc is not None:
+            import datetime
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except Exception:
                 self.proc.kill()
-                self.out = ""
+                out = ""
+            for line in (out or "").splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    names = [n for n, v in (("hw_slowdown", parts[6]), ("hw_thermal_slowdown", parts[7]),
+                                            ("sw_thermal_slowdown", parts[8]), ("sw_power_cap", parts[9]))
+                             if v.lower() == "active"]
+                    self.rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
+                                      "power": float(parts[4]), "reasons": names})
+                except ValueError:
+                    continue
 
     def mark(self, t0: float, t1: float):
-        """Wall-clock bounds of the timed region; only samples inside count."""
-        self.window = (t0, t1)
+        """Wall-clock bounds of a timed region; only samples inside some
+        marked region count."""
+        self.windows.append((t0, t1))
 
-    def summary(self):
-        import datetime
-        rows = []
-        for line in (self.out or "").splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                row = {"t": ts, "sm": float(parts[2]), "max": float(parts[3]), "power": float(parts[4]),
-                       "hw": parts[6], "hw_th": parts[7], "sw_th": parts[8], "pcap": parts[9]}
-            except ValueError:
-                continue
-            if self.window and not (self.window[0] - 0.05 <= row["t"] <= self.window[1] + 0.05):
-                continue
-            rows.append(row)
+    def summary(self, windows=None):
+        wins = windows if windows is not None else self.windows
+        rows = [r for r in self.rows if any(w0 - 0.002 <= r["t"] <= w1 + 0.002 for w0, w1 in wins)]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        reasons = set()
-        for r in rows:
-            if r["hw"].lower() == "active":
-                reasons.add("hw_slowdown")
-            if r["hw_th"].lower() == "active":
-                reasons.add("hw_thermal_slowdown")
-            if r["sw_th"].lower() == "active":
-                reasons.add("sw_thermal_slowdown")
-            if r["pcap"].lower() == "active":
-                reasons.add("sw_power_cap")
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({n for r in rows for n in r["reasons"]})
         return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows),
-                "power_w_max": max(r["power"] for r in rows)}
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(r["power"] for r in rows),
+                "source": self.source}
 
 
-def cpu_baseline(stft_host, W_host, target_s: float = 12.0) -> dict:
-    """Times the oracle (as it stands) on a bounded sample: the given clips,
-    processed repeatedly until about target_s seconds of CPU work are done."""
+def cpu_baseline(stft_host, W_host, target_s: float = 12.0, sample_note: str = "") -> dict:
+    """Times the oracle (as it stands) on the given clips, processed
+    repeatedly until about target_s seconds of CPU work are done."""
     import oracle
     oracle.build()
     n_clips = stft_host.shape[0]
@@ -176,12 +226,34 @@ def cpu_baseline(stft_host, W_host, target_s: float = 12.0) -> dict:
         if dt >= target_s:
             break
     return {"value": done / dt, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{done} clips ({n_clips} distinct clips of the workload, repeated) in {dt:.1f} s, dense "
+            "sample": f"{done} clips ({n_clips} distinct clips{sample_note}, repeated) in {dt:.1f} s, dense "
                       "double-precision oracle, OpenMP over clips"}
 
 
+def cpu_baseline_wave(w, x_host) -> dict:
+    """Times the oracle once on the whole waveform batch."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.mel_spectrogram(x_host, w.sample_rate, w.n_fft, w.hop_length, w.n_mels, f_min=w.f_min, f_max=w.f_max,
+                           center=w.center, pad_mode=w.pad_mode, power=w.power, mel_scale=w.mel_scale, norm=w.norm,
+                           log_mel=w.log_mel, out_dtype=w.out_dtype)
+    dt = time.perf_counter() - t0
+    return {"value": w.B / dt, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the whole batch ({w.B} clips) once in {dt:.1f} s: explicit padding and frames, O(N^2) "
+                      "DFT, dense filterbank, double precision, OpenMP over clips"}
+
+
+STFT_JOBS = ("stft_small", "stft_b8", "stft")
+WAVE_JOBS = ("wave_whisper", "wave_pcm16")
+# The five workloads in the order of the benchmark's configuration list:
+# log_mel_from_stft at B=1/F=300/NM=80, B=8/F=3000/NM=80 and B=256/F=3000/NM=128
+# (the headline), then the two mel_spectrogram workloads.
+CONFIG_ORDER = ("stft_small", "stft_b8", "stft", "wave_whisper", "wave_pcm16")
+
+
 class StftJob:
-    """log_mel_from_stft on the B=256, F=3000, NF=201, NM=128 batch (or --batch B)."""
+    """log_mel_from_stft on one of the three STFT workloads (or --batch B)."""
 
     def __init__(self, lm, workloads, dev, batch, name="stft"):
         import torch
@@ -190,6 +262,7 @@ class StftJob:
         if batch and batch != w.B:
             import dataclasses
             w = dataclasses.replace(w, B=batch, name=w.name.replace(f"b{w.B}_", f"b{batch}_"))
+        self.name = name
         self.lm, self.w, self.dev = lm, w, dev
         self.stft, self.W = workloads.stft_workload_inputs(w, device=dev)
         self.out = torch.empty((w.B, w.F, w.NM), dtype=torch.float32, device=dev)
@@ -245,8 +318,26 @@ class StftJob:
         return ("stft_logmel_kernel (one cooperative launch per step, timed with the workspace memset that "
                 "precedes it)")
 
-    def cpu_sample(self):
-        return self.stft[: min(64, self.w.B)].cpu().numpy(), self.W.cpu().numpy()
+    def roofline(self, mean_launch_s, min_launch_s, peak, peak_kind, trec=None):
+        achieved = self.bytes / mean_launch_s / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": peak_kind, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                "basis": "canonical bytes / mean per-step CUDA-event time (each step's event pair brackets the "
+                         "workspace memset and the kernel)",
+                "traffic": (trec["dram_bytes_per_launch"] if trec else None),
+                "traffic_source": ("profiles/traffic.json" if trec else "stale or missing"),
+                "kernel": self.kernel_note(), "launch_ms_mean": mean_launch_s * 1e3,
+                "launch_ms_min": min_launch_s * 1e3}
+
+    def cpu_baseline(self):
+        w = self.w
+        if w.B <= 8:
+            # the whole batch, repeated for a stable figure
+            return cpu_baseline(self.stft.cpu().numpy(), self.W.cpu().numpy(), target_s=2.0,
+                                sample_note=": the whole batch")
+        n = min(64, w.B)
+        return cpu_baseline(self.stft[:n].cpu().numpy(), self.W.cpu().numpy(), target_s=12.0,
+                            sample_note=f" of the {w.B}-clip workload")
 
 
 class WaveJob:
@@ -258,6 +349,7 @@ class WaveJob:
         if batch and batch != w.B:
             import dataclasses
             w = dataclasses.replace(w, B=batch, name=w.name.replace(f"_b{w.B}_", f"_b{batch}_"))
+        self.name = name
         self.lm, self.w, self.dev = lm, w, dev
         self.x = workloads.wave_workload_inputs(w, device=dev)
         self.mel = lm.MelSpectrogram(sample_rate=w.sample_rate, n_fft=w.n_fft, hop_length=w.hop_length,
@@ -265,7 +357,8 @@ class WaveJob:
                                      pad_mode=w.pad_mode, power=w.power, mel_scale=w.mel_scale, norm=w.norm,
                                      log_mel=w.log_mel,
                                      dtype=torch.float16 if w.out_dtype == "f16" else torch.float32)
-        self.out = self.mel(self.x)
+        self.ws = torch.empty(self.mel.workspace_size(w.B, w.T, dev), dtype=torch.uint8, device=dev)
+        self.out = self.mel(self.x, workspace=self.ws)
         self.units = w.B
         self.bytes = w.canonical_bytes
         self.flops = wave_flops(w)
@@ -275,10 +368,10 @@ class WaveJob:
 
     def step(self, inputs=None):
         x = inputs[0] if inputs is not None else self.x
-        self.mel(x, out=self.out)
+        self.mel(x, out=self.out, workspace=self.ws)
 
     def error(self):
-        return 0
+        return self.lm.workspace_error(self.ws)
 
     def host_setup(self):
         import torch
@@ -306,6 +399,21 @@ class WaveJob:
     def kernel_note(self):
         return "wave_mel_kernel" + (" + logmel_clamp_kernel" if self.w.log_mel else "")
 
+    def roofline(self, mean_launch_s, min_launch_s, peak, peak_kind, trec=None):
+        achieved = self.bytes / mean_launch_s / 1e9
+        tflops = self.flops / mean_launch_s / 1e12
+        return {"bound": "alu", "achieved": tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": tflops / FP32_PEAK_TFLOPS,
+                "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz",
+                "basis": "algorithmic flops (bench.wave_flops) / mean per-step CUDA-event time",
+                "traffic": None, "kernel": self.kernel_note(),
+                "hbm_gbs": achieved, "hbm_frac_of_measured": achieved / peak,
+                "flops_per_step": self.flops,
+                "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min_launch_s * 1e3}
+
+    def cpu_baseline(self):
+        return cpu_baseline_wave(self.w, self.x.cpu().numpy())
+
 
 # FP32 FMA peak of the GPU from its unit counts and clock: 152 SMs x 128
 # FP32 lanes x 2 flops per FMA x 2.07 GHz.
@@ -323,6 +431,49 @@ def wave_flops(w) -> float:
     nf = M + 1
     per_frame = 5 * M * math.log2(M) + 10 * nf + w.n_fft + 2 * 2 * nf + (w.n_mels if w.log_mel else 0)
     return w.B * w.n_frames * per_frame
+
+
+def make_job(lm, workloads, dev, name, batch=0):
+    if name in STFT_JOBS:
+        return StftJob(lm, workloads, dev, batch, name)
+    return WaveJob(lm, workloads, dev, name, batch)
+
+
+def timed_steps(job, run_step, steps, stream, flush, dev, clk=None, soak_s=0.0):
+    """Runs `steps` steps, each bracketed by CUDA events on the launching
+    stream (an L2 flush, when given, runs between steps outside the events).
+    With soak_s > 0 the same step first runs back to back, untimed, for about
+    that long, directly before the timed steps, so that the clock samples
+    describe the state the timed steps run in.  Returns the per-step times
+    (ms), the total (ms) and the wall-clock window."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    if soak_s > 0:
+        # about soak_s of back-to-back steps, enqueued in bursts so the host
+        # stays ahead of the GPU
+        per = max(1, int(soak_s * 1e3 / 0.25))
+        for _ in range(per):
+            run_step()
+    t_begin.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        run_step()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if clk is not None:
+        clk.mark(wall0, wall1)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(launch_ms) if flush is not None else t_begin.elapsed_time(t_end)
+    return launch_ms, total_ms, (wall0, wall1)
 
 
 def run_ours(args, world, rank, local):
@@ -347,10 +498,9 @@ def run_ours(args, world, rank, local):
     barrier()
     import log_mel_spectrogram_gb300 as lm
 
-    job = StftJob(lm, workloads, dev, args.batch, args.workload) if args.workload.startswith("stft") else WaveJob(lm, workloads, dev,
-                                                                                             args.workload, args.batch)
+    job = make_job(lm, workloads, dev, args.workload, args.batch)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if job.flush_l2 else None
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
 
     for _ in range(args.warmup):
         job.step()
@@ -368,87 +518,107 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         run_step = graph.replay
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    pci = None
+    try:
+        pci = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    except Exception:
+        pass
     barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        time.sleep(0.5)  # let the sampler start before the timed region
-        wall0 = time.time()
-        t_begin = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_begin.record(stream)
-        for i in range(args.steps):
-            if flush is not None:
-                flush.fill_(i & 0xFF)
-            starts[i].record(stream)
+    with ClockSampler(local, pci) as clk:
+        time.sleep(0.05)  # the sampler is running before the timed region
+        launch_ms, total_ms, head_win = timed_steps(job, run_step, args.steps, stream,
+                                                    flush if job.flush_l2 else None, dev, clk,
+                                                    soak_s=args.clock_soak)
+        barrier()
+        if job.error():
+            raise RuntimeError("device error word set during the timed region")
+
+        # Host-observed latency of one call: wall clock from the call to the
+        # end of a synchronize, with the inputs warm in L2.  Reported beside
+        # the device-timed throughput; it is what a B=1 caller waits for.
+        lat = []
+        for _ in range(min(args.steps, 200)):
+            h0 = time.perf_counter()
             run_step()
-            ends[i].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        clk.mark(wall0, time.time())
-        barrier()
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    # Steps run back to back unless an L2 flush separates them; then only the
-    # steps themselves are counted.
-    total_ms = sum(launch_ms) if flush is not None else t_begin.elapsed_time(t_end)
-    if job.error():
-        raise RuntimeError("device error word set during the timed region")
+            torch.cuda.synchronize(dev)
+            lat.append((time.perf_counter() - h0) * 1e3)
+        lat.sort()
 
-    # Host-observed latency of one call: wall clock from the call to the end
-    # of a synchronize, with the inputs warm in L2.  Reported beside the
-    # device-timed throughput; it is what a B=1 caller waits for.
-    lat = []
-    for _ in range(min(args.steps, 200)):
-        h0 = time.perf_counter()
-        run_step()
-        torch.cuda.synchronize(dev)
-        lat.append((time.perf_counter() - h0) * 1e3)
-    lat.sort()
+        total_ms = max_over_ranks(total_ms, world, dev)
+        ms_per_step = total_ms / args.steps
+        value = job_throughput(world, job.units, args.steps, total_ms)
 
-    total_ms = max_over_ranks(total_ms, world, dev)
-    ms_per_step = total_ms / args.steps
-    value = job_throughput(world, job.units, args.steps, total_ms)
+        # End to end through the public host-buffer call: every step copies
+        # the batch in from page-locked host memory and the result back out,
+        # inside the timed region (the library overlaps the two directions and
+        # the kernels chunk by chunk).  Inputs stay in host memory; the filter
+        # matrix is a device-resident parameter, as in a serving process.  The
+        # value is the whole run's throughput; per-step times are reported
+        # beside it, since one host stall on a shared machine can weigh on a
+        # short run.
+        e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 60))
+        e2e_value = None
+        h2d = d2h = 0
+        e2e_ok = None
+        e2e_steps_ms = []
+        if e2e_steps:
+            h2d, d2h = job.host_setup()
+            job.host_step()  # warm-up: creates the library's copy streams
+            torch.cuda.synchronize(dev)
+            barrier()
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+            marks[0].record(stream)
+            for i in range(e2e_steps):
+                job.host_step()
+                marks[i + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            barrier()
+            e2e_steps_ms = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(e2e_steps))
+            e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), world, dev)
+            e2e_value = job_throughput(world, job.units, e2e_steps, e2e_ms)
+            e2e_ok = job.host_check()
+            if not e2e_ok:
+                raise RuntimeError("host-buffer result differs from the device result")
 
-    # End to end through the public host-buffer call: every step copies the
-    # batch in from page-locked host memory and the result back out, inside
-    # the timed region (the library overlaps the two directions and the
-    # kernels chunk by chunk).  Inputs stay in host memory; the filter matrix
-    # is a device-resident parameter, as in a serving process.
-    # The value is the whole run's throughput; per-step times are reported
-    # beside it, since one host stall on a shared machine can weigh on a
-    # short run.
-    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 60))
-    e2e_value = None
-    h2d = d2h = 0
-    e2e_ok = None
-    e2e_steps_ms = []
-    if e2e_steps:
-        h2d, d2h = job.host_setup()
-        job.host_step()  # warm-up: creates the library's copy streams
-        torch.cuda.synchronize(dev)
-        barrier()
-        marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
-        marks[0].record(stream)
-        for i in range(e2e_steps):
-            job.host_step()
-            marks[i + 1].record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        e2e_steps_ms = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(e2e_steps))
-        e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), world, dev)
-        e2e_value = job_throughput(world, job.units, e2e_steps, e2e_ms)
-        e2e_ok = job.host_check()
-        if not e2e_ok:
-            raise RuntimeError("host-buffer result differs from the device result")
+        # The other workloads of the configuration list, each timed on its own
+        # (L2 flushed between steps) with the oracle timed beside it.  One GPU
+        # only: under torchrun each rank would repeat them to no purpose.
+        configs = {}
+        peak, peak_kind = _peaks()
+        if world == 1 and not args.no_configs and not args.batch and args.workload == "stft":
+            for name in CONFIG_ORDER:
+                if name == args.workload:
+                    continue
+                cj = make_job(lm, workloads, dev, name)
+                for _ in range(args.warmup):
+                    cj.step()
+                torch.cuda.synchronize(dev)
+                c_ms, c_total, _ = timed_steps(cj, cj.step, args.config_steps, stream, flush, dev, clk)
+                if cj.error():
+                    raise RuntimeError(f"device error word set while timing {name}")
+                c_mean = statistics.mean(c_ms) / 1e3
+                configs[name] = {
+                    "workload": cj.w.name, "value": cj.units * args.config_steps / (c_total / 1e3),
+                    "unit": "clips/s", "steps": args.config_steps, "ms_per_step": c_total / args.config_steps,
+                    "ms_per_step_min": min(c_ms), "ms_per_step_median": statistics.median(c_ms),
+                    "gpu_launches": args.config_steps * cj.kernels, "config": cj.config(),
+                    "roofline": cj.roofline(c_mean, min(c_ms) / 1e3, peak, peak_kind),
+                }
+                del cj
+                torch.cuda.empty_cache()
+        clocks_head = clk.summary([head_win])
+        clocks_all = clk.summary()
 
-    peak, peak_kind = _peaks()
     mean_launch_s = statistics.mean(launch_ms) / 1e3
-    achieved = job.bytes / mean_launch_s / 1e9
     trec = _traffic_record() if args.workload == "stft" and not args.batch else None
     config = job.config()
     config["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     config["launch"] = "cuda graph replay" if args.graph else "eager library call"
+    if args.clock_soak > 0:
+        config["clock_soak"] = (f"{args.clock_soak:g} s of the same step back to back, untimed, directly before "
+                                "the timed steps (clock samples cover both)")
+    roof = job.roofline(mean_launch_s, min(launch_ms) / 1e3, peak, peak_kind, trec)
     result = {
         "metric": METRIC if args.workload == "stft" else f"{job.w.name} clips/sec",
         "value": value,
@@ -462,23 +632,9 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded, generated on the device; see workloads.py)",
-        "achieved_hbm_gbs": achieved,
+        "achieved_hbm_gbs": job.bytes / mean_launch_s / 1e9,
         "config": config,
-        "roofline": ({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                      "frac": achieved / peak, "peak_kind": peak_kind,
-                      "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
-                      "traffic": (trec["dram_bytes_per_launch"] if trec else None),
-                      "traffic_source": ("profiles/traffic.json" if trec else "stale or missing"),
-                      "kernel": job.kernel_note(),
-                      "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)}
-                     if not hasattr(job, "flops") else
-                     {"bound": "alu", "achieved": job.flops / mean_launch_s / 1e12, "peak": FP32_PEAK_TFLOPS,
-                      "unit": "TFLOP/s", "frac": job.flops / mean_launch_s / 1e12 / FP32_PEAK_TFLOPS,
-                      "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz",
-                      "traffic": None, "kernel": job.kernel_note(),
-                      "hbm_gbs": achieved, "hbm_frac_of_measured": achieved / peak,
-                      "flops_per_step": job.flops,
-                      "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min(launch_ms)}),
+        "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "clips/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": job.host_api() if e2e_steps else None,
@@ -490,10 +646,22 @@ def run_ours(args, world, rank, local):
         "host_latency_ms": {"median": lat[len(lat) // 2], "p90": lat[(9 * len(lat)) // 10], "samples": len(lat),
                             "launch": "cuda graph replay" if args.graph else "eager library call"},
         "gpu_launches": args.steps * job.kernels,
-        "clocks": clk.summary(),
+        "clocks": clocks_head,
+        "clocks_all_timed_regions": clocks_all,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "stft":
-        result["cpu_baseline"] = cpu_baseline(*job.cpu_sample())
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = job.cpu_baseline()
+        for name, entry in configs.items():
+            cj = make_job(lm, workloads, dev, name)
+            entry["cpu_baseline"] = cj.cpu_baseline()
+            del cj
+    if configs:
+        head = {"workload": job.w.name, "value": value, "unit": "clips/s", "steps": args.steps,
+                "ms_per_step": ms_per_step, "roofline": roof, "see": "the top-level keys of this line"}
+        if "cpu_baseline" in result:
+            head["cpu_baseline"] = result["cpu_baseline"]
+        configs[args.workload] = head
+        result["configs"] = {n: configs[n] for n in CONFIG_ORDER if n in configs}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -585,6 +753,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs on smaller cases)")
     ap.add_argument("--graph", action="store_true", help="replay one captured CUDA graph per step")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other four workloads of the configuration list (profiling runs)")
+    ap.add_argument("--config-steps", type=int, default=200,
+                    help="timed steps for each of the other workloads (L2 flushed between steps)")
+    ap.add_argument("--clock-soak", type=float, default=1.0,
+                    help="seconds of untimed back-to-back steps directly before the timed steps, so that the "
+                         "clock samples describe a GPU under this load (0 = none)")
     ap.add_argument("--workload", choices=["stft", "stft_small", "stft_b8", "wave_whisper", "wave_pcm16"],
                     default="stft",
                     help="stft (default, the headline: B=256, F=3000, NM=128), stft_small (B=1, F=300, NM=80), "

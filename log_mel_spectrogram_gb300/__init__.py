@@ -289,6 +289,16 @@ class MelSpectrogram:
                       "lm_mel_n_frames")
         return int(n.value)
 
+    def workspace_size(self, B: int, T: int, device=None) -> int:
+        """Bytes of device workspace a call on B clips of T samples needs
+        (lm_mel_workspace_size); pass such a tensor as ``workspace`` to read
+        its device error word afterwards with workspace_error()."""
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        need = ctypes.c_size_t()
+        _native.check(_native.lib().lm_mel_workspace_size(self._plan(dev), int(B), int(T), ctypes.byref(need)),
+                      "lm_mel_workspace_size")
+        return max(int(need.value), 16)
+
     def __call__(self, wave: torch.Tensor, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                  stream=None) -> torch.Tensor:
         _no_grad_inputs(wave)
