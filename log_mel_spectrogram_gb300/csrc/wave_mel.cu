@@ -50,6 +50,8 @@ struct lm_mel_plan {
   float *fw;     // [n_mels][wmax]
   unsigned char *tables;  // n_fft <= 4096: tw_m | tw_n | window | {fstart, fwidth} | fw, the shared-memory image
   uint32_t tables_bytes;  // its size, a multiple of 16
+  unsigned char *reg_tables;  // n_fft 400 and 1024: the register kernels' image (reg::Tables)
+  uint32_t reg_tables_bytes;
 };
 
 namespace lm {
@@ -102,6 +104,8 @@ __device__ __forceinline__ float load_sample(const WaveArgs &a, int64_t b, int64
   if (a.in_i16) return static_cast<float>(static_cast<const int16_t *>(a.wave)[b * a.T + s]) * (1.0f / 32768.0f);
   return static_cast<const float *>(a.wave)[b * a.T + s];
 }
+
+#include "wave_reg.cuh"
 
 template <int NFFT>
 struct WaveCfg {
@@ -724,7 +728,7 @@ void free_plan(lm_mel_plan *pl) {
   if (!pl) return;
   for (void *ptr : {static_cast<void *>(pl->window), static_cast<void *>(pl->tw_m), static_cast<void *>(pl->tw_n),
                     static_cast<void *>(pl->fstart), static_cast<void *>(pl->fwidth), static_cast<void *>(pl->fw),
-                    static_cast<void *>(pl->tables)})
+                    static_cast<void *>(pl->tables), static_cast<void *>(pl->reg_tables)})
     if (ptr) cudaFree(ptr);
   delete pl;
 }
@@ -748,6 +752,56 @@ int64_t frames_for(const lm_mel_params &p, int64_t T) {
   return 1 + (len - p.n_fft) / p.hop_length;
 }
 
+// The register kernels' table image (reg::Tables<NFFT>) for n_fft 400 and
+// 1024, in double and rounded to f32: window pairs, each stage-2 lane's
+// twiddles exp(-2 pi i b c / M) for its inputs b, each lane's untangle
+// twiddles exp(-2 pi i k / N) for its bins k, and the filter rows times
+// 2^-power (the kernels form |2X|^power; scaling by a power of two is exact)
+// with their supports.
+template <int NFFT>
+std::vector<unsigned char> reg_image(const lm_mel_params &p, const HostTables &t) {
+  using C = reg::Cfg<NFFT>;
+  using Tb = reg::Tables<NFFT>;
+  std::vector<unsigned char> img(Tb::bytes(p.n_mels, t.wmax), 0);
+  auto put2 = [&](size_t off, double re, double im) {
+    const float v[2] = {static_cast<float>(re), static_cast<float>(im)};
+    std::memcpy(img.data() + off, v, sizeof(v));
+  };
+  auto root = [&](size_t off, long num, long den) {  // exp(-2 pi i num / den)
+    const double ang = -2.0 * M_PI * static_cast<double>(num % den) / static_cast<double>(den);
+    put2(off, std::cos(ang), std::sin(ang));
+  };
+  for (int n = 0; n < C::M; ++n) put2(8 * static_cast<size_t>(n), t.window[2 * n], t.window[2 * n + 1]);
+  for (int lane = 0; lane < C::LANES2; ++lane) {
+    for (int j = 0; j < C::R2; ++j) {
+      long b, c, k;  // stage-2 input row b of the lane's column c; bin k of its j-th output
+      if (NFFT == 400) {
+        c = lane;
+        b = j;
+        k = lane + 25 * j;
+      } else {
+        c = lane >> 1;
+        const int h = lane & 1;
+        b = 2 * j + h;
+        k = c + 16 * j + 256 * h;
+      }
+      root(Tb::tw2_off() + 8 * (static_cast<size_t>(lane) * C::TWROW + j), b * c, C::M);
+      root(Tb::twu_off() + 8 * (static_cast<size_t>(lane) * C::TWROW + j), k, NFFT);
+    }
+  }
+  const float scale = p.power == 1.f ? 0.5f : 0.25f;
+  std::vector<float> fw(t.fw);
+  for (float &v : fw) v *= scale;
+  std::memcpy(img.data() + Tb::fw_off(), fw.data(), fw.size() * sizeof(float));
+  for (int m = 0; m < p.n_mels; ++m) {
+    const int sw[2] = {t.fstart[m], t.fwidth[m]};
+    std::memcpy(img.data() + Tb::fsw_off(p.n_mels, t.wmax) + 8 * static_cast<size_t>(m), sw, sizeof(sw));
+  }
+  return img;
+}
+
+// Frames per tile of the generic kernel (the register kernels' tiles are
+// taller, so a workspace sized with this holds the tile keys of either).
 int tile_frames(int n_fft) {
   WaveKernel k;
   size_t smem;
@@ -796,6 +850,12 @@ extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan
       put(sw, sizeof(sw));
     }
     st = lm::upload(img, &pl->tables, &n_alloc);
+  }
+  if (st == LM_OK && (params->n_fft == 400 || params->n_fft == 1024)) {
+    std::vector<unsigned char> img = params->n_fft == 400 ? lm::reg_image<400>(*params, t)
+                                                           : lm::reg_image<1024>(*params, t);
+    pl->reg_tables_bytes = static_cast<uint32_t>(img.size());
+    st = lm::upload(img, &pl->reg_tables, &n_alloc);
   }
   if (st == LM_OK) {
     if (cudaError_t e = cudaGetDevice(&pl->device); e != cudaSuccess) st = lm::cuda_fail(e);
@@ -877,22 +937,45 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   size_t smem = 0;
   int tf = 1;
   int nt = 0;
-  lm::pick_wave_kernel(p.n_fft, p.n_mels, plan->wmax, &kern, &smem, &tf, &nt);
-  // Two buffers for the contiguous samples of one tile of frames (plus 32
-  // bytes of alignment slack), then two mbarriers.
   const int esize = in_dtype == LM_I16 ? 2 : 4;
-  const size_t seg_bytes =
-      (static_cast<size_t>((tf - 1) * static_cast<int64_t>(p.hop_length) + p.n_fft) * esize + 32 + 127) / 128 * 128;
-  const size_t seg_offset = smem;
   lm::DeviceInfo di;
   if (lm_status st = lm::current_device_info(&di); st != LM_OK) return st;
-  bool use_seg = (reinterpret_cast<uintptr_t>(wave) & 15) == 0 &&
-                 seg_offset + 2 * seg_bytes + 32 <= static_cast<size_t>(di.max_smem_optin);
-  // Without staging (unaligned input, or a hop so long the spans do not fit)
-  // every tile gathers its samples from global memory; the two mbarriers are
-  // still reserved, right after the tables, since every CTA initialises them.
-  const size_t seg_used = use_seg ? seg_bytes : 0;
-  smem = seg_offset + 2 * seg_used + 32;  // three mbarriers
+  // n_fft 400 and 1024 run the register kernels (wave_reg.cuh) unless
+  // LOGMEL_K3=stockham selects the generic shared-memory kernel (for A/B).
+  // (The register kernels index samples of a clip with 32 bits at its edges.)
+  bool use_reg = plan->reg_tables != nullptr && T < (int64_t{1} << 31) - 2 * (p.n_fft + p.pad) &&
+                 std::strcmp(lm::env_or("LOGMEL_K3", "auto"), "stockham") != 0;
+  if (use_reg) {
+    if (p.n_fft == 400) {
+      kern = lm::reg::wave_reg_kernel<400>;
+      smem = lm::reg::smem_bytes<400>(p.n_mels, plan->wmax);
+      tf = lm::reg::Cfg<400>::TF;
+      nt = lm::reg::Cfg<400>::NT;
+    } else {
+      kern = lm::reg::wave_reg_kernel<1024>;
+      smem = lm::reg::smem_bytes<1024>(p.n_mels, plan->wmax);
+      tf = lm::reg::Cfg<1024>::TF;
+      nt = lm::reg::Cfg<1024>::NT;
+    }
+    use_reg = smem <= static_cast<size_t>(di.max_smem_optin);
+  }
+  bool use_seg = false;
+  size_t seg_offset = 0, seg_used = 0;
+  if (!use_reg) {
+    lm::pick_wave_kernel(p.n_fft, p.n_mels, plan->wmax, &kern, &smem, &tf, &nt);
+    // Two buffers for the contiguous samples of one tile of frames (plus 32
+    // bytes of alignment slack), then two mbarriers.
+    const size_t seg_bytes =
+        (static_cast<size_t>((tf - 1) * static_cast<int64_t>(p.hop_length) + p.n_fft) * esize + 32 + 127) / 128 * 128;
+    seg_offset = smem;
+    use_seg = (reinterpret_cast<uintptr_t>(wave) & 15) == 0 &&
+              seg_offset + 2 * seg_bytes + 32 <= static_cast<size_t>(di.max_smem_optin);
+    // Without staging (unaligned input, or a hop so long the spans do not fit)
+    // every tile gathers its samples from global memory; the two mbarriers are
+    // still reserved, right after the tables, since every CTA initialises them.
+    seg_used = use_seg ? seg_bytes : 0;
+    smem = seg_offset + 2 * seg_used + 32;  // three mbarriers
+  }
   if (smem > static_cast<size_t>(di.max_smem_optin)) return LM_ERR_UNSUPPORTED;
   if (lm_status st = lm::ensure_smem_attribute(reinterpret_cast<const void *>(kern), static_cast<int>(smem));
       st != LM_OK)
@@ -926,8 +1009,8 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   a.fstart = plan->fstart;
   a.fwidth = plan->fwidth;
   a.fw = plan->fw;
-  a.tables = plan->tables;
-  a.tables_bytes = plan->tables_bytes;
+  a.tables = use_reg ? plan->reg_tables : plan->tables;
+  a.tables_bytes = use_reg ? plan->reg_tables_bytes : plan->tables_bytes;
   a.err = err_word ? err_word : static_cast<uint32_t *>(workspace);
   a.next_tile = static_cast<uint32_t *>(workspace) + 1;
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(T) * esize;

@@ -1,0 +1,615 @@
+// wave_reg.cuh -- waveform -> mel kernels for n_fft 400 and 1024 whose
+// transforms run mostly in registers (included by wave_mel.cu, inside its
+// namespace, after WaveArgs and map_index).
+//
+// The real FFT of a frame is the N/2 = M point complex FFT of its folded
+// samples z[n] = x[2n] + i x[2n+1] followed by the real-input untangle
+// ("flashmel" page, "How it works": the folded R2C for powers of two; here it
+// is used for 400 points too).  M = N1 * N2 is split Cooley-Tukey style,
+// input n = N2 a + b, output k = c + N1 d:
+//
+//   stage 1  thread b (N2 per frame) loads the points b, b + N2, ... straight
+//            from the waveform -- framing, centre padding and the window folded
+//            into the loads -- runs the N1-point DFT over a in registers and
+//            writes row b of the frame's shared-memory region;
+//   stage 2  the lane of column c multiplies column c by exp(-2 pi i b c / M)
+//            and runs the N2-point DFT over b in registers, which gives bins
+//            c + N1 d.  Bin k pairs with bin M - k in the real-input untangle,
+//            and the lane that holds M - k is in the same warp: one shuffle
+//            per value.  With A = Z[k], B = Z[M - k], S = A + conj B and
+//            T = exp(-2 pi i k / N) (-i) (A - conj B), 2 X[k] = S + T (and
+//            2 X[M] = S - T at k = 0); the factor 2 is folded into the
+//            filter weights (scaled by 2^-power, exactly).
+//
+// n_fft 400:  M = 200 = 25 x 8.  Stage 1: 8 threads per frame, four frames
+//             per warp, a 25-point DFT (5 x 5) each.  Stage 2: lane c < 25
+//             of the warp, one frame at a time, an 8-point DFT.
+// n_fft 1024: M = 512 = 16 x 32.  Stage 1: 32 threads per frame, a 16-point
+//             DFT (4 x 4) each.  Stage 2: the 32-point DFT of column c is
+//             shared by lanes 2c and 2c + 1: each transforms one parity of b
+//             (16 points), the two swap results with one shuffle per value,
+//             and lane 2c + h keeps the outputs d = d' + 16 h,
+//             X = V0[d'] + (-1)^h exp(-2 pi i d' / 32) V1[d'].
+//
+// A frame stays inside one warp from its samples to its power row, so the
+// stages synchronise with __syncwarp; the CTA synchronises twice per tile of
+// TF frames (power rows complete; mel projection done with the region).  The
+// mel projection runs lanes over the frames of a band, so each band's output
+// row is stored as one run of consecutive frames.
+#pragma once
+
+namespace reg {
+
+using fft::cadd;
+using fft::cmul;
+using fft::csub;
+
+// cos(2 pi r / N) for r in the first quadrant of N = 16 and N = 32, and cos
+// and sin(2 pi m / 25): the roots of unity rounded to f32.  Called with
+// arguments that are constants after unrolling, so every value folds into an
+// immediate operand.
+__device__ __forceinline__ float cos16(int r) {
+  switch (r) {
+    case 0: return 1.0f;
+    case 1: return 0.923879533f;
+    case 2: return 0.707106781f;
+    default: return 0.382683432f;
+  }
+}
+__device__ __forceinline__ float cos32(int r) {
+  switch (r) {
+    case 0: return 1.0f;
+    case 1: return 0.98078528f;
+    case 2: return 0.923879533f;
+    case 3: return 0.831469612f;
+    case 4: return 0.707106781f;
+    case 5: return 0.555570233f;
+    case 6: return 0.382683432f;
+    default: return 0.195090322f;
+  }
+}
+__device__ __forceinline__ float cos25(int m) {
+  switch (m) {  // cos(2 pi m / 25) = cos(2 pi (25 - m) / 25)
+    case 0: return 1.0f;
+    case 1: case 24: return 0.968583161f;
+    case 2: case 23: return 0.87630668f;
+    case 3: case 22: return 0.728968627f;
+    case 4: case 21: return 0.535826795f;
+    case 5: case 20: return 0.309016994f;
+    case 6: case 19: return 0.0627905195f;
+    case 7: case 18: return -0.187381315f;
+    case 8: case 17: return -0.425779292f;
+    case 9: case 16: return -0.63742399f;
+    case 10: case 15: return -0.809016994f;
+    case 11: case 14: return -0.929776486f;
+    default: return -0.992114701f;  // 12, 13
+  }
+}
+__device__ __forceinline__ float sin25(int m) {
+  const float sgn = m > 12 ? -1.0f : 1.0f;  // sin(2 pi m / 25) = -sin(2 pi (25 - m) / 25)
+  switch (m > 12 ? 25 - m : m) {
+    case 0: return 0.0f;
+    case 1: return sgn * 0.248689887f;
+    case 2: return sgn * 0.481753674f;
+    case 3: return sgn * 0.684547106f;
+    case 4: return sgn * 0.844327926f;
+    case 5: return sgn * 0.951056516f;
+    case 6: return sgn * 0.998026728f;
+    case 7: return sgn * 0.982287251f;
+    case 8: return sgn * 0.904827052f;
+    case 9: return sgn * 0.770513243f;
+    case 10: return sgn * 0.587785252f;
+    case 11: return sgn * 0.368124553f;
+    default: return sgn * 0.125333234f;  // 12
+  }
+}
+
+// cos and sin of 2 pi m / N for N = 16 or 32 from the first quadrant.
+template <int N>
+__device__ __forceinline__ float2 cs_pow2(int m) {
+  constexpr int Q = N / 4;
+  m &= N - 1;
+  const int q = m / Q, r = m % Q;
+  // sin(2 pi r / N) = cos(2 pi (Q - r) / N)
+  const float cr = N == 16 ? cos16(r) : cos32(r);
+  const float sr = r == 0 ? 0.0f : (N == 16 ? cos16(Q - r) : cos32(Q - r));
+  switch (q) {
+    case 0: return make_float2(cr, sr);
+    case 1: return make_float2(-sr, cr);
+    case 2: return make_float2(-cr, -sr);
+    default: return make_float2(sr, -cr);
+  }
+}
+
+// z * exp(-2 pi i m / N), m a compile-time constant after unrolling; the
+// quarter turns are exact.
+template <int N>
+__device__ __forceinline__ float2 rot(float2 z, int m) {
+  m %= N;
+  if (m == 0) return z;
+  if (4 * m == N) return make_float2(z.y, -z.x);        // -i
+  if (2 * m == N) return make_float2(-z.x, -z.y);       // -1
+  if (4 * m == 3 * N) return make_float2(-z.y, z.x);    // +i
+  float2 w;
+  if constexpr (N == 25) {
+    w = make_float2(cos25(m), -sin25(m));
+  } else {
+    const float2 cs = cs_pow2<N>(m);
+    w = make_float2(cs.x, -cs.y);
+  }
+  return cmul(z, w);
+}
+
+template <int R>
+struct Dft;
+template <>
+struct Dft<4> {
+  __device__ __forceinline__ static void run(float2 (&u)[4]) { fft::Dft<4>::run(u); }
+};
+template <>
+struct Dft<5> {
+  __device__ __forceinline__ static void run(float2 (&u)[5]) { fft::Dft<5>::run(u); }
+};
+template <>
+struct Dft<8> {
+  __device__ __forceinline__ static void run(float2 (&u)[8]) { fft::Dft<8>::run(u); }
+};
+
+// In-place N1*N2-point DFT, natural order in and out: input n = N2 a + b,
+// output k = c + N1 d; N2 DFTs of size N1, the twiddles exp(-2 pi i b c / N),
+// N1 DFTs of size N2.  Every index is a compile-time constant.
+template <int N1, int N2>
+__device__ __forceinline__ void dft_ct(float2 (&u)[N1 * N2]) {
+  constexpr int N = N1 * N2;
+#pragma unroll
+  for (int b = 0; b < N2; ++b) {
+    float2 t[N1];
+#pragma unroll
+    for (int a = 0; a < N1; ++a) t[a] = u[N2 * a + b];
+    Dft<N1>::run(t);
+#pragma unroll
+    for (int c = 0; c < N1; ++c) u[N2 * c + b] = rot<N>(t[c], b * c);
+  }
+  float2 out[N];
+#pragma unroll
+  for (int c = 0; c < N1; ++c) {
+    float2 t[N2];
+#pragma unroll
+    for (int b = 0; b < N2; ++b) t[b] = u[N2 * c + b];
+    Dft<N2>::run(t);
+#pragma unroll
+    for (int d = 0; d < N2; ++d) out[c + N1 * d] = t[d];
+  }
+#pragma unroll
+  for (int k = 0; k < N; ++k) u[k] = out[k];
+}
+
+template <>
+struct Dft<16> {
+  __device__ __forceinline__ static void run(float2 (&u)[16]) { dft_ct<4, 4>(u); }
+};
+template <>
+struct Dft<32> {
+  __device__ __forceinline__ static void run(float2 (&u)[32]) { dft_ct<4, 8>(u); }
+};
+template <>
+struct Dft<25> {
+  __device__ __forceinline__ static void run(float2 (&u)[25]) { dft_ct<5, 5>(u); }
+};
+
+template <int NFFT>
+struct Cfg;
+
+template <>
+struct Cfg<400> {
+  static constexpr int M = 200;
+  static constexpr int N1 = 25;      // stage-1 DFT size
+  static constexpr int N2 = 8;       // stage-1 threads per frame, stage-2 DFT size
+  static constexpr int ROW = 25;     // complex values per stage-1 row; rows of a column hit distinct banks
+  static constexpr int TF = 32;      // frames per tile
+  static constexpr int NT = 256;
+  static constexpr int FPW = TF / (NT / 32);  // frames per warp: 4
+  static constexpr int REGION = 2 * N2 * ROW;  // floats per frame region: 400
+  static constexpr int TWROW = 10;   // float2 per lane row of the stage-2 and untangle tables (8 used)
+  static constexpr int LANES2 = 25;  // lanes with a column in stage 2
+  static constexpr int R2 = 8;       // twiddles / bins per stage-2 lane
+  static constexpr int kMinBlocks = 3;
+};
+
+template <>
+struct Cfg<1024> {
+  static constexpr int M = 512;
+  static constexpr int N1 = 16;
+  static constexpr int N2 = 32;
+  static constexpr int ROW = 17;     // 16 values per row, padded: rows of one column fall in distinct banks
+  static constexpr int TF = 16;
+  static constexpr int NT = 256;
+  static constexpr int FPW = TF / (NT / 32);  // 2
+  static constexpr int REGION = 2 * N2 * ROW;  // 1088 floats
+  static constexpr int TWROW = 18;   // float2 per lane row (16 used)
+  static constexpr int LANES2 = 32;
+  static constexpr int R2 = 16;
+  static constexpr int kMinBlocks = 2;
+};
+
+// Table image (float2 units unless noted), one bulk copy per CTA:
+//   win2 [M]             (w[2n], w[2n+1]) per point n
+//   tw2  [LANES2][TWROW] stage-2 twiddles exp(-2 pi i b c / M) of each lane
+//   twu  [LANES2][TWROW] untangle twiddles exp(-2 pi i k / N) of each lane's bins
+//   fw   [n_mels][wmax]  f32 filter rows times 2^-power (wmax a multiple of 4)
+//   fsw  [n_mels]        int2 {first bin, width}
+template <int NFFT>
+struct Tables {
+  using C = Cfg<NFFT>;
+  __host__ __device__ static constexpr size_t tw2_off() { return 8 * static_cast<size_t>(C::M); }
+  __host__ __device__ static constexpr size_t twu_off() { return tw2_off() + 8 * C::LANES2 * C::TWROW; }
+  __host__ __device__ static constexpr size_t fw_off() { return twu_off() + 8 * C::LANES2 * C::TWROW; }
+  __host__ __device__ static size_t fsw_off(int n_mels, int wmax) {
+    return fw_off() + 4 * static_cast<size_t>(n_mels) * wmax;
+  }
+  __host__ __device__ static size_t bytes(int n_mels, int wmax) {
+    return (fsw_off(n_mels, wmax) + 8 * static_cast<size_t>(n_mels) + 15) / 16 * 16;
+  }
+};
+
+// Shared memory: TF frame regions | table image | 16 bytes (tile key, abort
+// flag, next tile) | one mbarrier.
+template <int NFFT>
+size_t smem_bytes(int n_mels, int wmax) {
+  using C = Cfg<NFFT>;
+  return 4 * static_cast<size_t>(C::TF) * C::REGION + Tables<NFFT>::bytes(n_mels, wmax) + 16 + 16;
+}
+
+// For a frame that touches the signal's edge: the index in the clip of each
+// sample s0 + 2 (stride i + lane_off) + e (i < k, e < 2) after the padding
+// rule, or -1 for a padding zero, written to idx[2 i + e].  One call per
+// frame, out of line (edge frames are two or three per clip); it touches no
+// global memory, so the caller's loads of the frame then go out together.
+// All indices fit 32 bits: the host sends clips of 2^31 samples or more to
+// the generic kernel.
+static __device__ __noinline__ void edge_indices(const WaveArgs &a, int s0, int lane_off, int stride, int k,
+                                                 int *idx) {
+  const int T = static_cast<int>(a.T), pz = a.pad_zero, mode = a.pad_mode;
+  // Centre padding applies to the signal already extended by pad_zero zeros
+  // on both sides (length T + 2 pad_zero); map there, then back.
+  const int Tz = T + 2 * pz;
+  for (int j = 0; j < 2 * k; ++j) {
+    const int sz = s0 + 2 * (stride * (j >> 1) + lane_off) + (j & 1) + pz;
+    int m = sz;
+    bool zero = false;
+    if (sz < 0 || sz >= Tz) {
+      switch (mode) {
+        case LM_PAD_CONSTANT: zero = true; break;
+        case LM_PAD_REPLICATE: m = sz < 0 ? 0 : Tz - 1; break;
+        case LM_PAD_CIRCULAR: m = sz % Tz; m = m < 0 ? m + Tz : m; break;
+        default: m = sz < 0 ? -sz : 2 * (Tz - 1) - sz;  // reflect, edge not repeated
+      }
+    }
+    const int i = m - pz;
+    idx[j] = (zero || i < 0 || i >= T) ? -1 : i;
+  }
+}
+
+// The K folded points n = STRIDE i + lane_off (i < K) of one frame, windowed:
+// u[i] = (x[2n] w[2n], x[2n+1] w[2n+1]).  s0 is the frame's first sample
+// (t hop - pad_left).  One branch per frame picks the load form: interior
+// frames read sample pairs directly (8-byte f32 or 4-byte int16 pairs where
+// the pair is aligned), edge frames map each sample.  `scratch` is this
+// thread's row of at least K float2 in shared memory.
+template <int K, int STRIDE>
+__device__ __forceinline__ void load_frame(const WaveArgs &a, int64_t b, int64_t s0, int lane_off, bool wave_aligned,
+                                           const float2 *win2, float2 *scratch, float2 (&u)[K]) {
+  constexpr float kI16 = 1.0f / 32768.0f;
+  const bool interior = s0 >= 0 && s0 + 2 * (STRIDE * (K - 1) + lane_off) + 1 < a.T;
+  const bool paired = wave_aligned && (((b * a.T + s0) & 1) == 0);
+  if (interior && a.in_i16) {
+    const int16_t *w = static_cast<const int16_t *>(a.wave) + b * a.T + s0 + 2 * lane_off;
+    if (paired) {
+      const int *w2 = reinterpret_cast<const int *>(w);
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int v = __ldg(w2 + STRIDE * i);
+        u[i] = make_float2(static_cast<float>(static_cast<int16_t>(v & 0xffff)) * kI16,
+                           static_cast<float>(static_cast<int16_t>(v >> 16)) * kI16);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < K; ++i)
+        u[i] = make_float2(static_cast<float>(__ldg(w + 2 * STRIDE * i)) * kI16,
+                           static_cast<float>(__ldg(w + 2 * STRIDE * i + 1)) * kI16);
+    }
+  } else if (interior) {
+    const float *w = static_cast<const float *>(a.wave) + b * a.T + s0 + 2 * lane_off;
+    if (paired) {
+      const float2 *w2 = reinterpret_cast<const float2 *>(w);
+#pragma unroll
+      for (int i = 0; i < K; ++i) u[i] = __ldg(w2 + STRIDE * i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < K; ++i) u[i] = make_float2(__ldg(w + 2 * STRIDE * i), __ldg(w + 2 * STRIDE * i + 1));
+    }
+  } else {
+    // Indices first, into this lane's own stage-1 row (free until the DFT
+    // result overwrites it), then a gather without branches -- a clamped
+    // index and a select -- so that every load is in flight at once.
+    int *idx = reinterpret_cast<int *>(scratch);
+    edge_indices(a, static_cast<int>(s0), lane_off, STRIDE, K, idx);
+    if (a.in_i16) {
+      const int16_t *w = static_cast<const int16_t *>(a.wave) + b * a.T;
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int j0 = idx[2 * i], j1 = idx[2 * i + 1];
+        const float x0 = static_cast<float>(__ldg(w + (j0 < 0 ? 0 : j0))) * kI16;
+        const float x1 = static_cast<float>(__ldg(w + (j1 < 0 ? 0 : j1))) * kI16;
+        u[i] = make_float2(j0 < 0 ? 0.f : x0, j1 < 0 ? 0.f : x1);
+      }
+    } else {
+      const float *w = static_cast<const float *>(a.wave) + b * a.T;
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int j0 = idx[2 * i], j1 = idx[2 * i + 1];
+        const float x0 = __ldg(w + (j0 < 0 ? 0 : j0));
+        const float x1 = __ldg(w + (j1 < 0 ? 0 : j1));
+        u[i] = make_float2(j0 < 0 ? 0.f : x0, j1 < 0 ? 0.f : x1);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const float2 wv = win2[STRIDE * i + lane_off];
+    u[i] = make_float2(u[i].x * wv.x, u[i].y * wv.y);
+  }
+}
+
+// |2 X[k]|^power from A = Z[k], B = Z[M - k] and tw = exp(-2 pi i k / N):
+// 2 X[k] = S + T with S = A + conj B, T = tw (-i) (A - conj B).  For k = 0
+// (A = B = Z[0], tw = 1), *top receives |2 X[M]|^power = |S - T|^power.
+template <bool kTop>
+__device__ __forceinline__ float untangle(float2 A, float2 B, float2 tw, bool power_one, float *top = nullptr) {
+  const float2 S = make_float2(A.x + B.x, A.y - B.y);
+  const float2 D = make_float2(A.x - B.x, A.y + B.y);
+  const float2 T = make_float2(fmaf(tw.x, D.y, tw.y * D.x), fmaf(tw.y, D.y, -tw.x * D.x));
+  const float2 P = make_float2(S.x + T.x, S.y + T.y);
+  float p = fmaf(P.x, P.x, P.y * P.y);
+  if (power_one) p = sqrtf(p);
+  if constexpr (kTop) {
+    const float2 Q = make_float2(S.x - T.x, S.y - T.y);
+    float q = fmaf(Q.x, Q.x, Q.y * Q.y);
+    if (power_one) q = sqrtf(q);
+    *top = q;
+  }
+  return p;
+}
+
+template <int NFFT>
+__global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg_kernel(const WaveArgs a) {
+  using C = Cfg<NFFT>;
+  using Tb = Tables<NFFT>;
+  constexpr int M = C::M, TF = C::TF, NT = C::NT, REGION = C::REGION;
+  extern __shared__ __align__(16) unsigned char smem[];
+  float *regions = reinterpret_cast<float *>(smem);
+  unsigned char *tables = smem + 4 * static_cast<size_t>(TF) * REGION;
+  const float2 *win2 = reinterpret_cast<const float2 *>(tables);
+  const float2 *tw2 = reinterpret_cast<const float2 *>(tables + Tb::tw2_off());
+  const float2 *twu = reinterpret_cast<const float2 *>(tables + Tb::twu_off());
+  const float *fw = reinterpret_cast<const float *>(tables + Tb::fw_off());
+  const int2 *fsw = reinterpret_cast<const int2 *>(tables + Tb::fsw_off(a.n_mels, a.wmax));
+  uint32_t *blk_key = reinterpret_cast<uint32_t *>(tables + a.tables_bytes);
+  int *abort_flag_p = reinterpret_cast<int *>(blk_key + 1);
+  volatile int *next_s = reinterpret_cast<volatile int *>(blk_key + 2);
+  uint64_t *tbar = reinterpret_cast<uint64_t *>(blk_key + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(tbar, 1);
+    *abort_flag_p = 0;
+    *blk_key = 0u;
+    fence_mbar_init();
+    mbar_arrive_expect_tx(tbar, a.tables_bytes);
+    bulk_g2s_plain(tables, a.tables, a.tables_bytes, tbar);
+  }
+  __syncthreads();  // the barrier is initialised
+  {
+    // Without the tables every later shared-memory index is meaningless: if
+    // any thread's wait gave up, the whole CTA stops (after the copy lands).
+    const bool ok = mbar_wait(tbar, 0, abort_flag_p, a.err);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) mbar_wait_drain(tbar, 0, a.err);
+      return;
+    }
+  }
+
+  const int64_t n_tiles = a.B * a.tiles_per_clip;
+  for (int64_t tile = blockIdx.x, nxt; tile < n_tiles; tile = nxt) {
+    const int64_t b = tile / a.tiles_per_clip;
+    const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(TF);
+    const int64_t left = a.n_frames - t0;
+    const int nf = left < TF ? static_cast<int>(left) : TF;
+    const bool wave_pair_aligned =
+        (reinterpret_cast<uintptr_t>(a.wave) & (a.in_i16 ? 3u : 7u)) == 0;
+
+    // ---------------- stage 1: framing + N1-point DFTs ----------------
+    if constexpr (NFFT == 400) {
+      const int q = lane >> 3, bb = lane & 7;
+      const int f = warp * C::FPW + q;
+      if (f < nf) {
+        float2 u[25];
+        float2 *row = reinterpret_cast<float2 *>(regions + f * REGION) + bb * C::ROW;
+        load_frame<25, 8>(a, b, (t0 + f) * a.hop - a.pad_left, bb, wave_pair_aligned, win2, row, u);
+        Dft<25>::run(u);
+#pragma unroll
+        for (int c = 0; c < 25; ++c) row[c] = u[c];
+      }
+    } else {
+#pragma unroll 1
+      for (int q = 0; q < C::FPW; ++q) {
+        const int f = warp * C::FPW + q;
+        if (f >= nf) break;
+        float2 u[16];
+        float2 *row = reinterpret_cast<float2 *>(regions + f * REGION) + lane * C::ROW;
+        load_frame<16, 32>(a, b, (t0 + f) * a.hop - a.pad_left, lane, wave_pair_aligned, win2, row, u);
+        Dft<16>::run(u);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) row[c] = u[c];
+      }
+    }
+    __syncwarp();
+
+    // ------- stage 2: N2-point DFTs, untangle, |2X|^power into the power rows -------
+    // Frame f's power row sits inside its own region, at float offset
+    // f * REGION + shift(f): lanes over the frames of one bin then hit
+    // distinct banks in the mel projection.
+    auto prow = [&](int f) { return regions + f * REGION + (NFFT == 400 ? (f >> 1) : f); };
+#pragma unroll 1
+    for (int q = 0; q < C::FPW; ++q) {
+      const int f = warp * C::FPW + q;
+      if (f >= nf) break;  // warp-uniform
+      const float2 *Y = reinterpret_cast<const float2 *>(regions + f * REGION);
+      const uint32_t pw = smem_u32(prow(f));
+      if constexpr (NFFT == 400) {
+        const int c = lane;  // column; lanes 25..31 idle
+        const bool act = c < C::LANES2;
+        float2 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = act ? Y[i * C::ROW + c] : make_float2(0.f, 0.f);
+        const float2 *tr = tw2 + (act ? c : 0) * C::TWROW;
+#pragma unroll
+        for (int i = 1; i < 8; ++i) v[i] = cmul(v[i], tr[i]);
+        Dft<8>::run(v);  // v[d] = Z[c + 25 d]
+        // Z[M - k] for k = c + 25 d is lane 25 - c's value 7 - d (lane 0:
+        // its own value (8 - d) mod 8).
+        const int src = (c >= 1 && act) ? 25 - c : lane;
+        float2 r[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          r[i].x = __shfl_sync(0xffffffffu, v[i].x, src);
+          r[i].y = __shfl_sync(0xffffffffu, v[i].y, src);
+        }
+        __syncwarp();  // every lane has read the region before power rows overwrite it
+        if (act) {
+          const uint32_t tu = smem_u32(twu + c * C::TWROW);
+          const uint32_t pc = pw + 4u * static_cast<uint32_t>(c);
+          if (c == 0) {
+            float top;
+            sts_f32(pc, untangle<true>(v[0], v[0], lds_f32x2(tu), a.power_is_one, &top));
+            sts_f32(pw + 4u * M, top);
+          } else {
+            sts_f32(pc, untangle<false>(v[0], r[7], lds_f32x2(tu), a.power_is_one));
+          }
+#pragma unroll
+          for (int d = 1; d < 8; ++d) {
+            const float2 Bz = c != 0 ? r[7 - d] : v[8 - d];
+            sts_f32(pc + 4u * (25 * d), untangle<false>(v[d], Bz, lds_f32x2(tu + 8u * d), a.power_is_one));
+          }
+        }
+      } else {
+        const int c = lane >> 1, h = lane & 1;
+        float2 v[16];
+        const float2 *tr = tw2 + lane * C::TWROW;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) v[m] = cmul(Y[(2 * m + h) * C::ROW + c], tr[m]);
+        Dft<16>::run(v);  // V_h[d']
+        // Lane 2c + h keeps d = d' + 16 h: X = V0 + (-1)^h W32^d' V1.
+#pragma unroll
+        for (int d = 0; d < 16; ++d) {
+          float2 o;
+          o.x = __shfl_xor_sync(0xffffffffu, v[d].x, 1);
+          o.y = __shfl_xor_sync(0xffffffffu, v[d].y, 1);
+          const float2 V0 = h ? o : v[d];
+          const float2 V1 = h ? v[d] : o;
+          const float2 T = rot<32>(V1, d);
+          v[d] = h ? csub(V0, T) : cadd(V0, T);  // Z[c + 16 d + 256 h]
+        }
+        // Z[M - k] is lane (lane >= 2 ? 33 - lane : 1 - lane)'s value 15 - d
+        // (lanes 0 and 1: value (16 - d) mod 16, and d = 0 pairs with itself).
+        const int src = lane >= 2 ? 33 - lane : 1 - lane;
+        float2 r[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          r[i].x = __shfl_sync(0xffffffffu, v[i].x, src);
+          r[i].y = __shfl_sync(0xffffffffu, v[i].y, src);
+        }
+        __syncwarp();
+        const uint32_t tu = smem_u32(twu + lane * C::TWROW);
+        const uint32_t pc = pw + 4u * static_cast<uint32_t>(c + 256 * h);
+        if (lane == 0) {
+          float top;
+          sts_f32(pc, untangle<true>(v[0], v[0], lds_f32x2(tu), a.power_is_one, &top));
+          sts_f32(pw + 4u * M, top);
+        } else {
+          sts_f32(pc, untangle<false>(v[0], lane >= 2 ? r[15] : v[0], lds_f32x2(tu), a.power_is_one));
+        }
+#pragma unroll
+        for (int d = 1; d < 16; ++d) {
+          const float2 Bz = lane >= 2 ? r[15 - d] : r[16 - d];
+          sts_f32(pc + 4u * (16 * d), untangle<false>(v[d], Bz, lds_f32x2(tu + 8u * d), a.power_is_one));
+        }
+      }
+    }
+    if (threadIdx.x == 0) *next_s = static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
+    __syncthreads();  // every power row of the tile is complete
+
+    // ---------------- mel projection and store ----------------
+    // Lanes run over frames (TF = 32: a warp per band; TF = 16: a half-warp
+    // per band), band groups over the rest.
+    float lmax = -INFINITY;
+    {
+      constexpr int LF = TF < 32 ? TF : 32;      // lanes per band
+      constexpr int NG = NT / LF;                // band groups
+      const int f = static_cast<int>(threadIdx.x) % LF;
+      const int g = static_cast<int>(threadIdx.x) / LF;
+      if (f < nf) {
+        const uint32_t pa0 = smem_u32(prow(f));
+        const int64_t orow0 = b * a.n_mels * a.n_frames + t0 + f;
+        for (int m = g; m < a.n_mels; m += NG) {
+          const int2 sw = fsw[m];
+          const uint32_t pa = pa0 + static_cast<uint32_t>(sw.x) * 4u;
+          const uint32_t wa = smem_u32(fw + m * a.wmax);
+          float acc = 0.f;
+          int t = 0;
+          for (; t + 4 <= sw.y; t += 4) {
+            const float4 w4 = lds_f32x4(wa + 4 * t);
+            acc = fmaf(w4.x, lds_f32(pa + 4 * t), acc);
+            acc = fmaf(w4.y, lds_f32(pa + 4 * t + 4), acc);
+            acc = fmaf(w4.z, lds_f32(pa + 4 * t + 8), acc);
+            acc = fmaf(w4.w, lds_f32(pa + 4 * t + 12), acc);
+          }
+          if (t < sw.y) {
+            const float4 w4 = lds_f32x4(wa + 4 * t);
+            acc = fmaf(w4.x, lds_f32(pa + 4 * t), acc);
+            if (t + 1 < sw.y) acc = fmaf(w4.y, lds_f32(pa + 4 * t + 4), acc);
+            if (t + 2 < sw.y) acc = fmaf(w4.z, lds_f32(pa + 4 * t + 8), acc);
+          }
+          const int64_t o = orow0 + static_cast<int64_t>(m) * a.n_frames;
+          if (a.log_mel) {
+            float l2;
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(fmaxf(acc, 1e-10f)));
+            const float v = l2 * 0.30102999566398120f;  // log10(x) = log2(x) log10(2)
+            lmax = fmaxf(lmax, v);
+            static_cast<float *>(a.out)[o] = v;
+          } else if (a.out_f16) {
+            static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
+          } else {
+            static_cast<float *>(a.out)[o] = acc;
+          }
+        }
+      }
+    }
+    if (a.log_mel) {
+      const uint32_t key = __reduce_max_sync(0xffffffffu, float_to_ordered(lmax));
+      if (lane == 0) atomicMax(blk_key, key);
+    }
+    nxt = *next_s;
+    __syncthreads();  // the regions are free for the next tile; the tile key is complete
+    if (a.log_mel && threadIdx.x == 0) {
+      a.tile_key[tile] = *blk_key;
+      *blk_key = 0u;
+    }
+  }
+  // This CTA is done: a programmatically dependent epilogue may be scheduled
+  // (it still waits for the whole grid before reading).
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+}  // namespace reg
