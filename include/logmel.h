@@ -307,7 +307,8 @@ lm_status lm_mel_plan_destroy(lm_mel_plan *plan);
 lm_status lm_mel_n_frames(const lm_mel_plan *plan, int64_t T, int64_t *n_frames);
 
 /* Bytes of device workspace lm_mel_spectrogram needs for B clips of T
- * samples (a header and, for log plans, one u32 per tile of frames). */
+ * samples (a header and, for log plans, one u32 per tile of frames and two
+ * per clip). */
 lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, int64_t T, size_t *bytes);
 
 /*
@@ -318,6 +319,11 @@ lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, int64_t T, s
  *   out       device, [B][n_mels][n_frames] f32 (LM_F32) or f16 (LM_F16),
  *             4-byte aligned.  log_mel plans require LM_F32.
  *   workspace device, >= lm_mel_workspace_size(plan, B, T) bytes.
+ *
+ * Log plans run as one launch where n_fft is 400 or 1024 (the clip floor
+ * and rescale are applied by the same cooperative grid; set
+ * LOGMEL_K3_EPILOGUE=separate for a second, clamp-only launch instead) and
+ * as two launches otherwise.  Non-log plans are one launch.
  *
  * Errors: LM_ERR_INVALID_ARG (null pointers, T too short for reflect
  * padding, n_frames < 1), LM_ERR_UNSUPPORTED (dtype combination),

@@ -75,6 +75,9 @@ struct WaveArgs {
   int32_t n_mels, wmax, tiles_per_clip, TF;
   uint32_t *err;           // device error word (workspace header)
   uint32_t *next_tile;     // tile counter (workspace header), zero at launch
+  uint32_t *clip_key;      // [B] fused log epilogue: the clip's maximum key (0 = none yet)
+  uint32_t *clip_done;     // [B] fused log epilogue: tiles of the clip whose maximum is folded in
+  int32_t fused;           // 1: the register kernel applies the clip floor and rescale itself
   uint64_t total_bytes;    // B * T * sample size
   uint32_t seg_offset;     // shared-memory offset of the two sample-span buffers
   uint32_t seg_bytes;      // bytes per span buffer (multiple of 128)
@@ -890,7 +893,10 @@ extern "C" lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, i
   const int64_t nfr = lm::frames_for(plan->p, T);
   const int tf = lm::tile_frames(plan->p.n_fft);
   const int64_t tpc = nfr > 0 ? (nfr + tf - 1) / tf : 0;
-  *bytes = (lm::kWorkspaceHeaderBytes + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + 255) / 256 * 256;
+  // header | tile keys [B * tpc] | (log plans) clip keys [B] | clip counters [B]
+  const size_t clip_arrays = plan->p.log_mel ? 2 * static_cast<size_t>(B) * sizeof(uint32_t) : 0;
+  *bytes = (lm::kWorkspaceHeaderBytes + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + clip_arrays + 255) / 256 *
+           256;
   return LM_OK;
 }
 
@@ -1020,9 +1026,35 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   const int64_t n_tiles = B * a.tiles_per_clip;
   if (n_tiles > INT32_MAX / 2) return LM_ERR_UNSUPPORTED;  // tile indices and the counter are 32-bit
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_tiles, static_cast<int64_t>(di.sm_count) * per_sm));
+  // Log plans on the register kernels apply the clip floor and rescale in the
+  // same launch (one cooperative grid; its CTAs wait for each other's clip
+  // maxima) when every tile fits some CTA's pending list; otherwise, or with
+  // LOGMEL_K3_EPILOGUE=separate, the clamp kernel runs after it.
+  {
+    const int64_t tpc_ws = (nfr + lm::tile_frames(p.n_fft) - 1) / lm::tile_frames(p.n_fft);  // the workspace layout's
+    a.clip_key = a.tile_key + B * tpc_ws;
+    a.clip_done = a.clip_key + B;
+    a.fused = use_reg && a.log_mel && static_cast<int64_t>(grid) * lm::reg::kPendMax >= n_tiles &&
+              std::strcmp(lm::env_or("LOGMEL_K3_EPILOGUE", "auto"), "separate") != 0;
+  }
   cudaStream_t s = stream;
-  // Clears the device error word (and, for log plans, the tile slots).
+  // Clears the device error word (and, for log plans, the tile slots and the
+  // clip keys and counters).
   LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, a.log_mel ? need : lm::kWorkspaceHeaderBytes, s));
+  if (a.fused) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(static_cast<unsigned>(nt));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    LM_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a));
+    return LM_OK;
+  }
   kern<<<grid, static_cast<unsigned>(nt), smem, s>>>(a);
   LM_CUDA_TRY(cudaGetLastError());
   if (a.log_mel) {

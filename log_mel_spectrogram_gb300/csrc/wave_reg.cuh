@@ -36,6 +36,15 @@
 // TF frames (power rows complete; mel projection done with the region).  The
 // mel projection runs lanes over the frames of a band, so each band's output
 // row is stored as one run of consecutive frames.
+//
+// Log plans finish in the same launch (the KBench spec's per-clip floor and
+// rescale, its "clip-resident" design note): each tile folds its maximum log
+// value into its clip's key and then counts itself into the clip's counter
+// with release order; a CTA keeps the tiles it computed in a short list, and
+// after its last tile waits (bounded) for each listed clip's counter to
+// complete and floors and rescales those tiles in place while they are still
+// in L2.  The grid is cooperative, tiles are claimed in order, and no CTA
+// waits before it has computed every tile it claimed, so every wait ends.
 #pragma once
 
 namespace reg {
@@ -252,13 +261,23 @@ struct Tables {
   }
 };
 
+// Fused log epilogue: tiles a CTA may hold until their clips' maxima are
+// known (the host keeps grid x kPendMax >= tiles, else it launches the
+// separate clamp kernel).
+constexpr int kPendMax = 32;
+
 // Shared memory: TF frame regions | table image | 16 bytes (tile key, abort
-// flag, next tile) | one mbarrier.
+// flag, next tile, pending count) | one mbarrier and the clip floor |
+// pending tiles [kPendMax].
 template <int NFFT>
 size_t smem_bytes(int n_mels, int wmax) {
   using C = Cfg<NFFT>;
-  return 4 * static_cast<size_t>(C::TF) * C::REGION + Tables<NFFT>::bytes(n_mels, wmax) + 16 + 16;
+  return 4 * static_cast<size_t>(C::TF) * C::REGION + Tables<NFFT>::bytes(n_mels, wmax) + 16 + 16 + 4 * kPendMax;
 }
+
+// (max(ls, floor) + 4) / 4 for floor = hi - 8; fma(x, 1/4, 1) rounds exactly
+// like (x + 4) / 4.
+__device__ __forceinline__ float rescale_log(float ls, float floor_v) { return fmaf(fmaxf(ls, floor_v), 0.25f, 1.0f); }
 
 // For a frame that touches the signal's edge: the index in the clip of each
 // sample s0 + 2 (stride i + lane_off) + e (i < k, e < 2) after the padding
@@ -397,7 +416,10 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
   uint32_t *blk_key = reinterpret_cast<uint32_t *>(tables + a.tables_bytes);
   int *abort_flag_p = reinterpret_cast<int *>(blk_key + 1);
   volatile int *next_s = reinterpret_cast<volatile int *>(blk_key + 2);
+  volatile int *n_pend_s = reinterpret_cast<volatile int *>(blk_key + 3);
   uint64_t *tbar = reinterpret_cast<uint64_t *>(blk_key + 4);
+  volatile float *floor_s = reinterpret_cast<volatile float *>(blk_key + 6);
+  int *pend = reinterpret_cast<int *>(blk_key + 8);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -421,11 +443,14 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
   }
 
   const int64_t n_tiles = a.B * a.tiles_per_clip;
+  const bool fused = a.log_mel && a.fused;
+  int n_pend = 0;  // thread 0: tiles held for the fused epilogue
   for (int64_t tile = blockIdx.x, nxt; tile < n_tiles; tile = nxt) {
     const int64_t b = tile / a.tiles_per_clip;
-    const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(TF);
+    // a.TF (= TF) frames per tile
+    const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(a.TF);
     const int64_t left = a.n_frames - t0;
-    const int nf = left < TF ? static_cast<int>(left) : TF;
+    const int nf = left < a.TF ? static_cast<int>(left) : a.TF;
     const bool wave_pair_aligned =
         (reinterpret_cast<uintptr_t>(a.wave) & (a.in_i16 ? 3u : 7u)) == 0;
 
@@ -547,7 +572,12 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
         }
       }
     }
-    if (threadIdx.x == 0) *next_s = static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
+    if (threadIdx.x == 0) {
+      // A CTA whose pending list would overflow claims no further tile; the
+      // others take the rest (grid x kPendMax >= tiles).
+      *next_s = (fused && n_pend + 1 >= kPendMax) ? static_cast<int>(n_tiles)
+                                                  : static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
+    }
     __syncthreads();  // every power row of the tile is complete
 
     // ---------------- mel projection and store ----------------
@@ -603,8 +633,78 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
     nxt = *next_s;
     __syncthreads();  // the regions are free for the next tile; the tile key is complete
     if (a.log_mel && threadIdx.x == 0) {
-      a.tile_key[tile] = *blk_key;
+      if (fused) {
+        // Fold the tile maximum into its clip's, then count the tile in with
+        // release order: a CTA that sees the count complete sees the maximum.
+        atomicMax(a.clip_key + b, *blk_key);
+        red_add_release_gpu(a.clip_done + b, 1u);
+        pend[n_pend++] = static_cast<int>(tile);
+      } else {
+        a.tile_key[tile] = *blk_key;
+      }
       *blk_key = 0u;
+    }
+  }
+
+  if (fused) {
+    // Fused epilogue: once every tile of a held tile's clip has folded in its
+    // maximum, floor and rescale the held tile in place (its log values are
+    // still in L2).  Waits only start after this CTA's last tile, so every
+    // tile a wait depends on is computed by a CTA that is not waiting.
+    if (threadIdx.x == 0) *n_pend_s = n_pend;
+    __syncthreads();
+    const int np = *n_pend_s;
+    for (int i = 0; i < np; ++i) {
+      const int64_t tile = pend[i];
+      const int64_t b = tile / a.tiles_per_clip;
+      if (threadIdx.x == 0) {
+        bool ok = true;
+        uint64_t tw0 = 0;
+        for (uint32_t it = 0; ld_acquire_gpu(a.clip_done + b) < static_cast<uint32_t>(a.tiles_per_clip); ++it) {
+          if ((it & 15u) == 15u) {
+            const uint64_t now = global_timer_ns();
+            if (tw0 == 0) {
+              tw0 = now;
+            } else if (now - tw0 > kWaitTimeoutNs) {
+              atomicOr(a.err, kErrClipTimeout);
+              ok = false;
+              break;
+            }
+          }
+          __nanosleep(128);
+        }
+        *floor_s = ok ? ordered_to_float(ld_relaxed_gpu(a.clip_key + b)) - 8.0f : __int_as_float(0x7fc00000);
+      }
+      __syncthreads();
+      const float floor_v = *floor_s;
+      if (floor_v != floor_v) break;  // a wait gave up (the error word says so): leave the rest as log values
+      const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(a.TF);
+      const int64_t left = a.n_frames - t0;
+      const int nf = left < a.TF ? static_cast<int>(left) : a.TF;
+      constexpr int LF = TF < 32 ? TF : 32;
+      constexpr int NG = NT / LF;
+      const int f = static_cast<int>(threadIdx.x) % LF;
+      if (f < nf) {
+        // Up to U bands per thread and pass, every load before any store, so
+        // the L2 round trips overlap (in place, one at a time they would
+        // serialise).
+        constexpr int U = 16;
+        float *o = static_cast<float *>(a.out) + b * a.n_mels * a.n_frames + t0 + f;
+        for (int m0 = static_cast<int>(threadIdx.x) / LF; m0 < a.n_mels; m0 += NG * U) {
+          float v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int m = m0 + u * NG;
+            v[u] = m < a.n_mels ? o[static_cast<int64_t>(m) * a.n_frames] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int m = m0 + u * NG;
+            if (m < a.n_mels) o[static_cast<int64_t>(m) * a.n_frames] = rescale_log(v[u], floor_v);
+          }
+        }
+      }
+      __syncthreads();  // floor_s is rewritten for the next held tile
     }
   }
   // This CTA is done: a programmatically dependent epilogue may be scheduled

@@ -201,3 +201,43 @@ def test_repeat_calls_are_bitwise_identical(lm):
         torch.cuda.synchronize()
         assert torch.equal(a, b)
         m.close()
+
+
+@pytest.mark.parametrize("n_fft,hop,sr,f_max", [(400, 160, 16000, 8000.0), (1024, 256, 22050, 11025.0)])
+def test_fused_and_separate_log_epilogues_agree(lm, oracle_mod, monkeypatch, n_fft, hop, sr, f_max):
+    # The register kernels floor and rescale log plans in the same launch
+    # (the clip maximum gathered across CTAs); LOGMEL_K3_EPILOGUE=separate
+    # runs the clamp kernel after them instead.  Both give the same bits, and
+    # the oracle's values.
+    x = workloads.wave_sines(5, 37000, sr, seed=n_fft + 5)
+    x[2, 20000:] *= 1e-5  # the clip floor matters
+    args = dict(sample_rate=sr, n_fft=n_fft, hop_length=hop, n_mels=128, f_max=f_max, log_mel=True)
+    m = lm.MelSpectrogram(**args)
+    fused = m(x.cuda())
+    monkeypatch.setenv("LOGMEL_K3_EPILOGUE", "separate")
+    sep = m(x.cuda())
+    torch.cuda.synchronize()
+    m.close()
+    assert torch.equal(fused, sep)
+    ref = oracle_mod.mel_spectrogram(x.numpy(), sr, n_fft, hop, 128, f_max=f_max, log_mel=True)
+    _gate(fused.cpu().numpy(), ref, 1e-4)
+
+
+def test_fused_log_epilogue_with_full_pending_lists(lm, oracle_mod, monkeypatch):
+    # 442 clips of 10 s: 32 tiles of 32 frames each, about 31 per CTA of the
+    # 400-point kernel, so CTAs fill their lists of held tiles and stop
+    # claiming; the result must not change.
+    x = workloads.wave_sines(442, 160000, 16000, seed=77, device="cuda")
+    args = dict(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, log_mel=True)
+    m = lm.MelSpectrogram(**args)
+    ws = torch.empty(m.workspace_size(442, 160000), dtype=torch.uint8, device="cuda")
+    fused = m(x, workspace=ws)
+    assert lm.workspace_error(ws) == 0
+    monkeypatch.setenv("LOGMEL_K3_EPILOGUE", "separate")
+    sep = m(x, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, sep)
+    for b in (0, 441):
+        ref = oracle_mod.mel_spectrogram(x[b:b + 1].cpu().numpy(), 16000, 400, 160, 128, f_max=8000.0, log_mel=True)
+        _gate(fused[b:b + 1].cpu().numpy(), ref, 1e-4)
+    m.close()
