@@ -311,7 +311,8 @@ class StftJob:
                 "canonical_bytes_per_step": w.canonical_bytes,
                 "l2": ("flushed between timed steps by writing 512 MB (outside the per-step events)" if self.flush_l2
                        else f"no flush: each step streams {w.canonical_bytes / 1e9:.2f} GB, more than 4x the L2"),
-                "variant": "resident" if info["resident"] else "twopass", "grid": info["grid"],
+                "variant": (f"cluster x{info['cluster']}" if info.get("cluster") else
+                            "resident" if info["resident"] else "twopass"), "grid": info["grid"],
                 "frames_per_tile": info["frames_per_tile"], "stages": info["stages"], "lag": info["lag"]}
 
     def kernel_note(self):

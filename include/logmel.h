@@ -121,16 +121,26 @@ lm_status lm_log_mel_from_stft(const void *stft, const float *mel_filters, float
 
 /* How lm_log_mel_from_stft will run a problem of this shape on the current
  * device (pure host-side planning; no work is enqueued).  Fields:
- *   resident       1 = single cooperative launch that keeps each tile's log
- *                  values on chip until its clip maximum is known and writes
- *                  the output once; 0 = two launches (log values, then the
- *                  in-place floor/rescale pass).
+ *   resident       1 = single cooperative launch, one persistent CTA per SM,
+ *                  that keeps each tile's log values on chip until its clip
+ *                  maximum is known and writes the output once.
+ *   cluster        > 0 = single launch of one thread-block cluster of this
+ *                  many CTAs per clip (small batches, when the device runs
+ *                  every clip's cluster at once): each CTA keeps its share
+ *                  of the clip's log values in shared memory, the cluster
+ *                  exchanges maxima through distributed shared memory, and
+ *                  the output is written once.
+ *                  resident = 0 and cluster = 0: two launches (log values,
+ *                  then the in-place floor/rescale pass).
  *   kernels        kernel launches per call (1 or 2; plus one memset of the
- *                  workspace header and clip counters).
- *   grid           CTAs of the main kernel (persistent, at most one per SM).
+ *                  workspace).
+ *   grid           CTAs of the main kernel.
  *   frames_per_tile, stages, lag: tile height, shared-memory ring depth, and
  *                  how many tiles each thread holds back before writing.
- *   smem_bytes     dynamic shared memory per CTA. */
+ *   smem_bytes     dynamic shared memory per CTA.
+ * LOGMEL_K1_VARIANT=resident|twopass|cluster forces a variant, and
+ * =nocluster leaves the cluster variant out (A/B); a forced variant that
+ * cannot run returns LM_ERR_UNSUPPORTED. */
 typedef struct lm_stft_launch_info {
   int32_t resident;
   int32_t kernels;
@@ -139,6 +149,8 @@ typedef struct lm_stft_launch_info {
   int32_t stages;
   int32_t lag;
   int64_t smem_bytes;
+  int32_t cluster;
+  int32_t reserved;
 } lm_stft_launch_info;
 
 lm_status lm_log_mel_from_stft_describe(int64_t B, int64_t F, int32_t NF, int32_t NM,
@@ -241,7 +253,8 @@ lm_status lm_workspace_error(const void *workspace, size_t workspace_bytes, uint
 /* ---- Fault injection for tests of the bounded waits (the source pages
  * have no counterpart) ----
  *
- * Runs lm_log_mel_from_stft (same arguments, results and errors) with two
+ * Runs lm_log_mel_from_stft on its one-CTA-per-SM kernel (same arguments,
+ * results and errors; the cluster variant has no cross-CTA waits) with two
  * changes that make one of its cross-CTA waits run out on purpose, so that
  * a test can check that the kernel gives up cleanly instead of hanging:
  *   withheld_tile  the maximum of this tile of frames is never published

@@ -35,7 +35,7 @@ class LogmelError(RuntimeError):
 class StftLaunchInfo(ctypes.Structure):
     _fields_ = [("resident", ctypes.c_int32), ("kernels", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("frames_per_tile", ctypes.c_int32), ("stages", ctypes.c_int32), ("lag", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int64)]
+                ("smem_bytes", ctypes.c_int64), ("cluster", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class MelParams(ctypes.Structure):

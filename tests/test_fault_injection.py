@@ -49,7 +49,9 @@ def _withhold(lm, stft, W, out, ws, tile, wait_ns):
 
 
 @pytest.mark.parametrize("shape,tile", [((4, 600, 201, 128), 30), ((8, 3000, 201, 80), 500)], ids=str)
-def test_withheld_tile_times_out_and_reports(lm, oracle_mod, shape, tile):
+def test_withheld_tile_times_out_and_reports(lm, oracle_mod, shape, tile, monkeypatch):
+    # the fault entry runs the one-CTA-per-SM kernel; describe that one
+    monkeypatch.setenv("LOGMEL_K1_VARIANT", "resident")
     B, F, NF, NM = shape
     info = lm.describe_log_mel_from_stft(B, F, NF, NM)
     assert info["resident"] == 1

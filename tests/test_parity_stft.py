@@ -66,9 +66,12 @@ def test_correctness_shapes(lm, oracle_mod, shape):
 @pytest.mark.parametrize("shape", [(1, 1, 201, 80), (3, 1, 201, 128), (2, 5, 1, 1), (1, 7, 3, 2), (4, 33, 64, 40),
                                    (3, 17, 401, 80), (5, 9, 129, 512), (2, 50, 2049, 128), (9, 3, 7, 300)],
                          ids=str)
-def test_edge_shapes(lm, oracle_mod, shape):
+@pytest.mark.parametrize("variant", ["auto", "nocluster"])
+def test_edge_shapes(lm, oracle_mod, shape, variant, monkeypatch):
     # F = 1, NF = 1, NM = 1, even NF (every tile aligned), odd B*F*NF (the
-    # tensor ends 8 bytes past a 16-byte boundary), NM up to 512, big NF.
+    # tensor ends 8 bytes past a 16-byte boundary), NM up to 512, big NF; on
+    # the variant small batches pick (one cluster per clip) and without it.
+    monkeypatch.setenv("LOGMEL_K1_VARIANT", variant)
     B, F, NF, NM = shape
     stft, W = workloads.stft_inputs(B, F, NF, NM, seed=11 + B + F + NF)
     _compare(*_run(lm, oracle_mod, stft, W))
@@ -99,7 +102,7 @@ def test_zero_and_wide_filter_rows(lm, oracle_mod):
     _compare(*_run(lm, oracle_mod, s2, Ww))
 
 
-@pytest.mark.parametrize("variant", ["resident", "twopass"])
+@pytest.mark.parametrize("variant", ["resident", "twopass", "cluster"])
 def test_variants_agree(lm, oracle_mod, variant, monkeypatch):
     monkeypatch.setenv("LOGMEL_K1_VARIANT", variant)
     stft, W = workloads.stft_inputs(6, 777, 201, 128, seed=21)
@@ -201,13 +204,15 @@ def test_full_size_headline_every_clip(lm, oracle_mod):
 
 @pytest.mark.parametrize("shape", [(3, 301, 201, 128), (2, 50, 64, 40), (6, 777, 201, 80), (1, 1, 1, 1),
                                    (1, 1, 2, 1), (2, 3, 5, 3)], ids=str)
-@pytest.mark.parametrize("variant", ["auto", "twopass"])
+@pytest.mark.parametrize("variant", ["auto", "resident", "twopass"])
 def test_source_eight_bytes_off_a_boundary(lm, oracle_mod, shape, variant, monkeypatch):
     # A contiguous complex64 view one element into its allocation starts 8
     # bytes past a 16-byte boundary: the first tile's first value is copied
     # by hand.  An even element count also ends 8 bytes past a boundary.
-    monkeypatch.setenv("LOGMEL_K1_VARIANT", variant)
     B, F, NF, NM = shape
+    if variant == "resident" and not lm.describe_log_mel_from_stft(B, F, NF, NM)["resident"]:
+        variant = "nocluster"  # a shape whose clips span too many steps for the resident mode
+    monkeypatch.setenv("LOGMEL_K1_VARIANT", variant)
     stft, W = workloads.stft_inputs(B, F, NF, NM, seed=90 + B + F + NF)
     big = torch.zeros(B * F * NF + 1, dtype=torch.complex64, device="cuda")
     big[1:] = stft.flatten().cuda()
@@ -229,3 +234,23 @@ def test_batch_view_of_a_larger_tensor(lm, oracle_mod):
     assert v.data_ptr() % 16 == 8
     out = lm.log_mel_from_stft(v, W.cuda())
     _compare(out.cpu().numpy(), oracle_mod.log_mel_from_stft(stft[1:].numpy(), W.numpy()))
+
+
+def test_small_batches_run_one_cluster_per_clip(lm, oracle_mod, monkeypatch):
+    # B = 7 Whisper clips: the device runs every clip's cluster of 16 CTAs at
+    # once, keeping 112 SMs busy, so the library picks the cluster variant;
+    # the one-CTA-per-SM kernel gives the same values.  Every clip is checked
+    # against the oracle.
+    import dataclasses
+    w = dataclasses.replace(workloads.WHISPER_STFT, B=7)
+    info = lm.describe_log_mel_from_stft(w.B, w.F, w.NF, w.NM)
+    assert 8 <= info["cluster"] <= 16 and info["kernels"] == 1
+    stft, W = workloads.stft_workload_inputs(w, device="cuda")
+    ws = torch.empty(lm.log_mel_from_stft_workspace_size(w.B, w.F, w.NF, w.NM), dtype=torch.uint8, device="cuda")
+    out = lm.log_mel_from_stft(stft, W, workspace=ws)
+    assert lm.workspace_error(ws) == 0
+    _compare(out.cpu().numpy(), oracle_mod.log_mel_from_stft(stft.cpu().numpy(), W.cpu().numpy()))
+    monkeypatch.setenv("LOGMEL_K1_VARIANT", "nocluster")
+    assert lm.describe_log_mel_from_stft(w.B, w.F, w.NF, w.NM)["cluster"] == 0
+    other = lm.log_mel_from_stft(stft, W, workspace=ws)
+    _compare(other.cpu().numpy(), out.cpu().numpy())
