@@ -670,6 +670,82 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
+SWEEP_NFFT = (64, 256, 512, 1024, 4096, 16384)
+
+
+def run_sweep(args, world, rank, local):
+    """The full-spectrum sweep of the flashmel page's performance section:
+    hop = n_fft / 4, 128 mels, B = 32 clips of T = 160000 samples, one line
+    per n_fft in the sweep list (f32 in and out, no log; 16 kHz, HTK 0-8 kHz).
+    Each size is timed over --config-steps calls with L2 flushed in between,
+    and the oracle is timed beside it on a bounded sample (whole clips, up to
+    about a second of CPU work; its DFT is O(N^2))."""
+    import dataclasses
+    import torch
+
+    import __graft_entry__
+    import workloads
+    import oracle
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    import log_mel_spectrogram_gb300 as lm
+    oracle.build()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    peak, peak_kind = _peaks()
+    base = workloads.WaveWorkload("sweep", 32, 160000, 16000, 1024, 256, 128, 0.0, 8000.0, "htk", "f32", "f32",
+                                  False, 1005)
+    rows = []
+    with ClockSampler(local) as clk:
+        for n_fft in SWEEP_NFFT:
+            w = dataclasses.replace(base, name=f"sweep_b32_t160000_nfft{n_fft}_hop{n_fft // 4}_htk128",
+                                    n_fft=n_fft, hop_length=n_fft // 4)
+            job = WaveJob.__new__(WaveJob)
+            job.name, job.lm, job.w, job.dev = "sweep", lm, w, dev
+            job.x = workloads.wave_workload_inputs(w, device=dev)
+            job.mel = lm.MelSpectrogram(sample_rate=w.sample_rate, n_fft=w.n_fft, hop_length=w.hop_length,
+                                        n_mels=w.n_mels, f_min=w.f_min, f_max=w.f_max, center=w.center,
+                                        pad_mode=w.pad_mode, power=w.power, mel_scale=w.mel_scale, log_mel=False)
+            job.ws = torch.empty(job.mel.workspace_size(w.B, w.T, dev), dtype=torch.uint8, device=dev)
+            job.out = job.mel(job.x, workspace=job.ws)
+            job.units, job.bytes, job.flops, job.kernels, job.flush_l2 = w.B, w.canonical_bytes, wave_flops(w), 1, True
+            for _ in range(args.warmup):
+                job.step()
+            torch.cuda.synchronize(dev)
+            ms, total, _ = timed_steps(job, job.step, args.config_steps, stream, flush, dev, clk)
+            if job.error():
+                raise RuntimeError(f"device error word set in the sweep at n_fft {n_fft}")
+            us = statistics.median(ms) * 1e3
+            # oracle: one call on as many whole clips as it has threads (it
+            # runs one clip per thread)
+            x_host = job.x.cpu().numpy()
+            done = min(w.B, max(1, oracle.num_threads()))
+            t0 = time.perf_counter()
+            oracle.mel_spectrogram(x_host[:done], w.sample_rate, w.n_fft, w.hop_length, w.n_mels, f_max=w.f_max)
+            cpu_s = time.perf_counter() - t0
+            rows.append({"n_fft": n_fft, "hop": n_fft // 4, "n_frames": w.n_frames, "us_per_call_median": us,
+                         "us_per_call_min": min(ms) * 1e3, "clips_per_s": w.B / (us / 1e6),
+                         "essential_bytes": w.canonical_bytes, "essential_gbs": w.canonical_bytes / (us / 1e6) / 1e9,
+                         "hbm_frac_of_measured": w.canonical_bytes / (us / 1e6) / 1e9 / peak,
+                         "tflops": job.flops / (us / 1e6) / 1e12,
+                         "cpu_baseline": {"clips_per_s": done / cpu_s, "cores": oracle.num_threads(), "kind": "oracle",
+                                          "sample": f"{done} whole clips in one call, {cpu_s:.2f} s"}})
+            job.mel.close()
+            del job
+            torch.cuda.empty_cache()
+    print(json.dumps({"metric": "full-spectrum sweep: us per call (B=32, T=160000, hop=n_fft/4, 128 mels)",
+                      "value": next(r["clips_per_s"] for r in rows if r["n_fft"] == 1024), "unit": "clips/s",
+                      "n_gpus": 1, "steps": args.config_steps, "warmup": args.warmup, "higher_is_better": True,
+                      "dtype": "f32", "data": "synthetic (seeded sinusoids, workloads.wave_sines)",
+                      "config": {"workload": "sweep", "B": 32, "T": 160000, "sample_rate": 16000, "n_mels": 128,
+                                 "l2": "flushed between timed calls by writing 512 MB"},
+                      "peak_hbm_gbs": peak, "peak_kind": peak_kind, "sweep": rows,
+                      "clocks": clk.summary()}), flush=True)
+
+
 def run_reference(args, world, rank):
     """The oracle timed on host cores, each step a bounded sample of clips."""
     if rank != 0:
@@ -761,10 +837,10 @@ def main():
     ap.add_argument("--clock-soak", type=float, default=1.0,
                     help="seconds of untimed back-to-back steps directly before the timed steps, so that the "
                          "clock samples describe a GPU under this load (0 = none)")
-    ap.add_argument("--workload", choices=["stft", "stft_small", "stft_b8", "wave_whisper", "wave_pcm16"],
+    ap.add_argument("--workload", choices=["stft", "stft_small", "stft_b8", "wave_whisper", "wave_pcm16", "sweep"],
                     default="stft",
                     help="stft (default, the headline: B=256, F=3000, NM=128), stft_small (B=1, F=300, NM=80), "
-                         "stft_b8 (B=8, F=3000, NM=80) or one of the waveform workloads")
+                         "stft_b8 (B=8, F=3000, NM=80), one of the waveform workloads, or sweep (n_fft 64..16384)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -774,6 +850,9 @@ def main():
         return
     if args.impl == "torch_eager":
         run_torch_eager(args, world, rank, local)
+        return
+    if args.workload == "sweep":
+        run_sweep(args, world, rank, local)
         return
     run_ours(args, world, rank, local)
 
