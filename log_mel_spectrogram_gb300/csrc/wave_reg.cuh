@@ -222,6 +222,7 @@ struct Cfg<400> {
   static constexpr int TWROW = 10;   // float2 per lane row of the stage-2 and untangle tables (8 used)
   static constexpr int LANES2 = 25;  // lanes with a column in stage 2
   static constexpr int R2 = 8;       // twiddles / bins per stage-2 lane
+  static constexpr int S2P = 1;      // frames a warp carries through stage 2 together (2 measured slower)
   static constexpr int kMinBlocks = 3;
 };
 
@@ -347,10 +348,36 @@ __device__ __forceinline__ void load_frame(const WaveArgs &a, int64_t b, int64_t
 #pragma unroll
       for (int i = 0; i < K; ++i) u[i] = make_float2(__ldg(w + 2 * STRIDE * i), __ldg(w + 2 * STRIDE * i + 1));
     }
+  } else if (a.pad_mode == LM_PAD_REFLECT && a.pad_zero == 0) {
+    // Reflect padding (the common case): an index folds once, without
+    // branches (T > n_fft / 2, so one reflection is enough), and every load
+    // is in flight at once.
+    const int T = static_cast<int>(a.T);
+    const int base0 = static_cast<int>(s0) + 2 * lane_off;
+    auto fold = [T](int j) {
+      j = j < 0 ? -j : j;
+      return j >= T ? 2 * (T - 1) - j : j;
+    };
+    if (a.in_i16) {
+      const int16_t *w = static_cast<const int16_t *>(a.wave) + b * a.T;
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int j = base0 + 2 * STRIDE * i;
+        u[i] = make_float2(static_cast<float>(__ldg(w + fold(j))) * kI16,
+                           static_cast<float>(__ldg(w + fold(j + 1))) * kI16);
+      }
+    } else {
+      const float *w = static_cast<const float *>(a.wave) + b * a.T;
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int j = base0 + 2 * STRIDE * i;
+        u[i] = make_float2(__ldg(w + fold(j)), __ldg(w + fold(j + 1)));
+      }
+    }
   } else {
-    // Indices first, into this lane's own stage-1 row (free until the DFT
-    // result overwrites it), then a gather without branches -- a clamped
-    // index and a select -- so that every load is in flight at once.
+    // Other padding: indices first, into this lane's own stage-1 row (free
+    // until the DFT result overwrites it), then a gather without branches --
+    // a clamped index and a select -- so that every load is in flight at once.
     int *idx = reinterpret_cast<int *>(scratch);
     edge_indices(a, static_cast<int>(s0), lane_off, STRIDE, K, idx);
     if (a.in_i16) {
@@ -398,6 +425,72 @@ __device__ __forceinline__ float untangle(float2 A, float2 B, float2 tw, bool po
     *top = q;
   }
   return p;
+}
+
+// Stage 2 of the 400-point kernel for P frames of a warp at once, f0 ..
+// f0 + P - 1 (those below nf): lane c < 25 transforms column c of each, so
+// P independent chains of loads, DFT, shuffles and untangle overlap; the
+// column's twiddles are loaded once for all P.
+template <int P>
+__device__ __forceinline__ void stage2_400(float *regions, int f0, int nf, int lane, const float2 *tw2,
+                                           const float2 *twu, bool power_one) {
+  using C = Cfg<400>;
+  constexpr int M = C::M;
+  const int c = lane;  // column; lanes 25..31 idle
+  const bool act = c < C::LANES2;
+  const float2 *tr = tw2 + (act ? c : 0) * C::TWROW;
+  float2 v[P][8];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const bool ok = act && f0 + p < nf;
+    const float2 *Y = reinterpret_cast<const float2 *>(regions + (f0 + p) * C::REGION);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[p][i] = ok ? Y[i * C::ROW + c] : make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    const float2 t = tr[i];
+#pragma unroll
+    for (int p = 0; p < P; ++p) v[p][i] = cmul(v[p][i], t);
+  }
+#pragma unroll
+  for (int p = 0; p < P; ++p) Dft<8>::run(v[p]);  // v[p][d] = Z[c + 25 d] of frame f0 + p
+  // Z[M - k] for k = c + 25 d is lane 25 - c's value 7 - d (lane 0: its own
+  // value (8 - d) mod 8).
+  const int src = (c >= 1 && act) ? 25 - c : lane;
+  float2 r[P][8];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r[p][i].x = __shfl_sync(0xffffffffu, v[p][i].x, src);
+      r[p][i].y = __shfl_sync(0xffffffffu, v[p][i].y, src);
+    }
+  }
+  __syncwarp();  // every lane has read the regions before power rows overwrite them
+  if (act) {
+    const uint32_t tu = smem_u32(twu + c * C::TWROW);
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const int f = f0 + p;
+      if (f < nf) {
+        const uint32_t pw = smem_u32(regions + f * C::REGION + (f >> 1));
+        const uint32_t pc = pw + 4u * static_cast<uint32_t>(c);
+        if (c == 0) {
+          float top;
+          sts_f32(pc, untangle<true>(v[p][0], v[p][0], lds_f32x2(tu), power_one, &top));
+          sts_f32(pw + 4u * M, top);
+        } else {
+          sts_f32(pc, untangle<false>(v[p][0], r[p][7], lds_f32x2(tu), power_one));
+        }
+#pragma unroll
+        for (int d = 1; d < 8; ++d) {
+          const float2 Bz = c != 0 ? r[p][7 - d] : v[p][8 - d];
+          sts_f32(pc + 4u * (25 * d), untangle<false>(v[p][d], Bz, lds_f32x2(tu + 8u * d), power_one));
+        }
+      }
+    }
+  }
 }
 
 template <int NFFT>
@@ -486,49 +579,22 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
     // f * REGION + shift(f): lanes over the frames of one bin then hit
     // distinct banks in the mel projection.
     auto prow = [&](int f) { return regions + f * REGION + (NFFT == 400 ? (f >> 1) : f); };
+    if constexpr (NFFT == 400) {
+#pragma unroll 1
+      for (int q = 0; q < C::FPW; q += C::S2P) {
+        const int f0 = warp * C::FPW + q;
+        if (f0 >= nf) break;  // warp-uniform
+        stage2_400<C::S2P>(regions, f0, nf, lane, tw2, twu, a.power_is_one);
+      }
+    }
+    if constexpr (NFFT == 1024) {
 #pragma unroll 1
     for (int q = 0; q < C::FPW; ++q) {
       const int f = warp * C::FPW + q;
       if (f >= nf) break;  // warp-uniform
       const float2 *Y = reinterpret_cast<const float2 *>(regions + f * REGION);
       const uint32_t pw = smem_u32(prow(f));
-      if constexpr (NFFT == 400) {
-        const int c = lane;  // column; lanes 25..31 idle
-        const bool act = c < C::LANES2;
-        float2 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = act ? Y[i * C::ROW + c] : make_float2(0.f, 0.f);
-        const float2 *tr = tw2 + (act ? c : 0) * C::TWROW;
-#pragma unroll
-        for (int i = 1; i < 8; ++i) v[i] = cmul(v[i], tr[i]);
-        Dft<8>::run(v);  // v[d] = Z[c + 25 d]
-        // Z[M - k] for k = c + 25 d is lane 25 - c's value 7 - d (lane 0:
-        // its own value (8 - d) mod 8).
-        const int src = (c >= 1 && act) ? 25 - c : lane;
-        float2 r[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          r[i].x = __shfl_sync(0xffffffffu, v[i].x, src);
-          r[i].y = __shfl_sync(0xffffffffu, v[i].y, src);
-        }
-        __syncwarp();  // every lane has read the region before power rows overwrite it
-        if (act) {
-          const uint32_t tu = smem_u32(twu + c * C::TWROW);
-          const uint32_t pc = pw + 4u * static_cast<uint32_t>(c);
-          if (c == 0) {
-            float top;
-            sts_f32(pc, untangle<true>(v[0], v[0], lds_f32x2(tu), a.power_is_one, &top));
-            sts_f32(pw + 4u * M, top);
-          } else {
-            sts_f32(pc, untangle<false>(v[0], r[7], lds_f32x2(tu), a.power_is_one));
-          }
-#pragma unroll
-          for (int d = 1; d < 8; ++d) {
-            const float2 Bz = c != 0 ? r[7 - d] : v[8 - d];
-            sts_f32(pc + 4u * (25 * d), untangle<false>(v[d], Bz, lds_f32x2(tu + 8u * d), a.power_is_one));
-          }
-        }
-      } else {
+      {
         const int c = lane >> 1, h = lane & 1;
         float2 v[16];
         const float2 *tr = tw2 + lane * C::TWROW;
@@ -572,6 +638,7 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
         }
       }
     }
+    }
     if (threadIdx.x == 0) {
       // A CTA whose pending list would overflow claims no further tile; the
       // others take the rest (grid x kPendMax >= tiles).
@@ -590,26 +657,29 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
       const int f = static_cast<int>(threadIdx.x) % LF;
       const int g = static_cast<int>(threadIdx.x) / LF;
       if (f < nf) {
-        const uint32_t pa0 = smem_u32(prow(f));
+        // The first four taps of every band are read unconditionally: filter
+        // rows are zero-padded to a multiple of four, and the floats after a
+        // power row are the frame's own finite stage-1 values, so a padded
+        // tap adds exactly 0.  Bands are then straight-line code (wider bands
+        // finish in a loop) and two bands' chains overlap.
+        const float *pr = prow(f);
         const int64_t orow0 = b * a.n_mels * a.n_frames + t0 + f;
+#pragma unroll 2
         for (int m = g; m < a.n_mels; m += NG) {
           const int2 sw = fsw[m];
-          const uint32_t pa = pa0 + static_cast<uint32_t>(sw.x) * 4u;
-          const uint32_t wa = smem_u32(fw + m * a.wmax);
-          float acc = 0.f;
-          int t = 0;
-          for (; t + 4 <= sw.y; t += 4) {
-            const float4 w4 = lds_f32x4(wa + 4 * t);
-            acc = fmaf(w4.x, lds_f32(pa + 4 * t), acc);
-            acc = fmaf(w4.y, lds_f32(pa + 4 * t + 4), acc);
-            acc = fmaf(w4.z, lds_f32(pa + 4 * t + 8), acc);
-            acc = fmaf(w4.w, lds_f32(pa + 4 * t + 12), acc);
-          }
-          if (t < sw.y) {
-            const float4 w4 = lds_f32x4(wa + 4 * t);
-            acc = fmaf(w4.x, lds_f32(pa + 4 * t), acc);
-            if (t + 1 < sw.y) acc = fmaf(w4.y, lds_f32(pa + 4 * t + 4), acc);
-            if (t + 2 < sw.y) acc = fmaf(w4.z, lds_f32(pa + 4 * t + 8), acc);
+          const float *pa = pr + sw.x;
+          const float *wr = fw + m * a.wmax;
+          const float4 w4 = *reinterpret_cast<const float4 *>(wr);
+          float acc = w4.x * pa[0];
+          acc = fmaf(w4.y, pa[1], acc);
+          acc = fmaf(w4.z, pa[2], acc);
+          acc = fmaf(w4.w, pa[3], acc);
+          for (int t = 4; t < sw.y; t += 4) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(wr + t);
+            acc = fmaf(v4.x, pa[t], acc);
+            acc = fmaf(v4.y, pa[t + 1], acc);
+            acc = fmaf(v4.z, pa[t + 2], acc);
+            acc = fmaf(v4.w, pa[t + 3], acc);
           }
           const int64_t o = orow0 + static_cast<int64_t>(m) * a.n_frames;
           if (a.log_mel) {
