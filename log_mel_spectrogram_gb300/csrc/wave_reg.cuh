@@ -15,11 +15,13 @@
 //   stage 2  the lane of column c multiplies column c by exp(-2 pi i b c / M)
 //            and runs the N2-point DFT over b in registers, which gives bins
 //            c + N1 d.  Bin k pairs with bin M - k in the real-input untangle,
-//            and the lane that holds M - k is in the same warp: one shuffle
-//            per value.  With A = Z[k], B = Z[M - k], S = A + conj B and
-//            T = exp(-2 pi i k / N) (-i) (A - conj B), 2 X[k] = S + T (and
-//            2 X[M] = S - T at k = 0); the factor 2 is folded into the
-//            filter weights (scaled by 2^-power, exactly).
+//            and the lane that holds M - k is in the same warp.  With
+//            A = Z[k], B = Z[M - k], S = A + conj B and
+//            T = exp(-2 pi i k / N) (-i) (A - conj B), 2 X[k] = S + T and
+//            2 conj X[M - k] = S - T: each of the two lanes forms both bins
+//            of half of their common pairs, fetching half of the partner's
+//            values by shuffle.  The factor 2 is folded into the filter
+//            weights (scaled by 2^-power, exactly).
 //
 // n_fft 400:  M = 200 = 25 x 8.  Stage 1: 8 threads per frame, four frames
 //             per warp, a 25-point DFT (5 x 5) each.  Stage 2: lane c < 25
@@ -407,45 +409,49 @@ __device__ __forceinline__ void load_frame(const WaveArgs &a, int64_t b, int64_t
   }
 }
 
-// |2 X[k]|^power from A = Z[k], B = Z[M - k] and tw = exp(-2 pi i k / N):
-// 2 X[k] = S + T with S = A + conj B, T = tw (-i) (A - conj B).  For k = 0
-// (A = B = Z[0], tw = 1), *top receives |2 X[M]|^power = |S - T|^power.
-template <bool kTop>
-__device__ __forceinline__ float untangle(float2 A, float2 B, float2 tw, bool power_one, float *top = nullptr) {
+// Both bins of the untangle pair (k, M - k) from A = Z[k], B = Z[M - k] and
+// tw = exp(-2 pi i k / N): 2 X[k] = S + T and 2 conj X[M - k] = S - T, with
+// S = A + conj B and T = tw (-i) (A - conj B).  Returns |2 X[k]|^power in *pk
+// and |2 X[M - k]|^power in *pm.
+__device__ __forceinline__ void untangle_pair(float2 A, float2 B, float2 tw, bool power_one, float *pk, float *pm) {
   const float2 S = make_float2(A.x + B.x, A.y - B.y);
   const float2 D = make_float2(A.x - B.x, A.y + B.y);
   const float2 T = make_float2(fmaf(tw.x, D.y, tw.y * D.x), fmaf(tw.y, D.y, -tw.x * D.x));
   const float2 P = make_float2(S.x + T.x, S.y + T.y);
+  const float2 Q = make_float2(S.x - T.x, S.y - T.y);
   float p = fmaf(P.x, P.x, P.y * P.y);
-  if (power_one) p = sqrtf(p);
-  if constexpr (kTop) {
-    const float2 Q = make_float2(S.x - T.x, S.y - T.y);
-    float q = fmaf(Q.x, Q.x, Q.y * Q.y);
-    if (power_one) q = sqrtf(q);
-    *top = q;
+  float q = fmaf(Q.x, Q.x, Q.y * Q.y);
+  if (power_one) {
+    p = sqrtf(p);
+    q = sqrtf(q);
   }
-  return p;
+  *pk = p;
+  *pm = q;
 }
 
 // Stage 2 of the 400-point kernel for P frames of a warp at once, f0 ..
-// f0 + P - 1 (those below nf): lane c < 25 transforms column c of each, so
-// P independent chains of loads, DFT, shuffles and untangle overlap; the
-// column's twiddles are loaded once for all P.
+// f0 + P - 1 (those below nf): lane c < 25 transforms column c of each and
+// holds bins c + 25 d.  The untangle pair of bin k = c + 25 d is bin
+// M - k = (25 - c) + 25 (7 - d), held by lane 25 - c as its value 7 - d; lane
+// c forms both bins of its pairs d = 0..3 (lane 25 - c forms those of d =
+// 4..7), so it fetches only its partner's values 4..7.  Column 0 pairs with
+// itself (d with 8 - d): lane 0 forms d = 0..3 (d = 0 gives bins 0 and 200)
+// and bin 100 alone.
 template <int P>
 __device__ __forceinline__ void stage2_400(float *regions, int f0, int nf, int lane, const float2 *tw2,
                                            const float2 *twu, bool power_one) {
   using C = Cfg<400>;
   constexpr int M = C::M;
-  const int c = lane;  // column; lanes 25..31 idle
+  const int c = lane;  // column; lanes 25..31 run column 0 and discard it
   const bool act = c < C::LANES2;
-  const float2 *tr = tw2 + (act ? c : 0) * C::TWROW;
+  const int cc = act ? c : 0;
+  const float2 *tr = tw2 + cc * C::TWROW;
   float2 v[P][8];
 #pragma unroll
   for (int p = 0; p < P; ++p) {
-    const bool ok = act && f0 + p < nf;
     const float2 *Y = reinterpret_cast<const float2 *>(regions + (f0 + p) * C::REGION);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[p][i] = ok ? Y[i * C::ROW + c] : make_float2(0.f, 0.f);
+    for (int i = 0; i < 8; ++i) v[p][i] = Y[i * C::ROW + cc];
   }
 #pragma unroll
   for (int i = 1; i < 8; ++i) {
@@ -455,38 +461,36 @@ __device__ __forceinline__ void stage2_400(float *regions, int f0, int nf, int l
   }
 #pragma unroll
   for (int p = 0; p < P; ++p) Dft<8>::run(v[p]);  // v[p][d] = Z[c + 25 d] of frame f0 + p
-  // Z[M - k] for k = c + 25 d is lane 25 - c's value 7 - d (lane 0: its own
-  // value (8 - d) mod 8).
   const int src = (c >= 1 && act) ? 25 - c : lane;
-  float2 r[P][8];
+  float2 r[P][4];  // the partner's values 7, 6, 5, 4
 #pragma unroll
   for (int p = 0; p < P; ++p) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      r[p][i].x = __shfl_sync(0xffffffffu, v[p][i].x, src);
-      r[p][i].y = __shfl_sync(0xffffffffu, v[p][i].y, src);
+    for (int i = 0; i < 4; ++i) {
+      r[p][i].x = __shfl_sync(0xffffffffu, v[p][7 - i].x, src);
+      r[p][i].y = __shfl_sync(0xffffffffu, v[p][7 - i].y, src);
     }
   }
   __syncwarp();  // every lane has read the regions before power rows overwrite them
   if (act) {
-    const uint32_t tu = smem_u32(twu + c * C::TWROW);
+    const float2 *tu = twu + c * C::TWROW;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
       const int f = f0 + p;
       if (f < nf) {
-        const uint32_t pw = smem_u32(regions + f * C::REGION + (f >> 1));
-        const uint32_t pc = pw + 4u * static_cast<uint32_t>(c);
-        if (c == 0) {
-          float top;
-          sts_f32(pc, untangle<true>(v[p][0], v[p][0], lds_f32x2(tu), power_one, &top));
-          sts_f32(pw + 4u * M, top);
-        } else {
-          sts_f32(pc, untangle<false>(v[p][0], r[p][7], lds_f32x2(tu), power_one));
-        }
+        float *pw = regions + f * C::REGION + (f >> 1);
 #pragma unroll
-        for (int d = 1; d < 8; ++d) {
-          const float2 Bz = c != 0 ? r[p][7 - d] : v[p][8 - d];
-          sts_f32(pc + 4u * (25 * d), untangle<false>(v[p][d], Bz, lds_f32x2(tu + 8u * d), power_one));
+        for (int d = 0; d < 4; ++d) {
+          const float2 B = c != 0 ? r[p][d] : v[p][(8 - d) & 7];
+          float pk, pm;
+          untangle_pair(v[p][d], B, tu[d], power_one, &pk, &pm);
+          pw[c + 25 * d] = pk;
+          pw[M - c - 25 * d] = pm;
+        }
+        if (c == 0) {
+          float pk, pm;
+          untangle_pair(v[p][4], v[p][4], tu[4], power_one, &pk, &pm);
+          pw[100] = pk;
         }
       }
     }
@@ -593,7 +597,6 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
       const int f = warp * C::FPW + q;
       if (f >= nf) break;  // warp-uniform
       const float2 *Y = reinterpret_cast<const float2 *>(regions + f * REGION);
-      const uint32_t pw = smem_u32(prow(f));
       {
         const int c = lane >> 1, h = lane & 1;
         float2 v[16];
@@ -612,29 +615,36 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
           const float2 T = rot<32>(V1, d);
           v[d] = h ? csub(V0, T) : cadd(V0, T);  // Z[c + 16 d + 256 h]
         }
-        // Z[M - k] is lane (lane >= 2 ? 33 - lane : 1 - lane)'s value 15 - d
-        // (lanes 0 and 1: value (16 - d) mod 16, and d = 0 pairs with itself).
+        // The untangle pair of bin k = c + 16 d + 256 h is bin M - k, lane
+        // (lane >= 2 ? 33 - lane : 1 - lane)'s value 15 - d (lanes 0 and 1,
+        // column 0: value 16 - d, and d = 0 pairs with itself).  A lane forms
+        // both bins of its pairs d = 0..7 (the partner forms d = 8..15; lane 0
+        // also forms d = 8, bins 128 and 384), so it fetches only the
+        // partner's values 15..8.
         const int src = lane >= 2 ? 33 - lane : 1 - lane;
-        float2 r[16];
+        float2 r[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          r[i].x = __shfl_sync(0xffffffffu, v[i].x, src);
-          r[i].y = __shfl_sync(0xffffffffu, v[i].y, src);
+        for (int i = 0; i < 8; ++i) {
+          r[i].x = __shfl_sync(0xffffffffu, v[15 - i].x, src);
+          r[i].y = __shfl_sync(0xffffffffu, v[15 - i].y, src);
         }
         __syncwarp();
-        const uint32_t tu = smem_u32(twu + lane * C::TWROW);
-        const uint32_t pc = pw + 4u * static_cast<uint32_t>(c + 256 * h);
-        if (lane == 0) {
-          float top;
-          sts_f32(pc, untangle<true>(v[0], v[0], lds_f32x2(tu), a.power_is_one, &top));
-          sts_f32(pw + 4u * M, top);
-        } else {
-          sts_f32(pc, untangle<false>(v[0], lane >= 2 ? r[15] : v[0], lds_f32x2(tu), a.power_is_one));
-        }
+        const float2 *tu = twu + lane * C::TWROW;
+        float *pwf = regions + f * REGION + f;
+        const int k0 = c + 256 * h;
 #pragma unroll
-        for (int d = 1; d < 16; ++d) {
-          const float2 Bz = lane >= 2 ? r[15 - d] : r[16 - d];
-          sts_f32(pc + 4u * (16 * d), untangle<false>(v[d], Bz, lds_f32x2(tu + 8u * d), a.power_is_one));
+        for (int d = 0; d < 8; ++d) {
+          const float2 B = lane >= 2 ? r[d] : (d == 0 ? v[0] : r[d - 1]);
+          float pk, pm;
+          untangle_pair(v[d], B, tu[d], a.power_is_one, &pk, &pm);
+          pwf[k0 + 16 * d] = pk;
+          pwf[M - k0 - 16 * d] = pm;
+        }
+        if (lane == 0) {
+          float pk, pm;
+          untangle_pair(v[8], r[7], tu[8], a.power_is_one, &pk, &pm);
+          pwf[128] = pk;
+          pwf[384] = pm;
         }
       }
     }
