@@ -571,6 +571,15 @@ void wave_entry(WaveKernel *k, size_t *smem, int *tf, int *nt, int n_mels, int w
   *nt = WaveCfg<NFFT>::NT;
 }
 
+// The register kernel of a size and its launch shape.
+template <int NFFT>
+void reg_entry(WaveKernel *k, size_t *smem, int *tf, int *nt, int n_mels, int wmax) {
+  *k = reg::wave_reg_kernel<NFFT>;
+  *smem = reg::smem_bytes<NFFT>(n_mels, wmax);
+  *tf = reg::Cfg<NFFT>::TF;
+  *nt = reg::Cfg<NFFT>::NT;
+}
+
 bool pick_wave_kernel(int n_fft, int n_mels, int wmax, WaveKernel *k, size_t *smem, int *tf, int *nt) {
   switch (n_fft) {
     case 64: wave_entry<64>(k, smem, tf, nt, n_mels, wmax); return true;
@@ -778,10 +787,10 @@ std::vector<unsigned char> reg_image(const lm_mel_params &p, const HostTables &t
   for (int lane = 0; lane < C::LANES2; ++lane) {
     for (int j = 0; j < C::R2; ++j) {
       long b, c, k;  // stage-2 input row b of the lane's column c; bin k of its j-th output
-      if (NFFT == 400) {
+      if (NFFT != 1024) {  // one lane per column
         c = lane;
         b = j;
-        k = lane + 25 * j;
+        k = lane + static_cast<long>(C::N1) * j;
       } else {
         c = lane >> 1;
         const int h = lane & 1;
@@ -854,11 +863,21 @@ extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan
     }
     st = lm::upload(img, &pl->tables, &n_alloc);
   }
-  if (st == LM_OK && (params->n_fft == 400 || params->n_fft == 1024)) {
-    std::vector<unsigned char> img = params->n_fft == 400 ? lm::reg_image<400>(*params, t)
-                                                           : lm::reg_image<1024>(*params, t);
-    pl->reg_tables_bytes = static_cast<uint32_t>(img.size());
-    st = lm::upload(img, &pl->reg_tables, &n_alloc);
+  if (st == LM_OK) {
+    std::vector<unsigned char> img;
+    switch (params->n_fft) {
+      case 64: img = lm::reg_image<64>(*params, t); break;
+      case 128: img = lm::reg_image<128>(*params, t); break;
+      case 256: img = lm::reg_image<256>(*params, t); break;
+      case 400: img = lm::reg_image<400>(*params, t); break;
+      case 512: img = lm::reg_image<512>(*params, t); break;
+      case 1024: img = lm::reg_image<1024>(*params, t); break;
+      default: break;  // the generic kernel only
+    }
+    if (!img.empty()) {
+      pl->reg_tables_bytes = static_cast<uint32_t>(img.size());
+      st = lm::upload(img, &pl->reg_tables, &n_alloc);
+    }
   }
   if (st == LM_OK) {
     if (cudaError_t e = cudaGetDevice(&pl->device); e != cudaSuccess) st = lm::cuda_fail(e);
@@ -952,16 +971,13 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   bool use_reg = plan->reg_tables != nullptr && T < (int64_t{1} << 31) - 2 * (p.n_fft + p.pad) &&
                  std::strcmp(lm::env_or("LOGMEL_K3", "auto"), "stockham") != 0;
   if (use_reg) {
-    if (p.n_fft == 400) {
-      kern = lm::reg::wave_reg_kernel<400>;
-      smem = lm::reg::smem_bytes<400>(p.n_mels, plan->wmax);
-      tf = lm::reg::Cfg<400>::TF;
-      nt = lm::reg::Cfg<400>::NT;
-    } else {
-      kern = lm::reg::wave_reg_kernel<1024>;
-      smem = lm::reg::smem_bytes<1024>(p.n_mels, plan->wmax);
-      tf = lm::reg::Cfg<1024>::TF;
-      nt = lm::reg::Cfg<1024>::NT;
+    switch (p.n_fft) {
+      case 64: lm::reg_entry<64>(&kern, &smem, &tf, &nt, p.n_mels, plan->wmax); break;
+      case 128: lm::reg_entry<128>(&kern, &smem, &tf, &nt, p.n_mels, plan->wmax); break;
+      case 256: lm::reg_entry<256>(&kern, &smem, &tf, &nt, p.n_mels, plan->wmax); break;
+      case 400: lm::reg_entry<400>(&kern, &smem, &tf, &nt, p.n_mels, plan->wmax); break;
+      case 512: lm::reg_entry<512>(&kern, &smem, &tf, &nt, p.n_mels, plan->wmax); break;
+      default: lm::reg_entry<1024>(&kern, &smem, &tf, &nt, p.n_mels, plan->wmax); break;
     }
     use_reg = smem <= static_cast<size_t>(di.max_smem_optin);
   }

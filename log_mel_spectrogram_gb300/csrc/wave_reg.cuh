@@ -1,6 +1,6 @@
-// wave_reg.cuh -- waveform -> mel kernels for n_fft 400 and 1024 whose
-// transforms run mostly in registers (included by wave_mel.cu, inside its
-// namespace, after WaveArgs and map_index).
+// wave_reg.cuh -- waveform -> mel kernels for n_fft 64, 128, 256, 400, 512 and
+// 1024 whose transforms run mostly in registers (included by wave_mel.cu,
+// inside its namespace, after WaveArgs and map_index).
 //
 // The real FFT of a frame is the N/2 = M point complex FFT of its folded
 // samples z[n] = x[2n] + i x[2n+1] followed by the real-input untangle
@@ -23,15 +23,16 @@
 //            values by shuffle.  The factor 2 is folded into the filter
 //            weights (scaled by 2^-power, exactly).
 //
-// n_fft 400:  M = 200 = 25 x 8.  Stage 1: 8 threads per frame, four frames
-//             per warp, a 25-point DFT (5 x 5) each.  Stage 2: lane c < 25
-//             of the warp, one frame at a time, an 8-point DFT.
-// n_fft 1024: M = 512 = 16 x 32.  Stage 1: 32 threads per frame, a 16-point
-//             DFT (4 x 4) each.  Stage 2: the 32-point DFT of column c is
-//             shared by lanes 2c and 2c + 1: each transforms one parity of b
-//             (16 points), the two swap results with one shuffle per value,
-//             and lane 2c + h keeps the outputs d = d' + 16 h,
-//             X = V0[d'] + (-1)^h exp(-2 pi i d' / 32) V1[d'].
+// Sizes:
+//   n_fft 64, 128, 256, 400, 512: M = 32 = 8 x 4, 64 = 8 x 8, 128 = 16 x 8,
+//     200 = 25 x 8, 256 = 16 x 16.  Stage 1: N2 threads per frame, each an
+//     N1-point DFT; stage 2: one lane per column, each an N2-point DFT; 32
+//     frames per tile, four per warp.
+//   n_fft 1024: M = 512 = 16 x 32.  Stage 1: 32 threads per frame, a 16-point
+//     DFT each.  Stage 2: the 32-point DFT of column c is shared by lanes 2c
+//     and 2c + 1: each transforms one parity of b (16 points), the two swap
+//     results with one shuffle per value, and lane 2c + h keeps the outputs
+//     d = d' + 16 h, X = V0[d'] + (-1)^h exp(-2 pi i d' / 32) V1[d'].
 //
 // A frame stays inside one warp from its samples to its power row, so the
 // stages synchronise with __syncwarp; the CTA synchronises twice per tile of
@@ -211,23 +212,41 @@ struct Dft<25> {
 template <int NFFT>
 struct Cfg;
 
-template <>
-struct Cfg<400> {
-  static constexpr int M = 200;
-  static constexpr int N1 = 25;      // stage-1 DFT size
-  static constexpr int N2 = 8;       // stage-1 threads per frame, stage-2 DFT size
-  static constexpr int ROW = 25;     // complex values per stage-1 row; rows of a column hit distinct banks
+// The sizes whose stage 2 gives each column one lane: M = N1 x N2, stage 1
+// with N2 threads per frame (an N1-point DFT each), stage 2 with N1 lanes per
+// frame (an N2-point DFT each), 32-frame tiles of 4 frames per warp.  Rows of
+// stage-1 output hold N1 values at a stride of ROW (odd where that spreads a
+// column over the banks).
+template <int NFFT_, int N1_, int N2_, int ROW_, int MINB_>
+struct ColCfg {
+  static constexpr int M = NFFT_ / 2;
+  static constexpr int N1 = N1_;     // stage-1 DFT size; stage-2 lanes per frame
+  static constexpr int N2 = N2_;     // stage-1 threads per frame; stage-2 DFT size
+  static constexpr int ROW = ROW_;   // complex values per stage-1 row (N1 used)
   static constexpr int TF = 32;      // frames per tile
   static constexpr int NT = 256;
   static constexpr int FPW = TF / (NT / 32);  // frames per warp: 4
-  static constexpr int REGION = 2 * N2 * ROW;  // floats per frame region: 400
-  static constexpr int TWROW = 10;   // float2 per lane row of the stage-2 and untangle tables (8 used)
-  static constexpr int LANES2 = 25;  // lanes with a column in stage 2
-  static constexpr int R2 = 8;       // twiddles / bins per stage-2 lane
-  static constexpr int S2P = 1;      // frames a warp carries through stage 2 together (2 measured slower)
-  static constexpr int kMinBlocks = 3;
+  static constexpr int REGION = 2 * N2 * ROW;  // floats per frame region
+  static constexpr int LANES2 = N1;  // table rows: one per column
+  static constexpr int R2 = N2;      // twiddles per column
+  static constexpr int TWROW = N2 + 2;  // float2 per table row: an odd number of 16-byte units
+  static constexpr int kMinBlocks = MINB_;
+  // A power row (M + 1 floats at an offset of up to 15) and the mel
+  // projection's reads up to 3 floats past it stay inside the frame's region.
+  static_assert(M == N1 * N2 && N1 <= 32 && 15 + M + 1 + 3 <= REGION, "column layout");
 };
+template <>
+struct Cfg<64> : ColCfg<64, 8, 4, 9, 3> {};
+template <>
+struct Cfg<128> : ColCfg<128, 8, 8, 9, 3> {};
+template <>
+struct Cfg<256> : ColCfg<256, 16, 8, 17, 3> {};
+template <>
+struct Cfg<400> : ColCfg<400, 25, 8, 25, 3> {};  // rows of 25 already spread a column over the banks
+template <>
+struct Cfg<512> : ColCfg<512, 16, 16, 17, 2> {};
 
+// n_fft 1024: stage 2's 32-point column DFTs are shared by lane pairs.
 template <>
 struct Cfg<1024> {
   static constexpr int M = 512;
@@ -429,70 +448,60 @@ __device__ __forceinline__ void untangle_pair(float2 A, float2 B, float2 tw, boo
   *pm = q;
 }
 
-// Stage 2 of the 400-point kernel for P frames of a warp at once, f0 ..
-// f0 + P - 1 (those below nf): lane c < 25 transforms column c of each and
-// holds bins c + 25 d.  The untangle pair of bin k = c + 25 d is bin
-// M - k = (25 - c) + 25 (7 - d), held by lane 25 - c as its value 7 - d; lane
-// c forms both bins of its pairs d = 0..3 (lane 25 - c forms those of d =
-// 4..7), so it fetches only its partner's values 4..7.  Column 0 pairs with
-// itself (d with 8 - d): lane 0 forms d = 0..3 (d = 0 gives bins 0 and 200)
-// and bin 100 alone.
-template <int P>
-__device__ __forceinline__ void stage2_400(float *regions, int f0, int nf, int lane, const float2 *tw2,
-                                           const float2 *twu, bool power_one) {
-  using C = Cfg<400>;
-  constexpr int M = C::M;
-  const int c = lane;  // column; lanes 25..31 run column 0 and discard it
-  const bool act = c < C::LANES2;
+// Stage 2 of the one-lane-per-column sizes for the frames f0 .. of one
+// iteration (32 / N1 frames, N1 lanes each): lane c transforms column c and
+// holds bins c + N1 d.  The untangle pair of bin k = c + N1 d is bin
+// M - k = (N1 - c) + N1 (N2 - 1 - d), the value N2 - 1 - d of the lane of
+// column N1 - c; lane c forms both bins of its pairs d < N2 / 2 (the partner
+// forms the others), so it fetches only the partner's values N2 - 1 ..
+// N2 / 2.  Column 0 pairs with itself (d with N2 - d; d = 0 gives bins 0 and
+// M, and bin M / 2 stands alone), and for even N1 so does column N1 / 2
+// (d with N2 - 1 - d).  Lanes without a column (N1 = 25) run column 0 of the
+// first frame and discard it.
+template <int NFFT>
+__device__ __forceinline__ void stage2_cols(float *regions, int f0, int nf, int lane, const float2 *tw2,
+                                            const float2 *twu, bool power_one) {
+  using C = Cfg<NFFT>;
+  constexpr int M = C::M, N1 = C::N1, N2 = C::N2;
+  constexpr int FPI = 32 / N1;  // frames per iteration
+  const int q = lane / N1;
+  const int c = lane - q * N1;
+  const int f = f0 + q;
+  const bool act = q < FPI && f < nf;
   const int cc = act ? c : 0;
+  const int fr = act ? f : f0;
+  const bool middle = (N1 % 2 == 0) && c == N1 / 2;
+  const float2 *Y = reinterpret_cast<const float2 *>(regions + fr * C::REGION);
   const float2 *tr = tw2 + cc * C::TWROW;
-  float2 v[P][8];
+  float2 v[N2];
 #pragma unroll
-  for (int p = 0; p < P; ++p) {
-    const float2 *Y = reinterpret_cast<const float2 *>(regions + (f0 + p) * C::REGION);
+  for (int i = 0; i < N2; ++i) v[i] = Y[i * C::ROW + cc];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[p][i] = Y[i * C::ROW + cc];
-  }
+  for (int i = 1; i < N2; ++i) v[i] = cmul(v[i], tr[i]);
+  Dft<N2>::run(v);  // v[d] = Z[c + N1 d]
+  const int src = (act && c != 0 && !middle) ? q * N1 + (N1 - c) : lane;
+  float2 r[N2 / 2];  // the partner's values N2 - 1 .. N2 / 2
 #pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    const float2 t = tr[i];
-#pragma unroll
-    for (int p = 0; p < P; ++p) v[p][i] = cmul(v[p][i], t);
-  }
-#pragma unroll
-  for (int p = 0; p < P; ++p) Dft<8>::run(v[p]);  // v[p][d] = Z[c + 25 d] of frame f0 + p
-  const int src = (c >= 1 && act) ? 25 - c : lane;
-  float2 r[P][4];  // the partner's values 7, 6, 5, 4
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      r[p][i].x = __shfl_sync(0xffffffffu, v[p][7 - i].x, src);
-      r[p][i].y = __shfl_sync(0xffffffffu, v[p][7 - i].y, src);
-    }
+  for (int i = 0; i < N2 / 2; ++i) {
+    r[i].x = __shfl_sync(0xffffffffu, v[N2 - 1 - i].x, src);
+    r[i].y = __shfl_sync(0xffffffffu, v[N2 - 1 - i].y, src);
   }
   __syncwarp();  // every lane has read the regions before power rows overwrite them
   if (act) {
     const float2 *tu = twu + c * C::TWROW;
+    float *pw = regions + f * C::REGION + (f >> 1);
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-      const int f = f0 + p;
-      if (f < nf) {
-        float *pw = regions + f * C::REGION + (f >> 1);
-#pragma unroll
-        for (int d = 0; d < 4; ++d) {
-          const float2 B = c != 0 ? r[p][d] : v[p][(8 - d) & 7];
-          float pk, pm;
-          untangle_pair(v[p][d], B, tu[d], power_one, &pk, &pm);
-          pw[c + 25 * d] = pk;
-          pw[M - c - 25 * d] = pm;
-        }
-        if (c == 0) {
-          float pk, pm;
-          untangle_pair(v[p][4], v[p][4], tu[4], power_one, &pk, &pm);
-          pw[100] = pk;
-        }
-      }
+    for (int d = 0; d < N2 / 2; ++d) {
+      const float2 B = c == 0 ? v[(N2 - d) % N2] : (middle ? v[N2 - 1 - d] : r[d]);
+      float pk, pm;
+      untangle_pair(v[d], B, tu[d], power_one, &pk, &pm);
+      pw[c + N1 * d] = pk;
+      pw[M - c - N1 * d] = pm;
+    }
+    if (c == 0) {
+      float pk, pm;
+      untangle_pair(v[N2 / 2], v[N2 / 2], tu[N2 / 2], power_one, &pk, &pm);
+      pw[M / 2] = pk;
     }
   }
 }
@@ -552,28 +561,29 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
         (reinterpret_cast<uintptr_t>(a.wave) & (a.in_i16 ? 3u : 7u)) == 0;
 
     // ---------------- stage 1: framing + N1-point DFTs ----------------
-    if constexpr (NFFT == 400) {
-      const int q = lane >> 3, bb = lane & 7;
-      const int f = warp * C::FPW + q;
-      if (f < nf) {
-        float2 u[25];
-        float2 *row = reinterpret_cast<float2 *>(regions + f * REGION) + bb * C::ROW;
-        load_frame<25, 8>(a, b, (t0 + f) * a.hop - a.pad_left, bb, wave_pair_aligned, win2, row, u);
-        Dft<25>::run(u);
-#pragma unroll
-        for (int c = 0; c < 25; ++c) row[c] = u[c];
-      }
-    } else {
+    // Thread b of frame f: N2 threads per frame (32 / N2 frames per pass).
+    {
+      constexpr int PER = C::N2;
+      constexpr int FPP = 32 / PER < C::FPW ? 32 / PER : C::FPW;  // frames per pass
+      constexpr int PASSES = C::FPW / FPP;
 #pragma unroll 1
-      for (int q = 0; q < C::FPW; ++q) {
+      for (int ps = 0; ps < PASSES; ++ps) {
+        const int q = ps * FPP + lane / PER;
+        const int bb = lane % PER;
         const int f = warp * C::FPW + q;
-        if (f >= nf) break;
-        float2 u[16];
-        float2 *row = reinterpret_cast<float2 *>(regions + f * REGION) + lane * C::ROW;
-        load_frame<16, 32>(a, b, (t0 + f) * a.hop - a.pad_left, lane, wave_pair_aligned, win2, row, u);
-        Dft<16>::run(u);
+        if (lane / PER < FPP && f < nf) {
+          float2 u[C::N1];
+          float2 *row = reinterpret_cast<float2 *>(regions + f * REGION) + bb * C::ROW;
+          load_frame<C::N1, C::N2>(a, b, (t0 + f) * a.hop - a.pad_left, bb, wave_pair_aligned, win2, row, u);
+          Dft<C::N1>::run(u);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) row[c] = u[c];
+          for (int c = 0; c < C::N1; ++c) row[c] = u[c];
+          // The row's padding slots hold zeros, not stale bits: the mel
+          // projection may read (and multiply by a zero weight) a few floats
+          // past a power row, and those must be finite.
+#pragma unroll
+          for (int c = C::N1; c < C::ROW; ++c) row[c] = make_float2(0.f, 0.f);
+        }
       }
     }
     __syncwarp();
@@ -582,13 +592,13 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
     // Frame f's power row sits inside its own region, at float offset
     // f * REGION + shift(f): lanes over the frames of one bin then hit
     // distinct banks in the mel projection.
-    auto prow = [&](int f) { return regions + f * REGION + (NFFT == 400 ? (f >> 1) : f); };
-    if constexpr (NFFT == 400) {
+    auto prow = [&](int f) { return regions + f * REGION + (NFFT == 1024 ? f : (f >> 1)); };
+    if constexpr (NFFT != 1024) {
 #pragma unroll 1
-      for (int q = 0; q < C::FPW; q += C::S2P) {
+      for (int q = 0; q < C::FPW; q += 32 / C::N1) {
         const int f0 = warp * C::FPW + q;
         if (f0 >= nf) break;  // warp-uniform
-        stage2_400<C::S2P>(regions, f0, nf, lane, tw2, twu, a.power_is_one);
+        stage2_cols<NFFT>(regions, f0, nf, lane, tw2, twu, a.power_is_one);
       }
     }
     if constexpr (NFFT == 1024) {
