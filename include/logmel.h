@@ -331,10 +331,16 @@ lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, int64_t T, s
  *             by 1/32768), contiguous, 4-byte aligned.          (read-only)
  *   out       device, [B][n_mels][n_frames] f32 (LM_F32) or f16 (LM_F16),
  *             4-byte aligned.  log_mel plans require LM_F32.
- *   workspace device, >= lm_mel_workspace_size(plan, B, T) bytes.
+ *   workspace device, >= lm_mel_workspace_size(plan, B, T) bytes, 4-byte
+ *             aligned; its contents on entry do not matter.  An 8-byte
+ *             aligned workspace needs no memset before the kernel (the
+ *             kernel clears its error word, tile counter and clip words
+ *             itself, keyed by a per-launch token); a 4-byte aligned one,
+ *             or any call made while the stream is being captured into a
+ *             graph, gets a memset first.
  *
- * Log plans run as one launch where n_fft is 400 or 1024 (the clip floor
- * and rescale are applied by the same cooperative grid; set
+ * Log plans run as one launch where n_fft is 64, 128, 256, 400, 512 or 1024
+ * (the clip floor and rescale are applied by the same cooperative grid; set
  * LOGMEL_K3_EPILOGUE=separate for a second, clamp-only launch instead) and
  * as two launches otherwise.  Non-log plans are one launch.
  *

@@ -41,6 +41,15 @@ constexpr size_t kWorkspaceHeaderBytes = 16;
 // Reads an environment override once; returns `fallback` when unset.
 const char *env_or(const char *name, const char *fallback);
 
+// A token that names one launch: nonzero and never repeated in this process
+// (a 64-bit counter started at a random value).  Kernels that get one clear
+// the workspace words that must start at zero themselves and publish the
+// token once they have; peers wait for it before their first access, so the
+// call needs no memset in front of it.  Returns 0 -- clear the workspace
+// with a memset -- while `stream` is being captured into a graph (a token
+// baked into a graph would repeat on every replay) or when the query fails.
+uint64_t call_token(cudaStream_t stream);
+
 // --- log_mel_from_stft -----------------------------------------------------
 
 // Workspace bytes of lm_log_mel_from_stft for this shape.

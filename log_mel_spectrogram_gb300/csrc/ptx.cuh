@@ -238,6 +238,35 @@ __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Waits (bounded by `limit_ns`) until the launch token at `p` reads `token`:
+// the words a peer cleared before publishing it are then visible to the
+// caller.  Returns false when the wait ran out or `abort_flag` was set.
+static __device__ __noinline__ bool wait_token(const uint64_t *p, uint64_t token, uint64_t limit_ns,
+                                               volatile int *abort_flag) {
+  uint64_t t0 = 0;
+  for (;;) {
+    if (ld_acquire_gpu_u64(p) == token) return true;
+    if (abort_flag && *abort_flag) return false;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > limit_ns) {
+      return false;
+    }
+    __nanosleep(100);
+  }
+}
+
 __device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

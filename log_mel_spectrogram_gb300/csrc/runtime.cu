@@ -1,8 +1,11 @@
 // runtime.cu -- host-side services shared by the entry points: status
 // strings, per-thread CUDA error record, per-device facts, kernel attribute
 // setup and the workspace error-word readback.
+#include <atomic>
+#include <chrono>
 #include <cstdlib>
 #include <mutex>
+#include <random>
 #include <set>
 #include <utility>
 #include <vector>
@@ -65,6 +68,23 @@ lm_status ensure_smem_attribute(const void *kernel, int bytes) {
 const char *env_or(const char *name, const char *fallback) {
   const char *v = std::getenv(name);
   return (v && *v) ? v : fallback;
+}
+
+uint64_t call_token(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return 0;
+  static std::atomic<uint64_t> counter{[] {
+    std::random_device rd;
+    const uint64_t r = (static_cast<uint64_t>(rd()) << 32) ^ rd();
+    return r ^ static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count());
+  }()};
+  uint64_t t = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (t == 0) t = counter.fetch_add(1, std::memory_order_relaxed) + 1;  // 0 means "no token"
+  return t;
 }
 
 }  // namespace lm

@@ -78,6 +78,10 @@ struct WaveArgs {
   uint32_t *clip_key;      // [B] fused log epilogue: the clip's maximum key (0 = none yet)
   uint32_t *clip_done;     // [B] fused log epilogue: tiles of the clip whose maximum is folded in
   int32_t fused;           // 1: the register kernel applies the clip floor and rescale itself
+  int32_t clear_err;       // 1: the error word is this call's own (CTA 0 clears it when there is a token)
+  uint64_t token;          // launch token (0: the host cleared the workspace with a memset)
+  uint64_t *ready;         // with a token: CTA 0 stores it here once the words above that start at zero are
+                           // clear; every CTA waits for it before its first tile claim
   uint64_t total_bytes;    // B * T * sample size
   uint32_t seg_offset;     // shared-memory offset of the two sample-span buffers
   uint32_t seg_bytes;      // bytes per span buffer (multiple of 128)
@@ -91,6 +95,32 @@ struct WaveArgs {
   const unsigned char *tables;  // shared-memory image of the tables (n_fft <= 4096)
   uint32_t tables_bytes;
 };
+
+// Launch token (CTA 0, thread 0): clears the error word (when it is this
+// call's own) and the tile counter, then publishes the token with release
+// order.  The fused epilogue's clip words are cleared by all of CTA 0 before
+// its first block barrier, which this thread passes before publishing.
+__device__ __forceinline__ void publish_cleared(const WaveArgs &a) {
+  if (a.clear_err) *a.err = 0u;
+  *a.next_tile = 0u;
+  __threadfence();
+  st_release_gpu_u64(a.ready, a.token);
+}
+
+// Thread 0: the CTA's next tile from the shared counter.  The first claim of
+// a launch with a token waits (bounded) for CTA 0's token; if that runs out
+// the CTA claims nothing more and the error word says why.
+__device__ __forceinline__ int claim_tile(const WaveArgs &a, bool *token_seen, int *abort_flag_p, int n_tiles) {
+  if (!*token_seen) {
+    if (!wait_token(a.ready, a.token, kWaitTimeoutNs, abort_flag_p)) {
+      *abort_flag_p = 1;
+      atomicOr(a.err, kErrClipTimeout);
+      return n_tiles;
+    }
+    *token_seen = true;
+  }
+  return static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
+}
 
 __device__ __forceinline__ int64_t map_index(int64_t s, int64_t T, int mode, bool *zero) {
   *zero = false;
@@ -237,6 +267,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       if (issued[b] > 0) mbar_wait_drain(&seg_bar[b], (issued[b] - 1u) & 1u, a.err);
   };
   if (threadIdx.x == 0) {
+    if (a.token != 0 && blockIdx.x == 0) publish_cleared(a);
     mbar_init(&seg_bar[0], 1);
     mbar_init(&seg_bar[1], 1);
     mbar_init(&seg_bar[2], 1);
@@ -272,6 +303,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
   const int64_t n_tiles = a.B * a.tiles_per_clip;
   volatile int *next_s = reinterpret_cast<volatile int *>(blk_key + 2);  // n_tiles < 2^31 (host check)
   int it = 0;
+  bool token_seen = a.token == 0;  // thread 0
   for (int64_t tile = blockIdx.x, nxt; tile < n_tiles; tile = nxt, ++it) {
     const int buf = it & 1;
     const int64_t b = tile / a.tiles_per_clip;
@@ -281,7 +313,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     const int nf = left < TF ? static_cast<int>(left) : TF;
     if (threadIdx.x == 0) {
       *blk_key = 0u;
-      *next_s = static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
+      *next_s = claim_tile(a, &token_seen, abort_flag_p, static_cast<int>(n_tiles));
     }
     // Tables loaded / previous tile finished with every buffer.  A wait that
     // gave up in the previous tile (its values are then wrong, but every
@@ -1054,9 +1086,15 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
               std::strcmp(lm::env_or("LOGMEL_K3_EPILOGUE", "auto"), "separate") != 0;
   }
   cudaStream_t s = stream;
-  // Clears the device error word (and, for log plans, the tile slots and the
-  // clip keys and counters).
-  LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, a.log_mel ? need : lm::kWorkspaceHeaderBytes, s));
+  // The device error word, the tile counter and the fused epilogue's clip
+  // keys and counters start at zero (tile slots are each written before they
+  // are read).  With a launch token CTA 0 clears them; without one (stream
+  // capture, or a workspace that is not 8-byte aligned) a memset does.
+  a.clear_err = err_word == nullptr;
+  a.ready = reinterpret_cast<uint64_t *>(static_cast<char *>(workspace) + 8);
+  a.token = (reinterpret_cast<uintptr_t>(workspace) & 7) == 0 ? lm::call_token(s) : 0;
+  if (a.token == 0)
+    LM_CUDA_TRY(cudaMemsetAsync(workspace, 0, a.log_mel ? need : lm::kWorkspaceHeaderBytes, s));
   if (a.fused) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);

@@ -537,7 +537,11 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
     mbar_arrive_expect_tx(tbar, a.tables_bytes);
     bulk_g2s_plain(tables, a.tables, a.tables_bytes, tbar);
   }
-  __syncthreads();  // the barrier is initialised
+  if (a.token != 0 && blockIdx.x == 0 && a.log_mel && a.fused) {
+    for (int64_t i = threadIdx.x; i < 2 * a.B; i += NT) a.clip_key[i] = 0u;  // clip_key, then clip_done
+  }
+  __syncthreads();  // the barrier is initialised (and CTA 0's clip words are clear)
+  if (a.token != 0 && blockIdx.x == 0 && threadIdx.x == 0) publish_cleared(a);
   {
     // Without the tables every later shared-memory index is meaningless: if
     // any thread's wait gave up, the whole CTA stops (after the copy lands).
@@ -551,6 +555,7 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
   const int64_t n_tiles = a.B * a.tiles_per_clip;
   const bool fused = a.log_mel && a.fused;
   int n_pend = 0;  // thread 0: tiles held for the fused epilogue
+  bool token_seen = a.token == 0;  // thread 0
   for (int64_t tile = blockIdx.x, nxt; tile < n_tiles; tile = nxt) {
     const int64_t b = tile / a.tiles_per_clip;
     // a.TF (= TF) frames per tile
@@ -663,7 +668,7 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
       // A CTA whose pending list would overflow claims no further tile; the
       // others take the rest (grid x kPendMax >= tiles).
       *next_s = (fused && n_pend + 1 >= kPendMax) ? static_cast<int>(n_tiles)
-                                                  : static_cast<int>(gridDim.x + atomicAdd(a.next_tile, 1u));
+                                                  : claim_tile(a, &token_seen, abort_flag_p, static_cast<int>(n_tiles));
     }
     __syncthreads();  // every power row of the tile is complete
 

@@ -254,3 +254,28 @@ def test_small_batches_run_one_cluster_per_clip(lm, oracle_mod, monkeypatch):
     assert lm.describe_log_mel_from_stft(w.B, w.F, w.NF, w.NM)["cluster"] == 0
     other = lm.log_mel_from_stft(stft, W, workspace=ws)
     _compare(other.cpu().numpy(), out.cpu().numpy())
+
+
+@pytest.mark.parametrize("variant", ["resident", "twopass", "auto"])
+def test_workspace_garbage_reuse_and_offset(lm, oracle_mod, variant, monkeypatch):
+    """A result may depend neither on what the workspace held before nor on
+    an earlier call with the same workspace: the workspace is filled with
+    random bytes, then used by calls in a row whose clip maxima differ (the
+    quieter batch would take the louder one's maxima from any stale slot),
+    and once through a view 4 bytes off an 8-byte boundary."""
+    monkeypatch.setenv("LOGMEL_K1_VARIANT", variant)
+    dev = torch.device("cuda")
+    B, F, NF, NM = 5, 700, 201, 80
+    n = lm.log_mel_from_stft_workspace_size(B, F, NF, NM)
+    raw = torch.empty(n + 64, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(77)
+    raw.copy_(torch.randint(1, 256, (n + 64,), dtype=torch.uint8, generator=g))
+    base = raw.data_ptr() % 256
+    o8 = (-base) % 256  # a 256-byte aligned start
+    for k, (scale, off) in enumerate(((1.0, o8), (1e-3, o8), (10.0, o8), (1.0, o8 + 4))):
+        stft, W = workloads.stft_inputs(B, F, NF, NM, seed=40 + k)
+        stft = stft * scale
+        ws = raw[off:off + n]
+        out = lm.log_mel_from_stft(stft.to(dev), W.to(dev), workspace=ws)
+        assert lm.workspace_error(ws) == 0
+        _compare(out.cpu().numpy(), oracle_mod.log_mel_from_stft(stft.numpy(), W.numpy()))

@@ -241,3 +241,34 @@ def test_fused_log_epilogue_with_full_pending_lists(lm, oracle_mod, monkeypatch)
         ref = oracle_mod.mel_spectrogram(x[b:b + 1].cpu().numpy(), 16000, 400, 160, 128, f_max=8000.0, log_mel=True)
         _gate(fused[b:b + 1].cpu().numpy(), ref, 1e-4)
     m.close()
+
+
+@pytest.mark.parametrize("n_fft,hop,sr,f_max,log_mel,epilogue", [
+    (400, 160, 16000, 8000.0, True, "auto"),       # register kernel, fused log epilogue
+    (400, 160, 16000, 8000.0, True, "separate"),   # register kernel, clamp kernel after it
+    (1024, 256, 22050, 11025.0, False, "auto"),    # register kernel, no log
+    (2048, 512, 22050, 11025.0, True, "auto"),     # generic kernel, clamp kernel after it
+])
+def test_workspace_garbage_reuse_and_offset(lm, oracle_mod, monkeypatch, n_fft, hop, sr, f_max, log_mel, epilogue):
+    """A call clears its error word, tile counter and clip words itself (no
+    memset in front of it): the workspace is filled with random bytes, then
+    used by calls in a row whose clip maxima differ, and once through a view
+    4 bytes off an 8-byte boundary (the memset path); every result is checked
+    against the oracle."""
+    monkeypatch.setenv("LOGMEL_K3_EPILOGUE", epilogue)
+    dev = torch.device("cuda")
+    B, T = 5, 6 * sr // 2
+    m = lm.MelSpectrogram(sample_rate=sr, n_fft=n_fft, hop_length=hop, n_mels=80, f_max=f_max, log_mel=log_mel)
+    n = m.workspace_size(B, T)
+    raw = torch.empty(n + 512, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(78)
+    raw.copy_(torch.randint(1, 256, (n + 512,), dtype=torch.uint8, generator=g))
+    o8 = (-raw.data_ptr()) % 256
+    for k, (scale, off) in enumerate(((1.0, o8), (1e-3, o8), (10.0, o8), (1.0, o8 + 4))):
+        x = workloads.wave_sines(B, T, sr, seed=90 + k) * scale
+        ws = raw[off:off + n]
+        got = m(x.to(dev), workspace=ws)
+        assert lm.workspace_error(ws) == 0
+        ref = oracle_mod.mel_spectrogram(x.numpy(), sr, n_fft, hop, 80, f_max=f_max, log_mel=log_mel)
+        _gate(got.float().cpu().numpy(), ref.astype(np.float64), 1e-4)
+    m.close()
