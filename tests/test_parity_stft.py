@@ -279,3 +279,21 @@ def test_workspace_garbage_reuse_and_offset(lm, oracle_mod, variant, monkeypatch
         out = lm.log_mel_from_stft(stft.to(dev), W.to(dev), workspace=ws)
         assert lm.workspace_error(ws) == 0
         _compare(out.cpu().numpy(), oracle_mod.log_mel_from_stft(stft.numpy(), W.numpy()))
+
+
+@pytest.mark.parametrize("variant", ["resident", "twopass", "cluster"])
+def test_floor_rewrites_in_every_variant(lm, oracle_mod, variant, monkeypatch):
+    """Values below the clip floor, spread over early, middle and last tiles
+    of every clip (resident mode stores every value as (v + 4) / 4 when
+    computed and stores the ones below the floor again once the clip maximum
+    is known, both during the stream and in the tail)."""
+    monkeypatch.setenv("LOGMEL_K1_VARIANT", variant)
+    B, F = (5, 700) if variant == "cluster" else (8, 3000)
+    stft, W = workloads.stft_inputs(B, F, 201, 80, seed=61)
+    for b in range(B):
+        for f0 in range(37 * b % 120, F, 240):
+            stft[b, f0:f0 + 90] *= 1e-6  # 120 dB down: far below the clip floor
+    got, ref = _run(lm, oracle_mod, stft, W)
+    _compare(got, ref)
+    for b in range(B):
+        assert np.isclose(got[b].min(), got[b].max() - 2.0, atol=1e-5)
