@@ -154,7 +154,13 @@ struct WaveCfg {
   // frame of a band group).  256 with 8-frame tiles beat every other pairing
   // tried at 400 points (160-640 threads, 8 or 16 frames: 50-79 us against
   // 48) and at 1024 (128-512 threads, 4-16 frames: 101-129 us against 95).
-  static constexpr int NT = 256;
+  // Above that shared memory allows one CTA per SM, whose barrier-separated
+  // passes need more warps to hide their latency: 32 clips of 160000 samples,
+  // hop n_fft / 4, 128 bands, L2 flushed, us per call with 256 / 512 / 1024
+  // threads: 2048: 84.0 / 124.9 / 147.5; 4096: 105.5 / 94.2 / 106.5; 8192:
+  // 303.1 / 188.4 / 155.6; 16384: 313.3 / 190.5 / 138.2 (no spills at 64
+  // registers with 1024 threads).
+  static constexpr int NT = NFFT >= 8192 ? 1024 : (NFFT == 4096 ? 512 : 256);
   static_assert(NT % 32 == 0 && NT % TF == 0, "thread count");
   // Up to 4096 every table sits in shared memory; beyond, only the FFT
   // twiddles do and the window, untangle twiddles and filterbank are read
@@ -293,6 +299,9 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     }
   } else {
     for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
+    // Thread 0's abort flag and barriers are initialised before any thread
+    // reads the flag below (that read precedes the loop's first barrier).
+    __syncthreads();
   }
 
   // Tiles are handed out dynamically: a CTA's first tile is its index, each

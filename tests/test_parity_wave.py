@@ -272,3 +272,30 @@ def test_workspace_garbage_reuse_and_offset(lm, oracle_mod, monkeypatch, n_fft, 
         ref = oracle_mod.mel_spectrogram(x.numpy(), sr, n_fft, hop, 80, f_max=f_max, log_mel=log_mel)
         _gate(got.float().cpu().numpy(), ref.astype(np.float64), 1e-4)
     m.close()
+
+
+def test_large_sizes_repeat_between_other_kernels(lm, oracle_mod):
+    """Calls at 8192 and 16384 points, interleaved with register-kernel calls
+    that leave other data in shared memory, give the same bits every time
+    (a CTA may not read its own shared-memory state before it is set), and
+    the first result of each matches the oracle."""
+    dev = torch.device("cuda")
+    T = 3 * 16384 + 77
+    x = workloads.wave_sines(2, T, 16000, seed=71)
+    xd = x.to(dev)
+    other = lm.MelSpectrogram(sample_rate=16000, n_fft=1024, hop_length=256, n_mels=128, f_max=8000.0, log_mel=True)
+    big = {n: lm.MelSpectrogram(sample_rate=16000, n_fft=n, hop_length=n // 2, n_mels=128, f_max=8000.0)
+           for n in (8192, 16384)}
+    first = {}
+    for _ in range(12):
+        for n, m in big.items():
+            other(xd)
+            got = m(xd)
+            if n not in first:
+                first[n] = got.clone()
+                ref = oracle_mod.mel_spectrogram(x.numpy(), 16000, n, n // 2, 128, f_max=8000.0)
+                _gate(got.cpu().numpy(), ref.astype(np.float64), 1e-4)
+            else:
+                assert torch.equal(got, first[n]), n
+    for m in (other, *big.values()):
+        m.close()
