@@ -236,11 +236,11 @@ struct ColCfg {
   static_assert(M == N1 * N2 && N1 <= 32 && 15 + M + 1 + 3 <= REGION, "column layout");
 };
 template <>
-struct Cfg<64> : ColCfg<64, 8, 4, 9, 3> {};
+struct Cfg<64> : ColCfg<64, 8, 4, 9, 4> {};
 template <>
-struct Cfg<128> : ColCfg<128, 8, 8, 9, 3> {};
+struct Cfg<128> : ColCfg<128, 8, 8, 9, 4> {};
 template <>
-struct Cfg<256> : ColCfg<256, 16, 8, 17, 3> {};
+struct Cfg<256> : ColCfg<256, 16, 8, 17, 4> {};
 template <>
 struct Cfg<400> : ColCfg<400, 25, 8, 25, 3> {};  // rows of 25 already spread a column over the banks
 template <>
@@ -782,8 +782,9 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
       if (f < nf) {
         // Up to U bands per thread and pass, every load before any store, so
         // the L2 round trips overlap (in place, one at a time they would
-        // serialise).
-        constexpr int U = 16;
+        // serialise).  Eight where the kernel runs four CTAs per SM: sixteen
+        // would set its register peak above 64.
+        constexpr int U = C::kMinBlocks >= 4 ? 8 : 16;
         float *o = static_cast<float *>(a.out) + b * a.n_mels * a.n_frames + t0 + f;
         for (int m0 = static_cast<int>(threadIdx.x) / LF; m0 < a.n_mels; m0 += NG * U) {
           float v[U];
