@@ -77,6 +77,7 @@ struct WaveArgs {
   uint32_t *next_tile;     // tile counter (workspace header), zero at launch
   uint32_t *clip_key;      // [B] fused log epilogue: the clip's maximum key (0 = none yet)
   uint32_t *clip_done;     // [B] fused log epilogue: tiles of the clip whose maximum is folded in
+  uint32_t *rescale_next;  // fused log epilogue: the next tile to floor and rescale
   int32_t fused;           // 1: the register kernel applies the clip floor and rescale itself
   int32_t clear_err;       // 1: the error word is this call's own (CTA 0 clears it when there is a token)
   uint64_t token;          // launch token (0: the host cleared the workspace with a memset)
@@ -953,8 +954,8 @@ extern "C" lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, i
   const int64_t nfr = lm::frames_for(plan->p, T);
   const int tf = lm::tile_frames(plan->p.n_fft);
   const int64_t tpc = nfr > 0 ? (nfr + tf - 1) / tf : 0;
-  // header | tile keys [B * tpc] | (log plans) clip keys [B] | clip counters [B]
-  const size_t clip_arrays = plan->p.log_mel ? 2 * static_cast<size_t>(B) * sizeof(uint32_t) : 0;
+  // header | tile keys [B * tpc] | (log plans) clip keys [B] | clip counters [B] | rescale counter
+  const size_t clip_arrays = plan->p.log_mel ? (2 * static_cast<size_t>(B) + 1) * sizeof(uint32_t) : 0;
   *bytes = (lm::kWorkspaceHeaderBytes + static_cast<size_t>(B * tpc) * sizeof(uint32_t) + clip_arrays + 255) / 256 *
            256;
   return LM_OK;
@@ -1085,14 +1086,14 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(n_tiles, static_cast<int64_t>(di.sm_count) * per_sm));
   // Log plans on the register kernels apply the clip floor and rescale in the
   // same launch (one cooperative grid; its CTAs wait for each other's clip
-  // maxima) when every tile fits some CTA's pending list; otherwise, or with
-  // LOGMEL_K3_EPILOGUE=separate, the clamp kernel runs after it.
+  // maxima); with LOGMEL_K3_EPILOGUE=separate, and on the generic kernel, the
+  // clamp kernel runs after it.
   {
     const int64_t tpc_ws = (nfr + lm::tile_frames(p.n_fft) - 1) / lm::tile_frames(p.n_fft);  // the workspace layout's
     a.clip_key = a.tile_key + B * tpc_ws;
     a.clip_done = a.clip_key + B;
-    a.fused = use_reg && a.log_mel && static_cast<int64_t>(grid) * lm::reg::kPendMax >= n_tiles &&
-              std::strcmp(lm::env_or("LOGMEL_K3_EPILOGUE", "auto"), "separate") != 0;
+    a.rescale_next = a.clip_done + B;
+    a.fused = use_reg && a.log_mel && std::strcmp(lm::env_or("LOGMEL_K3_EPILOGUE", "auto"), "separate") != 0;
   }
   cudaStream_t s = stream;
   // The device error word, the tile counter and the fused epilogue's clip

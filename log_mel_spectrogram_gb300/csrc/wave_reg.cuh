@@ -43,11 +43,13 @@
 // Log plans finish in the same launch (the KBench spec's per-clip floor and
 // rescale, its "clip-resident" design note): each tile folds its maximum log
 // value into its clip's key and then counts itself into the clip's counter
-// with release order; a CTA keeps the tiles it computed in a short list, and
-// after its last tile waits (bounded) for each listed clip's counter to
-// complete and floors and rescales those tiles in place while they are still
-// in L2.  The grid is cooperative, tiles are claimed in order, and no CTA
-// waits before it has computed every tile it claimed, so every wait ends.
+// with release order.  A CTA that finds no tile left to compute takes tiles
+// to floor and rescale from a second counter, in tile (so clip) order, waits
+// (bounded) for each one's clip counter to complete and rescales the tile in
+// place while it is still in L2 -- so CTAs that run out of work early
+// rescale the early clips while the others still compute the late ones.
+// The grid is cooperative and no CTA waits before every tile has been
+// claimed for computing, so every wait ends.
 #pragma once
 
 namespace reg {
@@ -283,18 +285,13 @@ struct Tables {
   }
 };
 
-// Fused log epilogue: tiles a CTA may hold until their clips' maxima are
-// known (the host keeps grid x kPendMax >= tiles, else it launches the
-// separate clamp kernel).
-constexpr int kPendMax = 32;
-
 // Shared memory: TF frame regions | table image | 16 bytes (tile key, abort
-// flag, next tile, pending count) | one mbarrier and the clip floor |
-// pending tiles [kPendMax].
+// flag, next tile, next tile to rescale) | one mbarrier, the clip floor and
+// 4 spare bytes.
 template <int NFFT>
 size_t smem_bytes(int n_mels, int wmax) {
   using C = Cfg<NFFT>;
-  return 4 * static_cast<size_t>(C::TF) * C::REGION + Tables<NFFT>::bytes(n_mels, wmax) + 16 + 16 + 4 * kPendMax;
+  return 4 * static_cast<size_t>(C::TF) * C::REGION + Tables<NFFT>::bytes(n_mels, wmax) + 16 + 16;
 }
 
 // (max(ls, floor) + 4) / 4 for floor = hi - 8; fma(x, 1/4, 1) rounds exactly
@@ -522,10 +519,9 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
   uint32_t *blk_key = reinterpret_cast<uint32_t *>(tables + a.tables_bytes);
   int *abort_flag_p = reinterpret_cast<int *>(blk_key + 1);
   volatile int *next_s = reinterpret_cast<volatile int *>(blk_key + 2);
-  volatile int *n_pend_s = reinterpret_cast<volatile int *>(blk_key + 3);
+  volatile int *resc_s = reinterpret_cast<volatile int *>(blk_key + 3);
   uint64_t *tbar = reinterpret_cast<uint64_t *>(blk_key + 4);
   volatile float *floor_s = reinterpret_cast<volatile float *>(blk_key + 6);
-  int *pend = reinterpret_cast<int *>(blk_key + 8);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -538,7 +534,8 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
     bulk_g2s_plain(tables, a.tables, a.tables_bytes, tbar);
   }
   if (a.token != 0 && blockIdx.x == 0 && a.log_mel && a.fused) {
-    for (int64_t i = threadIdx.x; i < 2 * a.B; i += NT) a.clip_key[i] = 0u;  // clip_key, then clip_done
+    // clip_key, clip_done and the rescale counter are adjacent
+    for (int64_t i = threadIdx.x; i < 2 * a.B + 1; i += NT) a.clip_key[i] = 0u;
   }
   __syncthreads();  // the barrier is initialised (and CTA 0's clip words are clear)
   if (a.token != 0 && blockIdx.x == 0 && threadIdx.x == 0) publish_cleared(a);
@@ -554,7 +551,6 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
 
   const int64_t n_tiles = a.B * a.tiles_per_clip;
   const bool fused = a.log_mel && a.fused;
-  int n_pend = 0;  // thread 0: tiles held for the fused epilogue
   bool token_seen = a.token == 0;  // thread 0
   for (int64_t tile = blockIdx.x, nxt; tile < n_tiles; tile = nxt) {
     const int64_t b = tile / a.tiles_per_clip;
@@ -664,12 +660,7 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
       }
     }
     }
-    if (threadIdx.x == 0) {
-      // A CTA whose pending list would overflow claims no further tile; the
-      // others take the rest (grid x kPendMax >= tiles).
-      *next_s = (fused && n_pend + 1 >= kPendMax) ? static_cast<int>(n_tiles)
-                                                  : claim_tile(a, &token_seen, abort_flag_p, static_cast<int>(n_tiles));
-    }
+    if (threadIdx.x == 0) *next_s = claim_tile(a, &token_seen, abort_flag_p, static_cast<int>(n_tiles));
     __syncthreads();  // every power row of the tile is complete
 
     // ---------------- mel projection and store ----------------
@@ -733,7 +724,6 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
         // release order: a CTA that sees the count complete sees the maximum.
         atomicMax(a.clip_key + b, *blk_key);
         red_add_release_gpu(a.clip_done + b, 1u);
-        pend[n_pend++] = static_cast<int>(tile);
       } else {
         a.tile_key[tile] = *blk_key;
       }
@@ -742,37 +732,46 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
   }
 
   if (fused) {
-    // Fused epilogue: once every tile of a held tile's clip has folded in its
-    // maximum, floor and rescale the held tile in place (its log values are
-    // still in L2).  Waits only start after this CTA's last tile, so every
-    // tile a wait depends on is computed by a CTA that is not waiting.
-    if (threadIdx.x == 0) *n_pend_s = n_pend;
-    __syncthreads();
-    const int np = *n_pend_s;
-    for (int i = 0; i < np; ++i) {
-      const int64_t tile = pend[i];
-      const int64_t b = tile / a.tiles_per_clip;
+    // Fused epilogue: every tile has been claimed for computing; take tiles to
+    // floor and rescale from the shared counter, in tile order, each once its
+    // clip's counter is complete (its log values are still in L2).  Thread 0
+    // claims the next tile before waiting for the current one's clip.
+    int r_next = 0;  // thread 0
+    if (threadIdx.x == 0) r_next = static_cast<int>(atomicAdd(a.rescale_next, 1u));
+    for (;;) {
       if (threadIdx.x == 0) {
-        bool ok = true;
-        uint64_t tw0 = 0;
-        for (uint32_t it = 0; ld_acquire_gpu(a.clip_done + b) < static_cast<uint32_t>(a.tiles_per_clip); ++it) {
-          if ((it & 15u) == 15u) {
-            const uint64_t now = global_timer_ns();
-            if (tw0 == 0) {
-              tw0 = now;
-            } else if (now - tw0 > kWaitTimeoutNs) {
-              atomicOr(a.err, kErrClipTimeout);
-              ok = false;
-              break;
+        const int r = r_next;
+        float fl = 0.f;
+        if (r < n_tiles) {
+          r_next = static_cast<int>(atomicAdd(a.rescale_next, 1u));
+          const int64_t b = r / a.tiles_per_clip;
+          bool ok = true;
+          uint64_t tw0 = 0;
+          for (uint32_t it = 0; ld_acquire_gpu(a.clip_done + b) < static_cast<uint32_t>(a.tiles_per_clip); ++it) {
+            if ((it & 15u) == 15u) {
+              const uint64_t now = global_timer_ns();
+              if (tw0 == 0) {
+                tw0 = now;
+              } else if (now - tw0 > kWaitTimeoutNs) {
+                atomicOr(a.err, kErrClipTimeout);
+                ok = false;
+                break;
+              }
             }
+            __nanosleep(128);
           }
-          __nanosleep(128);
+          fl = ok ? ordered_to_float(ld_relaxed_gpu(a.clip_key + b)) - 8.0f : __int_as_float(0x7fc00000);
         }
-        *floor_s = ok ? ordered_to_float(ld_relaxed_gpu(a.clip_key + b)) - 8.0f : __int_as_float(0x7fc00000);
+        *resc_s = r;
+        *floor_s = fl;
       }
       __syncthreads();
+      const int64_t tile = *resc_s;
       const float floor_v = *floor_s;
-      if (floor_v != floor_v) break;  // a wait gave up (the error word says so): leave the rest as log values
+      // every tile is taken, or a wait gave up (the error word says so; the
+      // tiles left keep their log values)
+      if (tile >= n_tiles || floor_v != floor_v) break;
+      const int64_t b = tile / a.tiles_per_clip;
       const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(a.TF);
       const int64_t left = a.n_frames - t0;
       const int nf = left < a.TF ? static_cast<int>(left) : a.TF;
@@ -800,7 +799,7 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
           }
         }
       }
-      __syncthreads();  // floor_s is rewritten for the next held tile
+      __syncthreads();  // resc_s and floor_s are rewritten for the next tile
     }
   }
   // This CTA is done: a programmatically dependent epilogue may be scheduled

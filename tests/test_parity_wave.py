@@ -203,7 +203,8 @@ def test_repeat_calls_are_bitwise_identical(lm):
         m.close()
 
 
-@pytest.mark.parametrize("n_fft,hop,sr,f_max", [(400, 160, 16000, 8000.0), (1024, 256, 22050, 11025.0)])
+@pytest.mark.parametrize("n_fft,hop,sr,f_max", [(400, 160, 16000, 8000.0), (1024, 256, 22050, 11025.0),
+                                                (64, 16, 16000, 8000.0), (256, 64, 16000, 8000.0)])
 def test_fused_and_separate_log_epilogues_agree(lm, oracle_mod, monkeypatch, n_fft, hop, sr, f_max):
     # The register kernels floor and rescale log plans in the same launch
     # (the clip maximum gathered across CTAs); LOGMEL_K3_EPILOGUE=separate
@@ -223,10 +224,11 @@ def test_fused_and_separate_log_epilogues_agree(lm, oracle_mod, monkeypatch, n_f
     _gate(fused.cpu().numpy(), ref, 1e-4)
 
 
-def test_fused_log_epilogue_with_full_pending_lists(lm, oracle_mod, monkeypatch):
-    # 442 clips of 10 s: 32 tiles of 32 frames each, about 31 per CTA of the
-    # 400-point kernel, so CTAs fill their lists of held tiles and stop
-    # claiming; the result must not change.
+def test_fused_log_epilogue_many_tiles_per_cta(lm, oracle_mod, monkeypatch):
+    # 442 clips of 10 s: 14,144 tiles of 32 frames, about 31 per CTA of the
+    # 400-point kernel, so CTAs that run out of tiles to compute rescale
+    # finished clips for a long time while others still compute; the result
+    # must equal the separate clamp kernel's, bit for bit.
     x = workloads.wave_sines(442, 160000, 16000, seed=77, device="cuda")
     args = dict(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, log_mel=True)
     m = lm.MelSpectrogram(**args)
