@@ -195,5 +195,62 @@ __device__ __forceinline__ bool run(float2 *a, float2 *b, const float2 *W) {
   }
 }
 
+// In-place form (decimation in time) for transforms too large for two
+// buffers: the input goes to the digit-reversed position dit_pos(n), and the
+// pass of radix R after span P applies butterfly (g, k), k < P, to the
+// elements g R P + k + j P (j < R), multiplying element j by
+// exp(-2 pi i j k / (P R)) -- the same factors, and table rows, as the
+// Stockham pass -- and writing output l back to g R P + k + l P.  After the
+// last pass the result is in natural order.
+//
+// Position of input n: the first pass transforms the R1 inputs n' + j M/R1
+// (j < R1) of group n' < M/R1, which sit at R1 pos_{M/R1}(n') + j.
+template <int M>
+__device__ __forceinline__ int dit_pos(int n) {
+  if constexpr (M == 1) {
+    return 0;
+  } else {
+    constexpr int R = next_radix<M, 1>();
+    constexpr int S = M / R;
+    return dit_pos<S>(n % S) * R + n / S;
+  }
+}
+
+// One in-place pass over one frame of M points (at Layout<M> positions) by
+// NT threads; the twiddle rows are read through L1 from global memory.
+template <int M, int R, int P, int NT>
+__device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict__ W) {
+  constexpr int ITEMS = M / R;
+#pragma unroll
+  for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
+    const int t = static_cast<int>(threadIdx.x) + r * NT;
+    if (ITEMS % NT != 0 && t >= ITEMS) break;
+    const int k = t % P;
+    const int base = (t / P) * R * P + k;
+    float2 u[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) u[j] = x[Layout<M>::at(base + j * P)];
+    if constexpr (P > 1) {
+      const float2 *row = W + rows_offset<M, P>() + k * row_stride<R>();
+#pragma unroll
+      for (int j = 1; j < R; ++j) u[j] = cmul(u[j], __ldg(row + j - 1));
+    }
+    Dft<R>::run(u);
+#pragma unroll
+    for (int l = 0; l < R; ++l) x[Layout<M>::at(base + l * P)] = u[l];
+  }
+}
+
+// Every pass, in place; a block barrier follows each.
+template <int M, int NT, int P = 1>
+__device__ __forceinline__ void run_inplace(float2 *x, const float2 *W) {
+  if constexpr (P < M) {
+    constexpr int R = next_radix<M, P>();
+    pass_inplace<M, R, P, NT>(x, W);
+    __syncthreads();
+    run_inplace<M, NT, P * R>(x, W);
+  }
+}
+
 }  // namespace fft
 }  // namespace lm

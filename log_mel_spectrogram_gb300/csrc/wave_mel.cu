@@ -141,9 +141,21 @@ __device__ __forceinline__ float load_sample(const WaveArgs &a, int64_t b, int64
 
 #include "wave_reg.cuh"
 
+// Above 4096 points one frame's two Stockham buffers and the twiddle table
+// leave room for a single CTA per SM.  At 8192 points the transform runs in
+// place instead (one buffer, the twiddle rows read through L1, a separate
+// power row, samples gathered without staging), which fits two 512-thread
+// CTAs per SM: 32 clips of 160000 samples, hop 2048, L2 flushed, 145.4 us
+// against 155.6 for one 1024-thread Stockham CTA.  At 16384 the in-place form
+// measured slower (147.5 us with two CTAs, 157.7 with one, against 137.5):
+// its digit-reversed stores in the framing step fall into few banks, which
+// only the doubled occupancy at 8192 outweighs.
+constexpr bool in_place_nfft(int n_fft) { return n_fft == 8192; }
+
 template <int NFFT>
 struct WaveCfg {
   static constexpr int M = NFFT / 2;
+  static constexpr bool kInPlace = in_place_nfft(NFFT);
   static constexpr int NF = NFFT / 2 + 1;
   static constexpr int NFP = NF | 1;  // odd power-tile row stride
   // Frames per tile, bounded by shared memory.  Up to 1024 points, 8: at
@@ -160,8 +172,8 @@ struct WaveCfg {
   // hop n_fft / 4, 128 bands, L2 flushed, us per call with 256 / 512 / 1024
   // threads: 2048: 84.0 / 124.9 / 147.5; 4096: 105.5 / 94.2 / 106.5; 8192:
   // 303.1 / 188.4 / 155.6; 16384: 313.3 / 190.5 / 138.2 (no spills at 64
-  // registers with 1024 threads).
-  static constexpr int NT = NFFT >= 8192 ? 1024 : (NFFT == 4096 ? 512 : 256);
+  // registers with 1024 threads).  8192 now runs in place (below).
+  static constexpr int NT = kInPlace ? 512 : (NFFT >= 8192 ? 1024 : (NFFT == 4096 ? 512 : 256));
   static_assert(NT % 32 == 0 && NT % TF == 0, "thread count");
   // Up to 4096 every table sits in shared memory; beyond, only the FFT
   // twiddles do and the window, untangle twiddles and filterbank are read
@@ -171,7 +183,7 @@ struct WaveCfg {
   // capped to match so they do not lower the occupancy further.  400 points
   // gets no minimum (0): the compiler's own choice there is 64 registers,
   // while an explicit 4 made it spill and 1 let it take 104.
-  static constexpr int kMinBlocks = NFFT == 400 ? 0 : (NFFT <= 512 ? 4 : (NFFT <= 1024 ? 2 : 1));
+  static constexpr int kMinBlocks = NFFT == 400 ? 0 : (NFFT <= 512 ? 4 : (NFFT <= 1024 || kInPlace ? 2 : 1));
   static constexpr bool kFuseFirst = (M & (M - 1)) == 0;
   // The power tile (TF rows of NFP floats) lives in whichever FFT buffer does
   // not hold the transform's result; it needs at most half of it.
@@ -196,6 +208,8 @@ inline uint32_t wave_tables_bytes(int n_fft, int n_mels, int wmax) {
 // Shared memory: bufA, bufB [BUF] float2 (TF frames of M points at Layout<M>
 // positions; the power tile reuses one) | the table image (tw_m only above
 // 4096 points) | keys
+//
+// In place (above 4096 points): buf [BUF] float2 | power row [NFP + 1] | keys.
 template <int NFFT>
 size_t wave_smem_bytes(int n_mels, int wmax) {
   using C = WaveCfg<NFFT>;
@@ -205,6 +219,7 @@ size_t wave_smem_bytes(int n_mels, int wmax) {
     b -= sizeof(float2) * C::M;
     b += wave_tables_bytes(NFFT, n_mels, wmax);
   }
+  if (C::kInPlace) b = sizeof(float2) * C::BUF + sizeof(float) * (C::NFP + 1);
   b += 16;  // tile key, abort flag, next tile
   return (b + 127) / 128 * 128;  // the sample-span buffers follow, 128-byte aligned
 }
@@ -215,14 +230,16 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
   constexpr int M = C::M, TF = C::TF, NFP = C::NFP, NT = C::NT;
   extern __shared__ __align__(16) unsigned char smem[];
   float2 *bufA = reinterpret_cast<float2 *>(smem);
-  float2 *bufB = bufA + C::BUF;
-  float *pw = reinterpret_cast<float *>(C::kResultInB ? bufA : bufB);
+  float2 *bufB = bufA + C::BUF;  // (not used in place)
+  float *pw = C::kInPlace ? reinterpret_cast<float *>(bufA + C::BUF)
+                          : reinterpret_cast<float *>(C::kResultInB ? bufA : bufB);
   float2 *twm = bufB + C::BUF;
   float2 *twn_s = twm + M;
   float *fw_s = reinterpret_cast<float *>(twn_s + M + 2);  // 16-byte aligned
   float *win_s = fw_s + a.n_mels * a.wmax;
   int2 *fsw_s = reinterpret_cast<int2 *>(win_s + NFFT);  // {first bin, width} per band
   uint32_t *blk_key = C::kSmallTables ? reinterpret_cast<uint32_t *>(reinterpret_cast<unsigned char *>(twm) + a.tables_bytes)
+                      : C::kInPlace   ? reinterpret_cast<uint32_t *>(pw + NFP + 1)
                                       : reinterpret_cast<uint32_t *>(twm + M);
   const float2 *twn = C::kSmallTables ? twn_s : a.tw_n;
   const float *win = C::kSmallTables ? win_s : a.window;
@@ -238,6 +255,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
   // The contiguous samples an interior tile (no padding in play) reads:
   // bulk-copy range [a0, a0 + bytes) of the waveform, 16-byte aligned.
   auto span_of = [&](int64_t tile, uint64_t *a0, uint32_t *bytes) -> bool {
+    if constexpr (C::kInPlace) return false;  // no staging buffers in that layout
     if (!a.use_seg) return false;
     const int64_t b = tile / a.tiles_per_clip;
     const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(TF);
@@ -299,7 +317,9 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       return;
     }
   } else {
-    for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
+    if constexpr (!C::kInPlace) {
+      for (int i = threadIdx.x; i < M; i += blockDim.x) twm[i] = a.tw_m[i];
+    }
     // Thread 0's abort flag and barriers are initialised before any thread
     // reads the flag below (that read precedes the loop's first barrier).
     __syncthreads();
@@ -473,14 +493,18 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
         }
         z = make_float2(x0 * win[2 * n], x1 * win[2 * n + 1]);
       }
-      bufA[C::L::at(idx)] = z;
+      // in place, point n goes to its digit-reversed position (one frame a tile)
+      bufA[C::L::at(C::kInPlace ? fft::dit_pos<M>(n) : idx)] = z;
     }
     __syncthreads();
 
     // 2. N/2-point complex FFT of every frame (its first pass already done
     // for aligned staged tiles, whose result is then in bufB)
     bool in_b;
-    if constexpr (C::kFuseFirst) {
+    if constexpr (C::kInPlace) {
+      fft::run_inplace<M, NT>(bufA, a.tw_m);
+      in_b = false;
+    } else if constexpr (C::kFuseFirst) {
       if (fused) {
         in_b = !fft::run<M, TF, NT, fft::next_radix<M, 1>()>(bufB, bufA, twm);
       } else {
@@ -1032,7 +1056,7 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
     const size_t seg_bytes =
         (static_cast<size_t>((tf - 1) * static_cast<int64_t>(p.hop_length) + p.n_fft) * esize + 32 + 127) / 128 * 128;
     seg_offset = smem;
-    use_seg = (reinterpret_cast<uintptr_t>(wave) & 15) == 0 &&
+    use_seg = !lm::in_place_nfft(p.n_fft) && (reinterpret_cast<uintptr_t>(wave) & 15) == 0 &&
               seg_offset + 2 * seg_bytes + 32 <= static_cast<size_t>(di.max_smem_optin);
     // Without staging (unaligned input, or a hop so long the spans do not fit)
     // every tile gathers its samples from global memory; the two mbarriers are
