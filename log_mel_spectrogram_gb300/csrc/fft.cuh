@@ -38,6 +38,16 @@ struct Layout {
   __host__ __device__ static constexpr int size(int n) { return kPad ? n + (n >> 5) + 1 : n; }
 };
 
+// The in-place layout adds a second padding slot every 512 elements: the
+// digit-reversed stores of the framing step (consecutive inputs to positions
+// 64, 512 and 4096 apart) then spread over the banks instead of landing in
+// one or two.
+template <int M>
+struct LayoutIP {
+  __host__ __device__ static constexpr int at(int x) { return x + (x >> 5) + (x >> 9); }
+  __host__ __device__ static constexpr int size(int n) { return n + (n >> 5) + (n >> 9) + 1; }
+};
+
 template <int R>
 struct Dft;
 
@@ -216,7 +226,7 @@ __device__ __forceinline__ int dit_pos(int n) {
   }
 }
 
-// One in-place pass over one frame of M points (at Layout<M> positions) by
+// One in-place pass over one frame of M points (at LayoutIP<M> positions) by
 // NT threads; the twiddle rows are read through L1 from global memory.
 template <int M, int R, int P, int NT>
 __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict__ W) {
@@ -229,7 +239,7 @@ __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict
     const int base = (t / P) * R * P + k;
     float2 u[R];
 #pragma unroll
-    for (int j = 0; j < R; ++j) u[j] = x[Layout<M>::at(base + j * P)];
+    for (int j = 0; j < R; ++j) u[j] = x[LayoutIP<M>::at(base + j * P)];
     if constexpr (P > 1) {
       const float2 *row = W + rows_offset<M, P>() + k * row_stride<R>();
 #pragma unroll
@@ -237,7 +247,7 @@ __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict
     }
     Dft<R>::run(u);
 #pragma unroll
-    for (int l = 0; l < R; ++l) x[Layout<M>::at(base + l * P)] = u[l];
+    for (int l = 0; l < R; ++l) x[LayoutIP<M>::at(base + l * P)] = u[l];
   }
 }
 

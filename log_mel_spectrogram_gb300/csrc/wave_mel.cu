@@ -29,6 +29,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include <cuda_fp16.h>
@@ -142,15 +143,15 @@ __device__ __forceinline__ float load_sample(const WaveArgs &a, int64_t b, int64
 #include "wave_reg.cuh"
 
 // Above 4096 points one frame's two Stockham buffers and the twiddle table
-// leave room for a single CTA per SM.  At 8192 points the transform runs in
-// place instead (one buffer, the twiddle rows read through L1, a separate
-// power row, samples gathered without staging), which fits two 512-thread
-// CTAs per SM: 32 clips of 160000 samples, hop 2048, L2 flushed, 145.4 us
-// against 155.6 for one 1024-thread Stockham CTA.  At 16384 the in-place form
-// measured slower (147.5 us with two CTAs, 157.7 with one, against 137.5):
-// its digit-reversed stores in the framing step fall into few banks, which
-// only the doubled occupancy at 8192 outweighs.
-constexpr bool in_place_nfft(int n_fft) { return n_fft == 8192; }
+// (199 KB at 16384) leave room for a single CTA per SM.  Those sizes
+// transform in place instead (one buffer laid out with fft::LayoutIP, the
+// twiddle rows read through L1, a separate power row, samples gathered
+// without staging), which fits two 512-thread CTAs per SM.  32 clips of
+// 160000 samples, hop n_fft / 4, L2 flushed, us per call: 8192: 155.6 with
+// one 1024-thread Stockham CTA, 145.4 in place with one padding level,
+// 141.1 with LayoutIP's two; 16384: 137.2 Stockham, 147.5 in place with one
+// level, 133.1 with two.
+constexpr bool in_place_nfft(int n_fft) { return n_fft >= 8192; }
 
 template <int NFFT>
 struct WaveCfg {
@@ -171,9 +172,9 @@ struct WaveCfg {
   // passes need more warps to hide their latency: 32 clips of 160000 samples,
   // hop n_fft / 4, 128 bands, L2 flushed, us per call with 256 / 512 / 1024
   // threads: 2048: 84.0 / 124.9 / 147.5; 4096: 105.5 / 94.2 / 106.5; 8192:
-  // 303.1 / 188.4 / 155.6; 16384: 313.3 / 190.5 / 138.2 (no spills at 64
-  // registers with 1024 threads).  8192 now runs in place (below).
-  static constexpr int NT = kInPlace ? 512 : (NFFT >= 8192 ? 1024 : (NFFT == 4096 ? 512 : 256));
+  // 303.1 / 188.4 / 155.6; 16384: 313.3 / 190.5 / 138.2.  8192 and 16384 now
+  // run in place, two 512-thread CTAs per SM (see in_place_nfft).
+  static constexpr int NT = (kInPlace || NFFT == 4096) ? 512 : 256;
   static_assert(NT % 32 == 0 && NT % TF == 0, "thread count");
   // Up to 4096 every table sits in shared memory; beyond, only the FFT
   // twiddles do and the window, untangle twiddles and filterbank are read
@@ -188,7 +189,7 @@ struct WaveCfg {
   // The power tile (TF rows of NFP floats) lives in whichever FFT buffer does
   // not hold the transform's result; it needs at most half of it.
   static constexpr bool kResultInB = fft::num_passes<M>() % 2 == 1;
-  using L = fft::Layout<M>;
+  using L = std::conditional_t<kInPlace, fft::LayoutIP<M>, fft::Layout<M>>;
   static constexpr int BUF = L::size(TF * M);  // float2 slots per FFT buffer
   static_assert(TF * NFP * sizeof(float) <= BUF * sizeof(float2), "power tile must fit an FFT buffer");
 };
