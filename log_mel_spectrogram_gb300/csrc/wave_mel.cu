@@ -8,13 +8,18 @@
 // triangular mel filterbank, all computed in double and rounded to f32; the
 // filterbank is packed per band as first nonzero bin, width and weights.
 //
+// n_fft 64...1024 run the register kernels of wave_reg.cuh, which keep each
+// frame's transform inside one warp and finish log plans in the same launch.
+// The generic kernel below serves the larger sizes (and LOGMEL_K3=stockham):
+//
 // Kernel (one persistent CTA per SM slot, tiles of TF consecutive frames of
 // one clip):
 //  1. framing: frame t reads samples t*hop - n_fft/2 + j of the clip; the
 //     padding (reflect / constant / replicate / circular) is index
 //     arithmetic, and tiles that touch no edge load samples directly.  Pairs
 //     of windowed samples form the N/2 complex points z[n] = x[2n] + i x[2n+1];
-//  2. an N/2-point complex FFT in shared memory (fft.cuh);
+//  2. an N/2-point complex FFT in shared memory (fft.cuh): Stockham passes
+//     between two buffers, or in place in one buffer at 8192 and 16384 points;
 //  3. the real-input untangle X[k] = E[k] + exp(-2 pi i k/N) O[k], with
 //     E = (Z[k] + conj Z[N/2-k]) / 2 and O = (Z[k] - conj Z[N/2-k]) / (2i),
 //     straight into a power tile |X[k]|^power (odd row stride);
@@ -51,7 +56,7 @@ struct lm_mel_plan {
   float *fw;     // [n_mels][wmax]
   unsigned char *tables;  // n_fft <= 4096: tw_m | tw_n | window | {fstart, fwidth} | fw, the shared-memory image
   uint32_t tables_bytes;  // its size, a multiple of 16
-  unsigned char *reg_tables;  // n_fft 400 and 1024: the register kernels' image (reg::Tables)
+  unsigned char *reg_tables;  // n_fft 64...1024: the register kernels' image (reg::Tables)
   uint32_t reg_tables_bytes;
 };
 
@@ -1032,7 +1037,7 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   const int esize = in_dtype == LM_I16 ? 2 : 4;
   lm::DeviceInfo di;
   if (lm_status st = lm::current_device_info(&di); st != LM_OK) return st;
-  // n_fft 400 and 1024 run the register kernels (wave_reg.cuh) unless
+  // n_fft 64, 128, 256, 400, 512 and 1024 run the register kernels (wave_reg.cuh) unless
   // LOGMEL_K3=stockham selects the generic shared-memory kernel (for A/B).
   // (The register kernels index samples of a clip with 32 bits at its edges.)
   bool use_reg = plan->reg_tables != nullptr && T < (int64_t{1} << 31) - 2 * (p.n_fft + p.pad) &&
