@@ -540,6 +540,31 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
   __syncthreads();  // the barrier is initialised (and CTA 0's clip words are clear)
   if (a.token != 0 && blockIdx.x == 0 && threadIdx.x == 0) publish_cleared(a);
   {
+    // While the tables are in flight, pull the first tile's samples into L2
+    // (one prefetch per 128-byte line of the tile's span, spread over the
+    // threads), so that the two latencies overlap.
+    const int64_t tile = blockIdx.x;
+    const int64_t b = tile / a.tiles_per_clip;
+    const int64_t t0 = (tile - b * a.tiles_per_clip) * static_cast<int64_t>(a.TF);
+    const int64_t left = a.n_frames - t0;
+    const int nf = left < a.TF ? static_cast<int>(left) : a.TF;
+    int64_t s_lo = t0 * a.hop - a.pad_left;
+    int64_t s_hi = (t0 + nf - 1) * a.hop - a.pad_left + NFFT;  // one past the last sample
+    s_lo = s_lo < 0 ? 0 : s_lo;
+    s_hi = s_hi > a.T ? a.T : s_hi;
+    if (tile < a.B * a.tiles_per_clip && s_lo < s_hi) {
+      const int es = a.in_i16 ? 2 : 4;
+      const char *p0 = static_cast<const char *>(a.wave) + (b * a.T + s_lo) * es;
+      const int64_t lines = ((s_hi - s_lo) * es + 127) / 128 + 1;
+      const uintptr_t l0 = reinterpret_cast<uintptr_t>(p0) & ~uintptr_t{127};
+      for (int64_t i = threadIdx.x; i < lines; i += NT) {
+        const uintptr_t line = l0 + 128 * static_cast<uintptr_t>(i);
+        if (line < reinterpret_cast<uintptr_t>(a.wave) + a.total_bytes)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+      }
+    }
+  }
+  {
     // Without the tables every later shared-memory index is meaningless: if
     // any thread's wait gave up, the whole CTA stops (after the copy lands).
     const bool ok = mbar_wait(tbar, 0, abort_flag_p, a.err);
