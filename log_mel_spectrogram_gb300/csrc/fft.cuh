@@ -1,5 +1,7 @@
-// fft.cuh -- shared-memory mixed-radix complex FFT (Stockham autosort) for
-// the waveform path, plus the small in-register DFT kernels it is made of.
+// fft.cuh -- shared-memory mixed-radix complex FFT for the waveform path:
+// Stockham autosort between two buffers, and an in-place decimation-in-time
+// form in one buffer for the largest sizes (end of file); plus the small
+// in-register DFT kernels both are made of.
 //
 // Forward transform, X[k] = sum_n x[n] exp(-2 pi i n k / M).  A pass of
 // radix R after earlier passes whose radices multiply to P takes element
@@ -214,7 +216,7 @@ __device__ __forceinline__ bool run(float2 *a, float2 *b, const float2 *W) {
 // last pass the result is in natural order.
 //
 // Position of input n: the first pass transforms the R1 inputs n' + j M/R1
-// (j < R1) of group n' < M/R1, which sit at R1 pos_{M/R1}(n') + j.
+// (j < R1) of group n' < M/R1, which sit at R1 dit_pos<M/R1>(n') + j.
 template <int M>
 __device__ __forceinline__ int dit_pos(int n) {
   if constexpr (M == 1) {

@@ -1,6 +1,6 @@
 // runtime.cu -- host-side services shared by the entry points: status
 // strings, per-thread CUDA error record, per-device facts, kernel attribute
-// setup and the workspace error-word readback.
+// setup, per-launch tokens and the workspace error-word readback.
 #include <atomic>
 #include <chrono>
 #include <cstdlib>
