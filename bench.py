@@ -360,7 +360,10 @@ class WaveJob:
         self.units = w.B
         self.bytes = w.canonical_bytes
         self.flops = wave_flops(w)
-        self.kernels = 2 if w.log_mel else 1
+        # log plans: the transform and the clamp kernel (one launch with
+        # LOGMEL_K3_EPILOGUE=fused on the register kernels, n_fft <= 1024)
+        fused = os.environ.get("LOGMEL_K3_EPILOGUE") == "fused" and w.n_fft <= 1024
+        self.kernels = 2 if (w.log_mel and not fused) else 1
         self.flush_l2 = True  # 14-28 MB per step fits in L2
         self.inputs = [self.x]
 

@@ -339,10 +339,12 @@ lm_status lm_mel_workspace_size(const lm_mel_plan *plan, int64_t B, int64_t T, s
  *             or any call made while the stream is being captured into a
  *             graph, gets a memset first.
  *
- * Log plans run as one launch where n_fft is 64, 128, 256, 400, 512 or 1024
- * (the clip floor and rescale are applied by the same cooperative grid; set
- * LOGMEL_K3_EPILOGUE=separate for a second, clamp-only launch instead) and
- * as two launches otherwise.  Non-log plans are one launch.
+ * Log plans run as two launches: the transform, then a clamp-only kernel
+ * launched as a programmatic dependent (its launch overlaps the first
+ * kernel's tail).  With LOGMEL_K3_EPILOGUE=fused, where n_fft is 64, 128,
+ * 256, 400, 512 or 1024, the clip floor and rescale are applied by the same
+ * cooperative grid instead (one launch, the same bits; measured slower).
+ * Non-log plans are one launch.
  *
  * Errors: LM_ERR_INVALID_ARG (null pointers, T too short for reflect
  * padding, n_frames < 1), LM_ERR_UNSUPPORTED (dtype combination),

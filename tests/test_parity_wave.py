@@ -206,14 +206,15 @@ def test_repeat_calls_are_bitwise_identical(lm):
 @pytest.mark.parametrize("n_fft,hop,sr,f_max", [(400, 160, 16000, 8000.0), (1024, 256, 22050, 11025.0),
                                                 (64, 16, 16000, 8000.0), (256, 64, 16000, 8000.0)])
 def test_fused_and_separate_log_epilogues_agree(lm, oracle_mod, monkeypatch, n_fft, hop, sr, f_max):
-    # The register kernels floor and rescale log plans in the same launch
-    # (the clip maximum gathered across CTAs); LOGMEL_K3_EPILOGUE=separate
-    # runs the clamp kernel after them instead.  Both give the same bits, and
-    # the oracle's values.
+    # With LOGMEL_K3_EPILOGUE=fused the register kernels floor and rescale
+    # log plans in the same launch (the clip maximum gathered across CTAs);
+    # by default (separate) the clamp kernel runs after them.  Both give the
+    # same bits, and the oracle's values.
     x = workloads.wave_sines(5, 37000, sr, seed=n_fft + 5)
     x[2, 20000:] *= 1e-5  # the clip floor matters
     args = dict(sample_rate=sr, n_fft=n_fft, hop_length=hop, n_mels=128, f_max=f_max, log_mel=True)
     m = lm.MelSpectrogram(**args)
+    monkeypatch.setenv("LOGMEL_K3_EPILOGUE", "fused")
     fused = m(x.cuda())
     monkeypatch.setenv("LOGMEL_K3_EPILOGUE", "separate")
     sep = m(x.cuda())
@@ -233,6 +234,7 @@ def test_fused_log_epilogue_many_tiles_per_cta(lm, oracle_mod, monkeypatch):
     args = dict(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, log_mel=True)
     m = lm.MelSpectrogram(**args)
     ws = torch.empty(m.workspace_size(442, 160000), dtype=torch.uint8, device="cuda")
+    monkeypatch.setenv("LOGMEL_K3_EPILOGUE", "fused")
     fused = m(x, workspace=ws)
     assert lm.workspace_error(ws) == 0
     monkeypatch.setenv("LOGMEL_K3_EPILOGUE", "separate")
@@ -246,7 +248,7 @@ def test_fused_log_epilogue_many_tiles_per_cta(lm, oracle_mod, monkeypatch):
 
 
 @pytest.mark.parametrize("n_fft,hop,sr,f_max,log_mel,epilogue", [
-    (400, 160, 16000, 8000.0, True, "auto"),       # register kernel, fused log epilogue
+    (400, 160, 16000, 8000.0, True, "fused"),      # register kernel, fused log epilogue
     (400, 160, 16000, 8000.0, True, "separate"),   # register kernel, clamp kernel after it
     (1024, 256, 22050, 11025.0, False, "auto"),    # register kernel, no log
     (2048, 512, 22050, 11025.0, True, "auto"),     # generic kernel, clamp kernel after it
