@@ -565,7 +565,8 @@ def run_ours(args, world, rank, local):
         e2e_steps_ms = []
         if e2e_steps:
             h2d, d2h = job.host_setup()
-            job.host_step()  # warm-up: creates the library's copy streams
+            for _ in range(max(1, args.warmup)):
+                job.host_step()  # warm-up (the first creates the library's copy streams)
             torch.cuda.synchronize(dev)
             barrier()
             marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
