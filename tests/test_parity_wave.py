@@ -303,3 +303,17 @@ def test_large_sizes_repeat_between_other_kernels(lm, oracle_mod):
                 assert torch.equal(got, first[n]), n
     for m in (other, *big.values()):
         m.close()
+
+
+@pytest.mark.parametrize("n_fft,win_length,pad,normalized,center,pad_mode,power", [
+    (4096, 3000, 0, True, True, "circular", 2.0),      # generic kernel, Stockham, tables in shared memory
+    (8192, 5000, 100, True, False, "constant", 1.0),   # in place, no centre padding, magnitude
+    (16384, 16384, 37, False, True, "replicate", 2.0),  # in place, replicate padding after `pad` zeros
+])
+def test_large_sizes_argument_surface(lm, oracle_mod, n_fft, win_length, pad, normalized, center, pad_mode, power):
+    # The torchaudio argument surface on the large-size paths; a few frames a
+    # clip keep the oracle's direct DFT to seconds.
+    T = 2 * n_fft + 500
+    x = workloads.wave_sines(2, T, 16000, seed=n_fft + 9)
+    _run(lm, oracle_mod, x, 16000, n_fft, n_fft // 4, 96, f_max=8000.0, center=center, pad_mode=pad_mode,
+         power=power, win_length=win_length, pad=pad, normalized=normalized)
