@@ -854,7 +854,20 @@ __global__ void __launch_bounds__(256) logmel_clamp_kernel(float *out, const uin
   // values: wait until that grid has finished and its writes are visible
   // (a no-op for an ordinary launch).
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int U = 8;  // 16-byte loads in flight per thread before any store
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+    float *o = out + b * per_clip;
+    float4 *o4 = reinterpret_cast<float4 *>(o);
+    const int64_t n4 = vec4 ? per_clip / 4 : 0;
+    // The first values' loads do not depend on the clip maximum: they are
+    // issued before the tile slots are reduced, so the two L2 round trips
+    // overlap.
+    int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * stride < n4) v[u] = o4[i0 + u * stride];
     uint32_t m = 0;
     for (int i = threadIdx.x; i < tiles_per_clip; i += blockDim.x) m = max(m, tile_key[b * tiles_per_clip + i]);
     m = __reduce_max_sync(0xffffffffu, m);
@@ -864,20 +877,10 @@ __global__ void __launch_bounds__(256) logmel_clamp_kernel(float *out, const uin
     for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = max(m, warp_keys[w]);
     __syncthreads();
     const float floor_v = ordered_to_float(m) - 8.0f;
-    float *o = out + b * per_clip;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (vec4) {
-      // Eight 16-byte loads in flight per thread before any store: the
-      // rewrite is in place, so one-at-a-time would wait an L2 round trip
-      // per vector.
-      constexpr int U = 8;
-      float4 *o4 = reinterpret_cast<float4 *>(o);
-      const int64_t n4 = per_clip / 4;
-      for (int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i0 < n4; i0 += U * stride) {
-        float4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (i0 + u * stride < n4) v[u] = o4[i0 + u * stride];
+      // In place: every load of a pass before any of its stores, so that
+      // one-at-a-time does not wait an L2 round trip per vector.
+      while (i0 < n4) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           if (i0 + u * stride < n4) {
@@ -889,6 +892,10 @@ __global__ void __launch_bounds__(256) logmel_clamp_kernel(float *out, const uin
             o4[i0 + u * stride] = w;
           }
         }
+        i0 += U * stride;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (i0 + u * stride < n4) v[u] = o4[i0 + u * stride];
       }
     } else {
       for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < per_clip; i += stride)
