@@ -244,7 +244,8 @@ lm_status lm_log_mel_from_stft_noalloc_error(uint32_t *device_error, int32_t cle
  * used by lm_log_mel_from_stft or lm_mel_spectrogram.  *device_error = 0
  * means no kernel reported a problem; otherwise it holds bit flags:
  *   1  an mbarrier wait inside a kernel ran out (2 s)
- *   2  waiting for a clip's maximum ran out
+ *   2  waiting for another CTA's result ran out (a clip's maximum, or
+ *      the launch token of the CTA that clears the workspace)
  *   4  a filter pack did not match the call (the dense matrix was used)
  * Returns LM_ERR_DEVICE_FAULT when it is nonzero. */
 lm_status lm_workspace_error(const void *workspace, size_t workspace_bytes, uint32_t *device_error,

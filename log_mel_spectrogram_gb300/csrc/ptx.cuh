@@ -15,7 +15,7 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 // Device error word bits.
 constexpr uint32_t kErrMbarTimeout = 1u;    // an mbarrier wait ran out
-constexpr uint32_t kErrClipTimeout = 2u;    // waiting for a clip's maximum ran out
+constexpr uint32_t kErrClipTimeout = 2u;    // waiting for another CTA (a clip's maximum, a launch token) ran out
 constexpr uint32_t kErrBadPack = 4u;        // packed filters do not match the call (the dense matrix was used)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
