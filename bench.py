@@ -10,9 +10,12 @@ Prints one JSON line (rank 0).  ``value`` is whole-job clips/s with inputs
 already resident in HBM; ``e2e`` is the same metric through the library's
 host-buffer call (lm_log_mel_from_stft_host / lm_mel_spectrogram_host): the
 batch starts in page-locked host memory and the result ends there, with both
-copies inside the timed region.  ``--impl reference`` times the CPU oracle (the
-plain double-precision definition) on the host cores, on a bounded sample
-of the same workload per step.
+copies inside the timed region.  ``cpu_baseline`` times the CPU oracle on
+the host cores on each workload's whole batch, and ``parity`` compares the
+GPU result of the timed steps with that oracle output element by element.
+``--impl reference`` times the CPU oracle (the plain double-precision
+definition) on the host cores, on a bounded sample of the same workload per
+step.
 
 Under torchrun with N > 1 ranks each rank runs its own full batch on its own
 GPU (independent replicas, weak scaling; no collective on the data path).
@@ -211,37 +214,67 @@ class ClockSampler:
                 "source": self.source}
 
 
-def cpu_baseline(stft_host, W_host, target_s: float = 12.0, sample_note: str = "") -> dict:
+def parity_errors(got, ref, tol: float) -> dict:
+    """Elementwise comparison of a GPU result with the oracle's: the largest
+    absolute error, the largest relative error (over elements with
+    |oracle| >= 1e-2: log-mel outputs pass through zero), the relative
+    Frobenius error, the largest ratio of an element's error to its allowance
+    tol + tol |oracle| (<= 1 inside the gate), and whether every element is
+    inside the gate."""
+    import numpy as np
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    err = np.abs(g - r)
+    big = np.abs(r) >= 1e-2
+    allow = tol + tol * np.abs(r)
+    return {"vs": "oracle, whole batch", "max_abs": float(err.max()),
+            "max_rel": float((err[big] / np.abs(r[big])).max()) if big.any() else 0.0,
+            "rel_fro": float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)),
+            "gate": f"|gpu - oracle| <= {tol:g} + {tol:g} |oracle|",
+            "max_gate_ratio": float((err / allow).max()),
+            "within_gate": bool(np.all(err <= allow))}
+
+
+def cpu_baseline(stft_host, W_host, target_s: float = 12.0, sample_note: str = "", got=None) -> dict:
     """Times the oracle (as it stands) on the given clips, processed
-    repeatedly until about target_s seconds of CPU work are done."""
+    repeatedly until about target_s seconds of CPU work are done.  With `got`
+    (the GPU result for the same clips) the dict also carries "parity"."""
     import oracle
     oracle.build()
     n_clips = stft_host.shape[0]
     done = 0
     t0 = time.perf_counter()
     while True:
-        oracle.log_mel_from_stft(stft_host, W_host)
+        ref = oracle.log_mel_from_stft(stft_host, W_host)
         done += n_clips
         dt = time.perf_counter() - t0
         if dt >= target_s:
             break
-    return {"value": done / dt, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{done} clips ({n_clips} distinct clips{sample_note}, repeated) in {dt:.1f} s, dense "
-                      "double-precision oracle, OpenMP over clips"}
+    out = {"value": done / dt, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"{done} clips ({n_clips} distinct clips{sample_note}, repeated) in {dt:.1f} s, dense "
+                     "double-precision oracle, OpenMP over clips"}
+    if got is not None:
+        out["parity"] = parity_errors(got, ref, 1e-4)
+    return out
 
 
-def cpu_baseline_wave(w, x_host) -> dict:
-    """Times the oracle once on the whole waveform batch."""
+def cpu_baseline_wave(w, x_host, got=None) -> dict:
+    """Times the oracle once on the whole waveform batch; with `got` (the GPU
+    result) the dict also carries "parity" (f16 output against the oracle
+    rounded to f16, at 2e-3)."""
     import oracle
     oracle.build()
     t0 = time.perf_counter()
-    oracle.mel_spectrogram(x_host, w.sample_rate, w.n_fft, w.hop_length, w.n_mels, f_min=w.f_min, f_max=w.f_max,
-                           center=w.center, pad_mode=w.pad_mode, power=w.power, mel_scale=w.mel_scale, norm=w.norm,
-                           log_mel=w.log_mel, out_dtype=w.out_dtype)
+    ref = oracle.mel_spectrogram(x_host, w.sample_rate, w.n_fft, w.hop_length, w.n_mels, f_min=w.f_min,
+                                 f_max=w.f_max, center=w.center, pad_mode=w.pad_mode, power=w.power,
+                                 mel_scale=w.mel_scale, norm=w.norm, log_mel=w.log_mel, out_dtype=w.out_dtype)
     dt = time.perf_counter() - t0
-    return {"value": w.B / dt, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"the whole batch ({w.B} clips) once in {dt:.1f} s: explicit padding and frames, O(N^2) "
-                      "DFT, dense filterbank, double precision, OpenMP over clips"}
+    out = {"value": w.B / dt, "unit": "clips/s", "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"the whole batch ({w.B} clips) once in {dt:.1f} s: explicit padding and frames, O(N^2) "
+                     "DFT, dense filterbank, double precision, OpenMP over clips"}
+    if got is not None:
+        out["parity"] = parity_errors(got, ref, 2e-3 if w.out_dtype == "f16" else 1e-4)
+    return out
 
 
 STFT_JOBS = ("stft_small", "stft_b8", "stft")
@@ -335,7 +368,7 @@ class StftJob:
         # the whole batch (256 clips take about a second on 16 cores), repeated
         # for a stable figure
         return cpu_baseline(self.stft.cpu().numpy(), self.W.cpu().numpy(), target_s=2.0 if w.B <= 8 else 10.0,
-                            sample_note=": the whole batch")
+                            sample_note=": the whole batch", got=self.out.cpu().numpy())
 
 
 class WaveJob:
@@ -413,7 +446,7 @@ class WaveJob:
                 "launch_ms_mean": mean_launch_s * 1e3, "launch_ms_min": min_launch_s * 1e3}
 
     def cpu_baseline(self):
-        return cpu_baseline_wave(self.w, self.x.cpu().numpy())
+        return cpu_baseline_wave(self.w, self.x.cpu().numpy(), got=self.out.float().cpu().numpy())
 
 
 # FP32 FMA peak of the GPU from its unit counts and clock: 152 SMs x 128
@@ -652,16 +685,23 @@ def run_ours(args, world, rank, local):
         "clocks_all_timed_regions": clocks_all,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # The oracle's run on each whole batch doubles as a parity check of
+        # the GPU result the timed steps produced.
         result["cpu_baseline"] = job.cpu_baseline()
+        result["parity"] = result["cpu_baseline"].pop("parity", None)
         for name, entry in configs.items():
             cj = make_job(lm, workloads, dev, name)
+            for _ in range(max(1, args.warmup)):
+                cj.step()
             entry["cpu_baseline"] = cj.cpu_baseline()
+            entry["parity"] = entry["cpu_baseline"].pop("parity", None)
             del cj
     if configs:
         head = {"workload": job.w.name, "value": value, "unit": "clips/s", "steps": args.steps,
                 "ms_per_step": ms_per_step, "roofline": roof, "see": "the top-level keys of this line"}
         if "cpu_baseline" in result:
             head["cpu_baseline"] = result["cpu_baseline"]
+            head["parity"] = result.get("parity")
         configs[args.workload] = head
         result["configs"] = {n: configs[n] for n in CONFIG_ORDER if n in configs}
     if rank == 0:
