@@ -247,6 +247,9 @@ lm_status lm_log_mel_from_stft_noalloc_error(uint32_t *device_error, int32_t cle
  *   2  waiting for another CTA's result ran out (a clip's maximum, or
  *      the launch token of the CTA that clears the workspace)
  *   4  a filter pack did not match the call (the dense matrix was used)
+ *   8  (only in the bounds-checked debug build, compiled with
+ *      -DLOGMEL_CHECKED) a computed global-memory index fell outside its
+ *      buffer; the access was skipped
  * Returns LM_ERR_DEVICE_FAULT when it is nonzero. */
 lm_status lm_workspace_error(const void *workspace, size_t workspace_bytes, uint32_t *device_error,
                              lm_stream_t stream);

@@ -60,53 +60,71 @@ def lib() -> ctypes.CDLL:
         if not path.exists():
             raise RuntimeError(f"liblogmel.so is not built ({path}); run __graft_entry__.build() "
                                "or python -m log_mel_spectrogram_gb300.build")
-        L = ctypes.CDLL(str(path))
-        i64, i32, u32, sz, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t, ctypes.c_void_p
-        L.lm_status_string.argtypes = [ctypes.c_int]
-        L.lm_status_string.restype = ctypes.c_char_p
-        L.lm_last_cuda_error.restype = ctypes.c_int
-        L.lm_version.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_workspace_size.argtypes = [i64, i64, i32, i32, ctypes.POINTER(sz)]
-        L.lm_log_mel_from_stft_workspace_size.restype = ctypes.c_int
-        L.lm_log_mel_from_stft.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, sz, vp]
-        L.lm_log_mel_from_stft.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_describe.argtypes = [i64, i64, i32, i32, ctypes.POINTER(StftLaunchInfo)]
-        L.lm_log_mel_from_stft_describe.restype = ctypes.c_int
-        L.lm_mel_filters_pack_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
-        L.lm_mel_filters_pack_size.restype = ctypes.c_int
-        L.lm_mel_filters_pack.argtypes = [vp, i32, i32, vp, sz, vp]
-        L.lm_mel_filters_pack.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_packed.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, sz, vp]
-        L.lm_log_mel_from_stft_packed.restype = ctypes.c_int
-        L.lm_workspace_error.argtypes = [vp, sz, ctypes.POINTER(u32), vp]
-        L.lm_workspace_error.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
-        L.lm_log_mel_from_stft_noalloc.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_noalloc_error.argtypes = [ctypes.POINTER(u32), i32, vp]
-        L.lm_log_mel_from_stft_noalloc_error.restype = ctypes.c_int
-        L.lm_debug_log_mel_from_stft_withhold.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, sz, i64,
-                                                          ctypes.c_uint64, vp]
-        L.lm_debug_log_mel_from_stft_withhold.restype = ctypes.c_int
-        L.lm_mel_plan_create.argtypes = [ctypes.POINTER(MelParams), ctypes.POINTER(vp)]
-        L.lm_mel_plan_create.restype = ctypes.c_int
-        L.lm_mel_plan_destroy.argtypes = [vp]
-        L.lm_mel_plan_destroy.restype = ctypes.c_int
-        L.lm_mel_n_frames.argtypes = [vp, i64, ctypes.POINTER(i64)]
-        L.lm_mel_n_frames.restype = ctypes.c_int
-        L.lm_mel_workspace_size.argtypes = [vp, i64, i64, ctypes.POINTER(sz)]
-        L.lm_mel_workspace_size.restype = ctypes.c_int
-        L.lm_mel_spectrogram.argtypes = [vp, vp, i32, i64, i64, vp, i32, vp, sz, vp]
-        L.lm_mel_spectrogram.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_host_workspace_size.argtypes = [i64, i64, i32, i32, i64, ctypes.POINTER(sz)]
-        L.lm_log_mel_from_stft_host_workspace_size.restype = ctypes.c_int
-        L.lm_log_mel_from_stft_host.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i64, vp, sz, vp]
-        L.lm_log_mel_from_stft_host.restype = ctypes.c_int
-        L.lm_mel_spectrogram_host_workspace_size.argtypes = [vp, i64, i64, i32, i32, i64, ctypes.POINTER(sz)]
-        L.lm_mel_spectrogram_host_workspace_size.restype = ctypes.c_int
-        L.lm_mel_spectrogram_host.argtypes = [vp, vp, i32, i64, i64, vp, i32, i64, vp, sz, vp]
-        L.lm_mel_spectrogram_host.restype = ctypes.c_int
-        _lib = L
+        _lib = _declare(ctypes.CDLL(str(path)))
         return _lib
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Argument and result types of every entry point (include/logmel.h)."""
+    i64, i32, u32, sz, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t, ctypes.c_void_p
+    L.lm_status_string.argtypes = [ctypes.c_int]
+    L.lm_status_string.restype = ctypes.c_char_p
+    L.lm_last_cuda_error.restype = ctypes.c_int
+    L.lm_version.restype = ctypes.c_int
+    L.lm_log_mel_from_stft_workspace_size.argtypes = [i64, i64, i32, i32, ctypes.POINTER(sz)]
+    L.lm_log_mel_from_stft_workspace_size.restype = ctypes.c_int
+    L.lm_log_mel_from_stft.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, sz, vp]
+    L.lm_log_mel_from_stft.restype = ctypes.c_int
+    L.lm_log_mel_from_stft_describe.argtypes = [i64, i64, i32, i32, ctypes.POINTER(StftLaunchInfo)]
+    L.lm_log_mel_from_stft_describe.restype = ctypes.c_int
+    L.lm_mel_filters_pack_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
+    L.lm_mel_filters_pack_size.restype = ctypes.c_int
+    L.lm_mel_filters_pack.argtypes = [vp, i32, i32, vp, sz, vp]
+    L.lm_mel_filters_pack.restype = ctypes.c_int
+    L.lm_log_mel_from_stft_packed.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp, sz, vp]
+    L.lm_log_mel_from_stft_packed.restype = ctypes.c_int
+    L.lm_workspace_error.argtypes = [vp, sz, ctypes.POINTER(u32), vp]
+    L.lm_workspace_error.restype = ctypes.c_int
+    L.lm_log_mel_from_stft_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp]
+    L.lm_log_mel_from_stft_noalloc.restype = ctypes.c_int
+    L.lm_log_mel_from_stft_noalloc_error.argtypes = [ctypes.POINTER(u32), i32, vp]
+    L.lm_log_mel_from_stft_noalloc_error.restype = ctypes.c_int
+    L.lm_debug_log_mel_from_stft_withhold.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, sz, i64,
+                                                      ctypes.c_uint64, vp]
+    L.lm_debug_log_mel_from_stft_withhold.restype = ctypes.c_int
+    L.lm_mel_plan_create.argtypes = [ctypes.POINTER(MelParams), ctypes.POINTER(vp)]
+    L.lm_mel_plan_create.restype = ctypes.c_int
+    L.lm_mel_plan_destroy.argtypes = [vp]
+    L.lm_mel_plan_destroy.restype = ctypes.c_int
+    L.lm_mel_n_frames.argtypes = [vp, i64, ctypes.POINTER(i64)]
+    L.lm_mel_n_frames.restype = ctypes.c_int
+    L.lm_mel_workspace_size.argtypes = [vp, i64, i64, ctypes.POINTER(sz)]
+    L.lm_mel_workspace_size.restype = ctypes.c_int
+    L.lm_mel_spectrogram.argtypes = [vp, vp, i32, i64, i64, vp, i32, vp, sz, vp]
+    L.lm_mel_spectrogram.restype = ctypes.c_int
+    L.lm_log_mel_from_stft_host_workspace_size.argtypes = [i64, i64, i32, i32, i64, ctypes.POINTER(sz)]
+    L.lm_log_mel_from_stft_host_workspace_size.restype = ctypes.c_int
+    L.lm_log_mel_from_stft_host.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i64, vp, sz, vp]
+    L.lm_log_mel_from_stft_host.restype = ctypes.c_int
+    L.lm_mel_spectrogram_host_workspace_size.argtypes = [vp, i64, i64, i32, i32, i64, ctypes.POINTER(sz)]
+    L.lm_mel_spectrogram_host_workspace_size.restype = ctypes.c_int
+    L.lm_mel_spectrogram_host.argtypes = [vp, vp, i32, i64, i64, vp, i32, i64, vp, sz, vp]
+    L.lm_mel_spectrogram_host.restype = ctypes.c_int
+    return L
+
+
+_checked = None
+
+
+def checked_lib() -> ctypes.CDLL:
+    """The bounds-checked debug variant (-DLOGMEL_CHECKED): every computed
+    global-memory index is tested against its buffer, and one outside sets
+    bit 8 of the error word and skips the access.  Built on first use."""
+    global _checked
+    with _lock:
+        if _checked is None:
+            _checked = _declare(ctypes.CDLL(str(_build.build(checked=True))))
+        return _checked
 
 
 def check(status: int, what: str) -> None:

@@ -17,6 +17,23 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr uint32_t kErrMbarTimeout = 1u;    // an mbarrier wait ran out
 constexpr uint32_t kErrClipTimeout = 2u;    // waiting for another CTA (a clip's maximum, a launch token) ran out
 constexpr uint32_t kErrBadPack = 4u;        // packed filters do not match the call (the dense matrix was used)
+constexpr uint32_t kErrBounds = 8u;         // checked builds: an index fell outside its buffer (access skipped)
+
+// Checked builds (-DLOGMEL_CHECKED, a debug variant of the library) test the
+// computed indices of global-memory accesses against their buffers: an index
+// outside [0, n) sets kErrBounds in the error word and the access is skipped,
+// so a wrong index shows up as an error bit instead of a fault.  In regular
+// builds LM_IN_BOUNDS is the constant true and costs nothing.
+#ifdef LOGMEL_CHECKED
+__device__ __forceinline__ bool in_bounds_checked(int64_t i, int64_t n, uint32_t *err) {
+  if (i >= 0 && i < n) return true;
+  atomicOr(err, kErrBounds);
+  return false;
+}
+#define LM_IN_BOUNDS(i, n, err) (::lm::in_bounds_checked(static_cast<int64_t>(i), static_cast<int64_t>(n), (err)))
+#else
+#define LM_IN_BOUNDS(i, n, err) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

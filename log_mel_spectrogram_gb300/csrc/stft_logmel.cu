@@ -235,7 +235,8 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
     if (c.active) {
 #pragma unroll
       for (int j = 0; j < FPT; ++j)
-        if (c.fg + j * a.FG < nf) __stcs(o + j * ostep, rescale(r[j * ostep], floor_v));
+        if (c.fg + j * a.FG < nf && LM_IN_BOUNDS((o - a.out) + j * ostep, a.B * a.F * a.NM, a.err))
+          __stcs(o + j * ostep, rescale(r[j * ostep], floor_v));
     }
     if (++sslot == kLag + 1) sslot = 0;
     return true;
@@ -277,7 +278,11 @@ __device__ __forceinline__ void consume(const StftArgs &a, unsigned char *smem, 
           }
           const float v = fast_log10(fmaxf(acc, 1e-10f));
           lmax = fmaxf(lmax, v);
-          dst[j * ostep] = v;
+          if constexpr (kResident) {
+            dst[j * ostep] = v;  // the shared-memory ring
+          } else {
+            if (LM_IN_BOUNDS((dst - a.out) + j * ostep, a.B * a.F * a.NM, a.err)) dst[j * ostep] = v;
+          }
         }
       }
     }
@@ -402,7 +407,6 @@ __device__ __forceinline__ int setup_band(const StftArgs &a, SmemAux &aux, Band 
 
 template <int FPT, bool kResident, int CW>
 __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const StftArgs a) {
-  constexpr int kConsumers = CW * 32;
   constexpr int kProducerWarp = CW;
   constexpr int kPublisherWarp = CW + 1;
   constexpr int kResolverWarp = CW + 2;
@@ -467,17 +471,24 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
         }
         if (lo < base) {
           // the first tile of a tensor that starts 8 bytes past a boundary
-          *reinterpret_cast<float2 *>(dst + (start - a0)) = *reinterpret_cast<const float2 *>(start);
+          if (LM_IN_BOUNDS(start - base, a.total_bytes - 7, a.err))
+            *reinterpret_cast<float2 *>(dst + (start - a0)) = *reinterpret_cast<const float2 *>(start);
           lo += 16;
           generic_written |= 1u << s;
         }
         if (hi > limit) {
           // the last tile of a tensor that ends 8 bytes past a boundary
-          *reinterpret_cast<float2 *>(dst + (end - 8 - a0)) = *reinterpret_cast<const float2 *>(end - 8);
+          if (LM_IN_BOUNDS(end - 8 - base, a.total_bytes - 7, a.err))
+            *reinterpret_cast<float2 *>(dst + (end - 8 - a0)) = *reinterpret_cast<const float2 *>(end - 8);
           hi = end & ~15ull;
           generic_written |= 1u << s;
         }
-        const uint32_t bytes = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+        uint32_t bytes = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+        // (checked builds) the copied range lies inside the tensor; if not,
+        // nothing is copied and the error word says so
+        if (bytes > 0 && !(LM_IN_BOUNDS(lo - base, a.total_bytes, a.err) &&
+                           LM_IN_BOUNDS(hi - 1 - base, a.total_bytes, a.err)))
+          bytes = 0;
         const int d = static_cast<int>(k & (kSlots - 1));
         aux.desc_frame0[d] = it.first_frame(a);
         aux.desc_nf[d] = it.frames(a);
@@ -509,7 +520,7 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
       const uint32_t key = tkey[r];
       tkey[r] = 0u;
       const int64_t tile = blockIdx.x + k * G;
-      if (tile != a.withhold_tile) st_relaxed_gpu(a.tile_key + tile, key);
+      if (tile != a.withhold_tile && LM_IN_BOUNDS(tile, a.n_tiles, a.err)) st_relaxed_gpu(a.tile_key + tile, key);
       mbar_arrive(&aux.pub_bar[r]);
     }
     return;
@@ -578,7 +589,11 @@ __global__ void __launch_bounds__(threads_for(CW), 1) stft_logmel_kernel(const S
         if ((poll >> w) & 1u) {
           const int nvec = (head[w] + tpc + 3) >> 2;
           for (int v = lane; v < nvec; v += 32) {
-            const uint4 x = ld_relaxed_gpu_v4(base[w] + 4 * v);
+            // (checked builds) the 16-byte group lies inside the slots, the
+            // 16-byte header before them or the 16 bytes of slack after
+            const uint4 x = LM_IN_BOUNDS((base[w] + 4 * v) - a.tile_key + 4, a.n_tiles + 5, a.err)
+                                ? ld_relaxed_gpu_v4(base[w] + 4 * v)
+                                : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t e[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -773,16 +788,23 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) stft_logmel_cluster_kernel(c
           generic_written &= ~(1u << s);
         }
         if (lo < base) {
-          *reinterpret_cast<float2 *>(dst + (start - a0)) = *reinterpret_cast<const float2 *>(start);
+          if (LM_IN_BOUNDS(start - base, a.total_bytes - 7, a.err))
+            *reinterpret_cast<float2 *>(dst + (start - a0)) = *reinterpret_cast<const float2 *>(start);
           lo += 16;
           generic_written |= 1u << s;
         }
         if (hi > limit) {
-          *reinterpret_cast<float2 *>(dst + (end - 8 - a0)) = *reinterpret_cast<const float2 *>(end - 8);
+          if (LM_IN_BOUNDS(end - 8 - base, a.total_bytes - 7, a.err))
+            *reinterpret_cast<float2 *>(dst + (end - 8 - a0)) = *reinterpret_cast<const float2 *>(end - 8);
           hi = end & ~15ull;
           generic_written |= 1u << s;
         }
-        const uint32_t bytes = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+        uint32_t bytes = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+        // (checked builds) the copied range lies inside the tensor; if not,
+        // nothing is copied and the error word says so
+        if (bytes > 0 && !(LM_IN_BOUNDS(lo - base, a.total_bytes, a.err) &&
+                           LM_IN_BOUNDS(hi - 1 - base, a.total_bytes, a.err)))
+          bytes = 0;
         const int d = k & (kSlots - 1);
         aux.desc_nf[d] = nf;
         aux.desc_head[d] = static_cast<int32_t>(start - a0);
@@ -835,11 +857,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) stft_logmel_cluster_kernel(c
         v.y = rescale(v.y, floor_v);
         v.z = rescale(v.z, floor_v);
         v.w = rescale(v.w, floor_v);
-        __stcs(reinterpret_cast<float4 *>(o) + i, v);
+        if (LM_IN_BOUNDS((o - a.out) + 4 * i + 3, a.B * a.F * a.NM, a.err)) __stcs(reinterpret_cast<float4 *>(o) + i, v);
       }
-      for (int64_t i = 4 * n4 + threadIdx.x; i < n; i += nthreads) __stcs(o + i, rescale(obuf[i], floor_v));
+      for (int64_t i = 4 * n4 + threadIdx.x; i < n; i += nthreads)
+        if (LM_IN_BOUNDS((o - a.out) + i, a.B * a.F * a.NM, a.err)) __stcs(o + i, rescale(obuf[i], floor_v));
     } else {
-      for (int64_t i = threadIdx.x; i < n; i += nthreads) __stcs(o + i, rescale(obuf[i], floor_v));
+      for (int64_t i = threadIdx.x; i < n; i += nthreads)
+        if (LM_IN_BOUNDS((o - a.out) + i, a.B * a.F * a.NM, a.err)) __stcs(o + i, rescale(obuf[i], floor_v));
     }
   }
   cluster_sync_all();  // the peers have read this CTA's maximum

@@ -141,6 +141,7 @@ __device__ __forceinline__ int64_t map_index(int64_t s, int64_t T, int mode, boo
 }
 
 __device__ __forceinline__ float load_sample(const WaveArgs &a, int64_t b, int64_t s) {
+  if (!LM_IN_BOUNDS(b * a.T + s, a.B * a.T, a.err)) return 0.f;  // (checked builds)
   if (a.in_i16) return static_cast<float>(static_cast<const int16_t *>(a.wave)[b * a.T + s]) * (1.0f / 32768.0f);
   return static_cast<const float *>(a.wave)[b * a.T + s];
 }
@@ -283,9 +284,14 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     uint64_t a0;
     uint32_t bytes;
     if (span_of(tile, &a0, &bytes)) {
-      mbar_arrive_expect_tx(&seg_bar[buf], bytes);
-      bulk_g2s(seg + buf * static_cast<size_t>(a.seg_bytes), static_cast<const char *>(a.wave) + a0, bytes,
-               &seg_bar[buf], policy_evict_first());
+      // (checked builds) the span lies inside the waveform and fits its
+      // buffer; if not, nothing is copied and the error word says so
+      const bool ok = LM_IN_BOUNDS(a0, a.total_bytes, a.err) && LM_IN_BOUNDS(a0 + bytes - 1, a.total_bytes, a.err) &&
+                      LM_IN_BOUNDS(bytes - 1, a.seg_bytes, a.err);
+      mbar_arrive_expect_tx(&seg_bar[buf], ok ? bytes : 0u);
+      if (ok)
+        bulk_g2s(seg + buf * static_cast<size_t>(a.seg_bytes), static_cast<const char *>(a.wave) + a0, bytes,
+                 &seg_bar[buf], policy_evict_first());
       ++issued[buf];
     }
   };
@@ -563,11 +569,11 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
         asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(fmaxf(acc, 1e-10f)));
         const float v = l2 * 0.30102999566398120f;  // log10(x) = log2(x) log10(2)
         lmax = fmaxf(lmax, v);
-        static_cast<float *>(a.out)[o] = v;
+        if (LM_IN_BOUNDS(o, a.B * a.n_mels * a.n_frames, a.err)) static_cast<float *>(a.out)[o] = v;
       } else if (a.out_f16) {
-        static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
+        if (LM_IN_BOUNDS(o, a.B * a.n_mels * a.n_frames, a.err)) static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
       } else {
-        static_cast<float *>(a.out)[o] = acc;
+        if (LM_IN_BOUNDS(o, a.B * a.n_mels * a.n_frames, a.err)) static_cast<float *>(a.out)[o] = acc;
       }
     };
     if constexpr (TF == 1) {
@@ -624,7 +630,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       const uint32_t key = __reduce_max_sync(0xffffffffu, float_to_ordered(lmax));
       if ((threadIdx.x & 31) == 0) atomicMax(blk_key, key);
       __syncthreads();
-      if (threadIdx.x == 0) a.tile_key[tile] = *blk_key;
+      if (threadIdx.x == 0 && LM_IN_BOUNDS(tile, a.B * a.tiles_per_clip, a.err)) a.tile_key[tile] = *blk_key;
     }
   }
   drain(false);

@@ -338,6 +338,11 @@ template <int K, int STRIDE>
 __device__ __forceinline__ void load_frame(const WaveArgs &a, int64_t b, int64_t s0, int lane_off, bool wave_aligned,
                                            const float2 *win2, float2 *scratch, float2 (&u)[K]) {
   constexpr float kI16 = 1.0f / 32768.0f;
+  if (!LM_IN_BOUNDS(b, a.B, a.err)) {  // (checked builds) the clip exists
+#pragma unroll
+    for (int i = 0; i < K; ++i) u[i] = make_float2(0.f, 0.f);
+    return;
+  }
   const bool interior = s0 >= 0 && s0 + 2 * (STRIDE * (K - 1) + lane_off) + 1 < a.T;
   const bool paired = wave_aligned && (((b * a.T + s0) & 1) == 0);
   if (interior && a.in_i16) {
@@ -380,16 +385,17 @@ __device__ __forceinline__ void load_frame(const WaveArgs &a, int64_t b, int64_t
       const int16_t *w = static_cast<const int16_t *>(a.wave) + b * a.T;
 #pragma unroll
       for (int i = 0; i < K; ++i) {
-        const int j = base0 + 2 * STRIDE * i;
-        u[i] = make_float2(static_cast<float>(__ldg(w + fold(j))) * kI16,
-                           static_cast<float>(__ldg(w + fold(j + 1))) * kI16);
+        const int j0 = fold(base0 + 2 * STRIDE * i), j1 = fold(base0 + 2 * STRIDE * i + 1);
+        u[i] = make_float2(LM_IN_BOUNDS(j0, T, a.err) ? static_cast<float>(__ldg(w + j0)) * kI16 : 0.f,
+                           LM_IN_BOUNDS(j1, T, a.err) ? static_cast<float>(__ldg(w + j1)) * kI16 : 0.f);
       }
     } else {
       const float *w = static_cast<const float *>(a.wave) + b * a.T;
 #pragma unroll
       for (int i = 0; i < K; ++i) {
-        const int j = base0 + 2 * STRIDE * i;
-        u[i] = make_float2(__ldg(w + fold(j)), __ldg(w + fold(j + 1)));
+        const int j0 = fold(base0 + 2 * STRIDE * i), j1 = fold(base0 + 2 * STRIDE * i + 1);
+        u[i] = make_float2(LM_IN_BOUNDS(j0, T, a.err) ? __ldg(w + j0) : 0.f,
+                           LM_IN_BOUNDS(j1, T, a.err) ? __ldg(w + j1) : 0.f);
       }
     }
   } else {
@@ -403,8 +409,9 @@ __device__ __forceinline__ void load_frame(const WaveArgs &a, int64_t b, int64_t
 #pragma unroll
       for (int i = 0; i < K; ++i) {
         const int j0 = idx[2 * i], j1 = idx[2 * i + 1];
-        const float x0 = static_cast<float>(__ldg(w + (j0 < 0 ? 0 : j0))) * kI16;
-        const float x1 = static_cast<float>(__ldg(w + (j1 < 0 ? 0 : j1))) * kI16;
+        const int k0 = j0 < 0 ? 0 : j0, k1 = j1 < 0 ? 0 : j1;
+        const float x0 = LM_IN_BOUNDS(k0, a.T, a.err) ? static_cast<float>(__ldg(w + k0)) * kI16 : 0.f;
+        const float x1 = LM_IN_BOUNDS(k1, a.T, a.err) ? static_cast<float>(__ldg(w + k1)) * kI16 : 0.f;
         u[i] = make_float2(j0 < 0 ? 0.f : x0, j1 < 0 ? 0.f : x1);
       }
     } else {
@@ -412,8 +419,9 @@ __device__ __forceinline__ void load_frame(const WaveArgs &a, int64_t b, int64_t
 #pragma unroll
       for (int i = 0; i < K; ++i) {
         const int j0 = idx[2 * i], j1 = idx[2 * i + 1];
-        const float x0 = __ldg(w + (j0 < 0 ? 0 : j0));
-        const float x1 = __ldg(w + (j1 < 0 ? 0 : j1));
+        const int k0 = j0 < 0 ? 0 : j0, k1 = j1 < 0 ? 0 : j1;
+        const float x0 = LM_IN_BOUNDS(k0, a.T, a.err) ? __ldg(w + k0) : 0.f;
+        const float x1 = LM_IN_BOUNDS(k1, a.T, a.err) ? __ldg(w + k1) : 0.f;
         u[i] = make_float2(j0 < 0 ? 0.f : x0, j1 < 0 ? 0.f : x1);
       }
     }
@@ -728,11 +736,12 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
             asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(fmaxf(acc, 1e-10f)));
             const float v = l2 * 0.30102999566398120f;  // log10(x) = log2(x) log10(2)
             lmax = fmaxf(lmax, v);
-            static_cast<float *>(a.out)[o] = v;
+            if (LM_IN_BOUNDS(o, a.B * a.n_mels * a.n_frames, a.err)) static_cast<float *>(a.out)[o] = v;
           } else if (a.out_f16) {
-            static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
+            if (LM_IN_BOUNDS(o, a.B * a.n_mels * a.n_frames, a.err))
+              static_cast<__half *>(a.out)[o] = __float2half_rn(acc);
           } else {
-            static_cast<float *>(a.out)[o] = acc;
+            if (LM_IN_BOUNDS(o, a.B * a.n_mels * a.n_frames, a.err)) static_cast<float *>(a.out)[o] = acc;
           }
         }
       }
@@ -747,10 +756,12 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
       if (fused) {
         // Fold the tile maximum into its clip's, then count the tile in with
         // release order: a CTA that sees the count complete sees the maximum.
-        atomicMax(a.clip_key + b, *blk_key);
-        red_add_release_gpu(a.clip_done + b, 1u);
+        if (LM_IN_BOUNDS(b, a.B, a.err)) {
+          atomicMax(a.clip_key + b, *blk_key);
+          red_add_release_gpu(a.clip_done + b, 1u);
+        }
       } else {
-        a.tile_key[tile] = *blk_key;
+        if (LM_IN_BOUNDS(tile, a.B * a.tiles_per_clip, a.err)) a.tile_key[tile] = *blk_key;
       }
       *blk_key = 0u;
     }
@@ -815,12 +826,17 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int m = m0 + u * NG;
-            v[u] = m < a.n_mels ? o[static_cast<int64_t>(m) * a.n_frames] : 0.f;
+            v[u] = (m < a.n_mels && LM_IN_BOUNDS((o - static_cast<float *>(a.out)) + static_cast<int64_t>(m) * a.n_frames,
+                                                 a.B * a.n_mels * a.n_frames, a.err))
+                       ? o[static_cast<int64_t>(m) * a.n_frames]
+                       : 0.f;
           }
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int m = m0 + u * NG;
-            if (m < a.n_mels) o[static_cast<int64_t>(m) * a.n_frames] = rescale_log(v[u], floor_v);
+            if (m < a.n_mels && LM_IN_BOUNDS((o - static_cast<float *>(a.out)) + static_cast<int64_t>(m) * a.n_frames,
+                                             a.B * a.n_mels * a.n_frames, a.err))
+              o[static_cast<int64_t>(m) * a.n_frames] = rescale_log(v[u], floor_v);
           }
         }
       }
