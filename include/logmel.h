@@ -139,8 +139,10 @@ lm_status lm_log_mel_from_stft(const void *stft, const float *mel_filters, float
  *                  how many tiles each thread holds back before writing.
  *   smem_bytes     dynamic shared memory per CTA.
  * LOGMEL_K1_VARIANT=resident|twopass|cluster forces a variant, and
- * =nocluster leaves the cluster variant out (A/B); a forced variant that
- * cannot run returns LM_ERR_UNSUPPORTED. */
+ * =nocluster leaves the cluster variant out (A/B), and LOGMEL_FPB=1|2|4|6|8
+ * forces the frames each consumer thread takes per tile (the workspace size
+ * follows it); a forced variant or tile that cannot run returns
+ * LM_ERR_UNSUPPORTED. */
 typedef struct lm_stft_launch_info {
   int32_t resident;
   int32_t kernels;

@@ -1024,6 +1024,14 @@ void tile_height(int NF, int NM, int *CW, int *FG, int *FPT) {
   const int fg_max = (*CW * 32) / NM;
   const int64_t frame_bytes = static_cast<int64_t>(NF) * 8;
   *FG = fg_max;
+  // LOGMEL_FPB=1|2|4|6|8 forces the frames per consumer thread (sixteen
+  // consumer warps; A/B only): the workspace size follows it, and a stage
+  // that leaves no room for two of them in shared memory is refused later.
+  const int forced = std::atoi(env_or("LOGMEL_FPB", "0"));
+  if (fg_max >= 1 && (forced == 1 || forced == 2 || forced == 4 || forced == 6 || forced == 8)) {
+    *FPT = forced;
+    return;
+  }
   *FPT = 0;
   for (int fpt : {8, 6, 4, 2, 1}) {
     if (static_cast<int64_t>(fg_max) * fpt * frame_bytes <= kStageTargetBytes) {

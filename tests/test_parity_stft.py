@@ -297,3 +297,15 @@ def test_floor_rewrites_in_every_variant(lm, oracle_mod, variant, monkeypatch):
     _compare(got, ref)
     for b in range(B):
         assert np.isclose(got[b].min(), got[b].max() - 2.0, atol=1e-5)
+
+
+@pytest.mark.parametrize("fpb", ["1", "2", "4", "8"])
+def test_frames_per_thread_override(lm, oracle_mod, fpb, monkeypatch):
+    """LOGMEL_FPB (A/B only) forces the tile height; the launch plan reports
+    it and every clip still matches the oracle."""
+    monkeypatch.setenv("LOGMEL_FPB", fpb)
+    shape = (5, 777, 201, 80)
+    info = lm.describe_log_mel_from_stft(*shape)
+    assert info["frames_per_tile"] == (16 * 32 // 80) * int(fpb)
+    stft, W = workloads.stft_inputs(*shape, seed=300 + int(fpb))
+    _compare(*_run(lm, oracle_mod, stft, W))
