@@ -216,18 +216,18 @@ struct Cfg;
 
 // The sizes whose stage 2 gives each column one lane: M = N1 x N2, stage 1
 // with N2 threads per frame (an N1-point DFT each), stage 2 with N1 lanes per
-// frame (an N2-point DFT each), 32-frame tiles of 4 frames per warp.  Rows of
-// stage-1 output hold N1 values at a stride of ROW (odd where that spreads a
-// column over the banks).
-template <int NFFT_, int N1_, int N2_, int ROW_, int MINB_>
+// frame (an N2-point DFT each), tiles of TF frames (a multiple of 32), TF / 8
+// frames per warp.  Rows of stage-1 output hold N1 values at a stride of ROW
+// (odd where that spreads a column over the banks).
+template <int NFFT_, int N1_, int N2_, int ROW_, int MINB_, int TF_ = 32>
 struct ColCfg {
   static constexpr int M = NFFT_ / 2;
   static constexpr int N1 = N1_;     // stage-1 DFT size; stage-2 lanes per frame
   static constexpr int N2 = N2_;     // stage-1 threads per frame; stage-2 DFT size
   static constexpr int ROW = ROW_;   // complex values per stage-1 row (N1 used)
-  static constexpr int TF = 32;      // frames per tile
+  static constexpr int TF = TF_;     // frames per tile
   static constexpr int NT = 256;
-  static constexpr int FPW = TF / (NT / 32);  // frames per warp: 4
+  static constexpr int FPW = TF / (NT / 32);  // frames per warp
   static constexpr int REGION = 2 * N2 * ROW;  // floats per frame region
   static constexpr int LANES2 = N1;  // table rows: one per column
   static constexpr int R2 = N2;      // twiddles per column
@@ -235,12 +235,17 @@ struct ColCfg {
   static constexpr int kMinBlocks = MINB_;
   // A power row (M + 1 floats at an offset of up to 15) and the mel
   // projection's reads up to 3 floats past it stay inside the frame's region.
-  static_assert(M == N1 * N2 && N1 <= 32 && 15 + M + 1 + 3 <= REGION, "column layout");
+  static_assert(M == N1 * N2 && N1 <= 32 && 15 + M + 1 + 3 <= REGION && TF % 32 == 0, "column layout");
 };
+// 64-frame tiles at 64 and 128 points: stage 1's N2 threads per frame then
+// fill whole warps, and the per-tile work spreads over twice the frames (32
+// clips x 160000 samples, hop n_fft / 4, 128 bands: 64 points 96.3 -> 84.0
+// us, 128 points 57.3 -> 51.2; 128-frame tiles at 64 points 91.1, 64-frame
+// tiles at 256 points 49.2 against 45.1, with two CTAs per SM).
 template <>
-struct Cfg<64> : ColCfg<64, 8, 4, 9, 4> {};
+struct Cfg<64> : ColCfg<64, 8, 4, 9, 4, 64> {};
 template <>
-struct Cfg<128> : ColCfg<128, 8, 8, 9, 4> {};
+struct Cfg<128> : ColCfg<128, 8, 8, 9, 4, 64> {};
 template <>
 struct Cfg<256> : ColCfg<256, 16, 8, 17, 4> {};
 template <>
@@ -494,7 +499,8 @@ __device__ __forceinline__ void stage2_cols(float *regions, int f0, int nf, int 
   __syncwarp();  // every lane has read the regions before power rows overwrite them
   if (act) {
     const float2 *tu = twu + c * C::TWROW;
-    float *pw = regions + f * C::REGION + (f >> 1);
+    // the power row's offset inside the region: as the mel projection's prow
+    float *pw = regions + f * C::REGION + ((f >> 1) & 15);
 #pragma unroll
     for (int d = 0; d < N2 / 2; ++d) {
       const float2 B = c == 0 ? v[(N2 - d) % N2] : (middle ? v[N2 - 1 - d] : r[d]);
@@ -626,7 +632,7 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
     // Frame f's power row sits inside its own region, at float offset
     // f * REGION + shift(f): lanes over the frames of one bin then hit
     // distinct banks in the mel projection.
-    auto prow = [&](int f) { return regions + f * REGION + (NFFT == 1024 ? f : (f >> 1)); };
+    auto prow = [&](int f) { return regions + f * REGION + (NFFT == 1024 ? f : ((f >> 1) & 15)); };
     if constexpr (NFFT != 1024) {
 #pragma unroll 1
       for (int q = 0; q < C::FPW; q += 32 / C::N1) {
@@ -697,13 +703,14 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
     __syncthreads();  // every power row of the tile is complete
 
     // ---------------- mel projection and store ----------------
-    // Lanes run over frames (TF = 32: a warp per band; TF = 16: a half-warp
-    // per band), band groups over the rest.
+    // Lanes run over frames (32 at a time: a warp per band; TF = 16: a
+    // half-warp per band), band groups over the rest.
     float lmax = -INFINITY;
-    {
-      constexpr int LF = TF < 32 ? TF : 32;      // lanes per band
-      constexpr int NG = NT / LF;                // band groups
-      const int f = static_cast<int>(threadIdx.x) % LF;
+    constexpr int LF = TF < 32 ? TF : 32;  // lanes per band
+#pragma unroll 1
+    for (int fb = 0; fb < TF; fb += LF) {
+      constexpr int NG = NT / LF;  // band groups
+      const int f = fb + static_cast<int>(threadIdx.x) % LF;
       const int g = static_cast<int>(threadIdx.x) / LF;
       if (f < nf) {
         // The first four taps of every band are read unconditionally: filter
@@ -813,7 +820,9 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
       const int nf = left < a.TF ? static_cast<int>(left) : a.TF;
       constexpr int LF = TF < 32 ? TF : 32;
       constexpr int NG = NT / LF;
-      const int f = static_cast<int>(threadIdx.x) % LF;
+#pragma unroll 1
+      for (int fb = 0; fb < TF; fb += LF) {
+      const int f = fb + static_cast<int>(threadIdx.x) % LF;
       if (f < nf) {
         // Up to U bands per thread and pass, every load before any store, so
         // the L2 round trips overlap (in place, one at a time they would
@@ -839,6 +848,7 @@ __global__ void __launch_bounds__(Cfg<NFFT>::NT, Cfg<NFFT>::kMinBlocks) wave_reg
               o[static_cast<int64_t>(m) * a.n_frames] = rescale_log(v[u], floor_v);
           }
         }
+      }
       }
       __syncthreads();  // resc_s and floor_s are rewritten for the next tile
     }
