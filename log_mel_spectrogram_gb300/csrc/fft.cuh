@@ -230,11 +230,26 @@ __device__ __forceinline__ int dit_pos(int n) {
 
 // One in-place pass over one frame of M points (at LayoutIP<M> positions) by
 // NT threads; the twiddle rows are read through L1 from global memory.
+// When a thread's factors for the whole pass take at most 16 float2, it
+// loads all of them before its first butterfly, so their L2 round trips
+// overlap instead of following one another butterfly by butterfly.
 template <int M, int R, int P, int NT>
 __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict__ W) {
   constexpr int ITEMS = M / R;
+  constexpr int ROUNDS = (ITEMS + NT - 1) / NT;
+  constexpr bool kAhead = P > 1 && ITEMS % NT == 0 && ROUNDS * (R - 1) <= 16;
+  float2 tw[kAhead ? ROUNDS : 1][R];
+  if constexpr (kAhead) {
 #pragma unroll
-  for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
+    for (int r = 0; r < ROUNDS; ++r) {
+      const int t = static_cast<int>(threadIdx.x) + r * NT;
+      const float2 *row = W + rows_offset<M, P>() + (t % P) * row_stride<R>();
+#pragma unroll
+      for (int j = 1; j < R; ++j) tw[r][j] = __ldg(row + j - 1);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
     const int t = static_cast<int>(threadIdx.x) + r * NT;
     if (ITEMS % NT != 0 && t >= ITEMS) break;
     const int k = t % P;
@@ -242,7 +257,10 @@ __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict
     float2 u[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) u[j] = x[LayoutIP<M>::at(base + j * P)];
-    if constexpr (P > 1) {
+    if constexpr (kAhead) {
+#pragma unroll
+      for (int j = 1; j < R; ++j) u[j] = cmul(u[j], tw[r][j]);
+    } else if constexpr (P > 1) {
       const float2 *row = W + rows_offset<M, P>() + k * row_stride<R>();
 #pragma unroll
       for (int j = 1; j < R; ++j) u[j] = cmul(u[j], __ldg(row + j - 1));

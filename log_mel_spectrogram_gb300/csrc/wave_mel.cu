@@ -58,6 +58,8 @@ struct lm_mel_plan {
   uint32_t tables_bytes;  // its size, a multiple of 16
   unsigned char *reg_tables;  // n_fft 64...1024: the register kernels' image (reg::Tables)
   uint32_t reg_tables_bytes;
+  unsigned char *mel_image;   // n_fft 8192, 16384: the filterbank image (mel_image_bytes_for), or null
+  uint32_t mel_image_bytes;
 };
 
 namespace lm {
@@ -101,6 +103,8 @@ struct WaveArgs {
   const float *fw;
   const unsigned char *tables;  // shared-memory image of the tables (n_fft <= 4096)
   uint32_t tables_bytes;
+  const unsigned char *mel_image;  // in place: the filterbank image copied into the transform's buffer, or null
+  uint32_t mel_image_bytes;
 };
 
 // Launch token (CTA 0, thread 0): clears the error word (when it is this
@@ -231,6 +235,57 @@ size_t wave_smem_bytes(int n_mels, int wmax) {
   return (b + 127) / 128 * 128;  // the sample-span buffers follow, 128-byte aligned
 }
 
+// The in-place transform's filterbank image, copied into the transform's
+// buffer once the power row is complete: n_mels + 1 int2 {first bin of band
+// m, offset of its weights} (the last holds only the total, so band m's
+// width is the difference of two offsets), then every band's weights back
+// to back.  Zero (the projection then reads the plan's global tables) when
+// it does not fit the buffer: 128 bands fit at both sizes.
+inline uint32_t mel_image_bytes_for(int n_fft, int n_mels, const std::vector<int> &fwidth) {
+  size_t taps = 0;
+  for (int m = 0; m < n_mels; ++m) taps += static_cast<size_t>(fwidth[m]);
+  const size_t bytes = (8 * (static_cast<size_t>(n_mels) + 1) + 4 * taps + 15) / 16 * 16;
+  size_t room = 0;
+  if (n_fft == 8192) room = sizeof(float2) * WaveCfg<8192>::BUF;
+  if (n_fft == 16384) room = sizeof(float2) * WaveCfg<16384>::BUF;
+  return bytes <= room ? static_cast<uint32_t>(bytes) : 0u;
+}
+
+// A sample pair as a complex point: f32 pairs as they are, int16 pairs (one
+// 32-bit word) scaled by 1/32768.
+__device__ __forceinline__ float2 pair_point(float2 v) { return v; }
+__device__ __forceinline__ float2 pair_point(int v) {
+  return make_float2(static_cast<float>(static_cast<int16_t>(v & 0xffff)) * (1.0f / 32768.0f),
+                     static_cast<float>(static_cast<int16_t>(v >> 16)) * (1.0f / 32768.0f));
+}
+
+// Framing of an interior frame for the in-place transform, its sample pairs
+// aligned: each thread loads PB sample pairs and their window pairs at a
+// time, all in flight together, and stores each windowed point n at its
+// digit-reversed position.  src points at the frame's first sample pair.
+template <int M, int NT, typename Pair>
+__device__ __forceinline__ void frame_in_place(const Pair *src, const float2 *win2, float2 *buf) {
+  constexpr int PER = M / NT, PB = 8;
+  static_assert(M % NT == 0 && PER % PB == 0, "points per thread");
+#pragma unroll 1
+  for (int c = 0; c < PER; c += PB) {
+    Pair x[PB];
+    float2 w[PB];
+#pragma unroll
+    for (int j = 0; j < PB; ++j) {
+      const int n = static_cast<int>(threadIdx.x) + (c + j) * NT;
+      x[j] = __ldg(src + n);
+      w[j] = __ldg(win2 + n);
+    }
+#pragma unroll
+    for (int j = 0; j < PB; ++j) {
+      const int n = static_cast<int>(threadIdx.x) + (c + j) * NT;
+      const float2 v = pair_point(x[j]);
+      buf[fft::LayoutIP<M>::at(fft::dit_pos<M>(n))] = make_float2(v.x * w[j].x, v.y * w[j].y);
+    }
+  }
+}
+
 template <int NFFT>
 __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) wave_mel_kernel(const WaveArgs a) {
   using C = WaveCfg<NFFT>;
@@ -339,12 +394,14 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
 
   // Tiles are handed out dynamically: a CTA's first tile is its index, each
   // later one comes from a counter in the workspace header (zeroed per
-  // call), claimed at the start of the tile before it so its samples can be
-  // prefetched.  (Claiming two ahead measured slower: the last tiles go to
-  // CTAs that are not yet free.)
+  // call), claimed at the start of the tile before it; once that tile's
+  // framing is done, the claimed tile's samples are prefetched.  (Claiming
+  // two ahead measured slower: the last tiles go to CTAs that are not yet
+  // free.)
   const int64_t n_tiles = a.B * a.tiles_per_clip;
   volatile int *next_s = reinterpret_cast<volatile int *>(blk_key + 2);  // n_tiles < 2^31 (host check)
   int it = 0;
+  uint32_t mel_phase = 0u;  // filterbank image copies completed (in place)
   bool token_seen = a.token == 0;  // thread 0
   for (int64_t tile = blockIdx.x, nxt; tile < n_tiles; tile = nxt, ++it) {
     const int buf = it & 1;
@@ -353,18 +410,17 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     const int64_t t0 = static_cast<int64_t>(tloc) * TF;
     const int64_t left = a.n_frames - t0;
     const int nf = left < TF ? static_cast<int>(left) : TF;
+    // Thread 0 claims the next tile now and uses the answer only after this
+    // tile's framing, so the counter's round trip overlaps the framing.
+    int claimed = 0;
     if (threadIdx.x == 0) {
       *blk_key = 0u;
-      *next_s = claim_tile(a, &token_seen, abort_flag_p, static_cast<int>(n_tiles));
+      claimed = claim_tile(a, &token_seen, abort_flag_p, static_cast<int>(n_tiles));
     }
     // Tables loaded / previous tile finished with every buffer.  A wait that
     // gave up in the previous tile (its values are then wrong, but every
     // index stayed in bounds) ends the loop in every thread together.
     if (__syncthreads_or(*abort_flag != 0)) break;
-    nxt = *next_s;
-    // Prefetch the next tile's samples into the other span buffer; the
-    // previous tile's framing, its last reader, finished before the barrier.
-    if (threadIdx.x == 0 && nxt < n_tiles) issue_span(nxt, buf ^ 1);
     uint64_t span_a0;
     uint32_t span_bytes;
     const bool staged = span_of(tile, &span_a0, &span_bytes);
@@ -388,6 +444,19 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     // Power-of-two sizes fuse the framing into the first FFT pass; at 400
     // points the fused radix-5 pass measured slower than framing on its own.
     const bool fused = paired && C::kFuseFirst;
+    bool gathered = false;  // in place: the frame is already in the buffer
+    if constexpr (C::kInPlace) {
+      const int64_t p0 = b * a.T + s_first;  // the frame's first sample
+      if (interior && ((reinterpret_cast<uintptr_t>(a.wave) & (a.in_i16 ? 3u : 7u)) == 0) && (p0 & 1) == 0 &&
+          LM_IN_BOUNDS(p0 + NFFT - 1, a.B * a.T, a.err)) {
+        const float2 *win2 = reinterpret_cast<const float2 *>(win);
+        if (a.in_i16)
+          frame_in_place<M, NT>(reinterpret_cast<const int *>(static_cast<const int16_t *>(a.wave) + p0), win2, bufA);
+        else
+          frame_in_place<M, NT>(reinterpret_cast<const float2 *>(static_cast<const float *>(a.wave) + p0), win2, bufA);
+        gathered = true;
+      }
+    }
     if (paired && !fused) {
       // 32-bit shared addresses; thread idx handles point n of frame f.
       constexpr int ITEMS = TF * M;
@@ -474,7 +543,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
           sts_f32x2(dst0 + 8u * static_cast<uint32_t>(C::L::at(f * M + i * R0 + l)), u[l]);
       }
     }
-    for (int idx = paired ? TF * M : static_cast<int>(threadIdx.x); idx < TF * M; idx += blockDim.x) {
+    for (int idx = (paired || gathered) ? TF * M : static_cast<int>(threadIdx.x); idx < TF * M; idx += blockDim.x) {
       const int f = idx / M;
       const int n = idx - f * M;
       float2 z = make_float2(0.f, 0.f);
@@ -509,6 +578,13 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       bufA[C::L::at(C::kInPlace ? fft::dit_pos<M>(n) : idx)] = z;
     }
     __syncthreads();
+    // Publish the next tile (read after the untangle's barrier) and prefetch
+    // its samples into the other span buffer, whose last reader, the previous
+    // tile's framing, finished two barriers ago.
+    if (threadIdx.x == 0) {
+      *next_s = claimed;
+      if (claimed < n_tiles) issue_span(claimed, buf ^ 1);
+    }
 
     // 2. N/2-point complex FFT of every frame (its first pass already done
     // for aligned staged tiles, whose result is then in bufB)
@@ -535,10 +611,8 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     {
       constexpr int KP = M / 2 + 1;  // pairs per frame (M is even)
       constexpr int ITEMS = TF * KP;
-#pragma unroll 2
-      for (int r = 0; r < (ITEMS + NT - 1) / NT; ++r) {
-        const int idx = static_cast<int>(threadIdx.x) + r * NT;
-        if (ITEMS % NT != 0 && idx >= ITEMS) break;
+      constexpr int ROUNDS = (ITEMS + NT - 1) / NT;
+      auto untangle = [&](int idx, float2 tw) {
         const int f = idx / KP;
         const int k = idx - f * KP;
         const float2 A = Z[C::L::at(f * M + k)];
@@ -546,7 +620,7 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
         const float2 E = make_float2(0.5f * (A.x + Bz.x), 0.5f * (A.y - Bz.y));
         // O = (A - conj B) / (2i) = -i (A - conj B) / 2
         const float2 O = make_float2(0.5f * (A.y + Bz.y), -0.5f * (A.x - Bz.x));
-        const float2 TO = fft::cmul(twn[k], O);
+        const float2 TO = fft::cmul(tw, O);
         float p0 = fmaf(E.x + TO.x, E.x + TO.x, (E.y + TO.y) * (E.y + TO.y));
         float p1 = fmaf(E.x - TO.x, E.x - TO.x, (E.y - TO.y) * (E.y - TO.y));
         if (a.power_is_one) {
@@ -555,9 +629,33 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
         }
         pw[f * NFP + k] = p0;
         if (k != M / 2) pw[f * NFP + M - k] = p1;
+      };
+      if constexpr (C::kInPlace) {
+        // One frame (TF = 1, so idx = k); the twiddles come from global
+        // memory, all of this thread's in flight at once.
+        float2 tw[ROUNDS];
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+          const int idx = static_cast<int>(threadIdx.x) + r * NT;
+          tw[r] = (ITEMS % NT == 0 || idx < ITEMS) ? __ldg(twn + idx) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+          const int idx = static_cast<int>(threadIdx.x) + r * NT;
+          if (ITEMS % NT != 0 && idx >= ITEMS) break;
+          untangle(idx, tw[r]);
+        }
+      } else {
+#pragma unroll 2
+        for (int r = 0; r < ROUNDS; ++r) {
+          const int idx = static_cast<int>(threadIdx.x) + r * NT;
+          if (ITEMS % NT != 0 && idx >= ITEMS) break;
+          untangle(idx, twn[idx - (idx / KP) * KP]);
+        }
       }
     }
     __syncthreads();
+    nxt = *next_s;
 
     // 4. mel projection and store
     float lmax = -INFINITY;
@@ -580,14 +678,77 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
       // One frame, filters hundreds of bins wide: a warp per band, lanes
       // over taps, then a shuffle reduction.
       const int lane = threadIdx.x & 31;
-      for (int m = threadIdx.x >> 5; m < a.n_mels; m += NT / 32) {
-        const int st = fstart[m], wd = fwidth[m];
-        const float *w = fw + m * a.wmax;
-        float acc = 0.f;
-        for (int t = lane; t < wd; t += 32) acc = fmaf(w[t], pw[st + t], acc);
+      bool from_smem = false, skip = false;
+      if constexpr (C::kInPlace) {
+        if (a.mel_image != nullptr) {
+          // The transform's buffer is free once the power row is complete:
+          // the plan's filterbank image goes there in one bulk copy, and the
+          // projection then reads shared memory only (from global memory
+          // every band paid dependent L2 round trips for its support and
+          // its weights).
+          if (threadIdx.x == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&seg_bar[0], a.mel_image_bytes);
+            bulk_g2s_plain(bufA, a.mel_image, a.mel_image_bytes, &seg_bar[0]);
+            ++issued[0];
+          }
+          const bool ok = mbar_wait(&seg_bar[0], mel_phase & 1u, abort_flag, a.err);
+          ++mel_phase;
+          // a wait that gave up leaves this tile's output unwritten (the
+          // abort flag ends the loop at the next barrier)
+          from_smem = __all_sync(0xffffffffu, ok);
+          skip = !from_smem;
+        }
+      }
+      if (skip) {
+      } else if (from_smem) {
+        // G bands of the warp at a time (m, m + NW, ...): their tap loops and
+        // shuffle reductions are independent chains, interleaved.  Each
+        // band's sum is formed in the same order as one band at a time.
+        constexpr int G = 4, NW = NT / 32;
+        const uint32_t hdr = smem_u32(bufA);
+        const uint32_t wts = hdr + 8u * static_cast<uint32_t>(a.n_mels + 1);
+        const uint32_t pw0 = smem_u32(pw);
+        for (int m0 = threadIdx.x >> 5; m0 < a.n_mels; m0 += G * NW) {
+          uint32_t wa[G], pa[G];
+          int wd[G], wmx = 0;
+          float acc[G];
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
-        if (lane == 0) emit(m, 0, acc);
+          for (int g = 0; g < G; ++g) {
+            const int m = m0 + g * NW;
+            const int2 h = m < a.n_mels ? lds_s32x2(hdr + 8u * m) : make_int2(0, 0);  // {first bin, offset}
+            wd[g] = m < a.n_mels ? lds_s32(hdr + 8u * (m + 1) + 4u) - h.y : 0;
+            wa[g] = wts + 4u * static_cast<uint32_t>(h.y);
+            pa[g] = pw0 + 4u * static_cast<uint32_t>(h.x);
+            acc[g] = 0.f;
+            wmx = max(wmx, wd[g]);
+          }
+          for (int t = lane; t < wmx; t += 32) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              if (t < wd[g]) acc[g] = fmaf(lds_f32(wa[g] + 4u * t), lds_f32(pa[g] + 4u * t), acc[g]);
+          }
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], d);
+          }
+          if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              if (m0 + g * NW < a.n_mels) emit(m0 + g * NW, 0, acc[g]);
+          }
+        }
+      } else {
+        for (int m = threadIdx.x >> 5; m < a.n_mels; m += NT / 32) {
+          const int st = fstart[m], wd = fwidth[m];
+          const float *w = fw + m * a.wmax;
+          float acc = 0.f;
+          for (int t = lane; t < wd; t += 32) acc = fmaf(w[t], pw[st + t], acc);
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+          if (lane == 0) emit(m, 0, acc);
+        }
       }
     } else {
       // Thread = (frame f, band group): lanes run over the TF frames of one
@@ -818,7 +979,8 @@ void free_plan(lm_mel_plan *pl) {
   if (!pl) return;
   for (void *ptr : {static_cast<void *>(pl->window), static_cast<void *>(pl->tw_m), static_cast<void *>(pl->tw_n),
                     static_cast<void *>(pl->fstart), static_cast<void *>(pl->fwidth), static_cast<void *>(pl->fw),
-                    static_cast<void *>(pl->tables), static_cast<void *>(pl->reg_tables)})
+                    static_cast<void *>(pl->tables), static_cast<void *>(pl->reg_tables),
+                    static_cast<void *>(pl->mel_image)})
     if (ptr) cudaFree(ptr);
   delete pl;
 }
@@ -955,6 +1117,24 @@ extern "C" lm_status lm_mel_plan_create(const lm_mel_params *params, lm_mel_plan
     if (!img.empty()) {
       pl->reg_tables_bytes = static_cast<uint32_t>(img.size());
       st = lm::upload(img, &pl->reg_tables, &n_alloc);
+    }
+  }
+  if (st == LM_OK && lm::in_place_nfft(params->n_fft)) {
+    // the filterbank image the in-place kernel copies into its buffer
+    pl->mel_image_bytes = lm::mel_image_bytes_for(params->n_fft, params->n_mels, t.fwidth);
+    if (pl->mel_image_bytes > 0) {
+      std::vector<unsigned char> img(pl->mel_image_bytes, 0);
+      const size_t w0 = 8 * (static_cast<size_t>(params->n_mels) + 1);
+      int off = 0;
+      for (int m = 0; m <= params->n_mels; ++m) {
+        const int h[2] = {m < params->n_mels ? t.fstart[m] : 0, off};
+        std::memcpy(img.data() + 8 * static_cast<size_t>(m), h, sizeof(h));
+        if (m == params->n_mels) break;
+        std::memcpy(img.data() + w0 + 4 * static_cast<size_t>(off), t.fw.data() + static_cast<size_t>(m) * t.wmax,
+                    4 * static_cast<size_t>(t.fwidth[m]));
+        off += t.fwidth[m];
+      }
+      st = lm::upload(img, &pl->mel_image, &n_alloc);
     }
   }
   if (st == LM_OK) {
@@ -1111,6 +1291,8 @@ lm_status lm::mel_spectrogram_run(const lm_mel_plan *plan, const void *wave, int
   a.fw = plan->fw;
   a.tables = use_reg ? plan->reg_tables : plan->tables;
   a.tables_bytes = use_reg ? plan->reg_tables_bytes : plan->tables_bytes;
+  a.mel_image = plan->mel_image;
+  a.mel_image_bytes = plan->mel_image_bytes;
   a.err = err_word ? err_word : static_cast<uint32_t *>(workspace);
   a.next_tile = static_cast<uint32_t *>(workspace) + 1;
   a.total_bytes = static_cast<uint64_t>(B) * static_cast<uint64_t>(T) * esize;

@@ -84,13 +84,15 @@ def test_withheld_tile_times_out_and_reports(lm, oracle_mod, shape, tile, monkey
     assert _close(out2.cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("k", [1, 3, 7])
-def test_forced_plan_allocation_failure_frees_what_was_allocated(lm, monkeypatch, k):
+@pytest.mark.parametrize("n_fft,k", [(400, 1), (400, 3), (400, 7), (16384, 7)])
+def test_forced_plan_allocation_failure_frees_what_was_allocated(lm, monkeypatch, n_fft, k):
     # LOGMEL_FAULT=plan_alloc:k fails the k-th device allocation of a plan:
     # the call reports LM_ERR_OUT_OF_MEMORY and frees the k - 1 before it.
+    # (At 400 points the 7th is the shared-memory table image; at 16384 it
+    # is the filterbank image of the in-place kernel.)
     from log_mel_spectrogram_gb300 import _native
-    p = _native.MelParams(sample_rate=16000, n_fft=400, hop_length=160, n_mels=128, f_max=8000.0, center=1,
-                          power=2.0)
+    p = _native.MelParams(sample_rate=16000, n_fft=n_fft, hop_length=n_fft // 4, n_mels=128, f_max=8000.0,
+                          center=1, power=2.0)
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     monkeypatch.setenv("LOGMEL_FAULT", f"plan_alloc:{k}")

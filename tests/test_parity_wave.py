@@ -72,10 +72,13 @@ def test_power_of_two_sizes(lm, oracle_mod, n_fft):
 
 @pytest.mark.parametrize("n_fft", [8192, 16384])
 def test_large_fft_sizes(lm, oracle_mod, n_fft):
-    # Past 4096 points the window, untangle twiddles and filterbank are read
-    # from global memory, one frame per tile, a warp per mel band.  8192 still
-    # stages aligned sample spans; 16384 always gathers.  Seven frames a clip
-    # keep the oracle's direct DFT to a few seconds.
+    # Past 4096 points the transform runs in place, one frame per tile: the
+    # window and untangle twiddles are read from global memory, interior
+    # frames load aligned sample pairs directly (clip 1 of an odd T starts
+    # unaligned and gathers), and the filterbank image is copied into the
+    # transform's buffer for the projection where it fits (128 and 80 bands;
+    # 256 bands at 8192 points do not fit and read the global tables).  Seven
+    # frames a clip keep the oracle's direct DFT to a few seconds.
     T = 3 * n_fft + 77
     x = workloads.wave_sines(2, T, 22050, seed=n_fft)
     _run(lm, oracle_mod, x, 22050, n_fft, n_fft // 2, 128, f_max=11025.0, mel_scale="slaney", norm="slaney")
