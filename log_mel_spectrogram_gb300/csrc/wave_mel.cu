@@ -25,7 +25,10 @@
 //     straight into a power tile |X[k]|^power (odd row stride);
 //  4. the banded mel projection, one output per thread, lanes over frames so
 //     each band's row of the output [B, n_mels, n_frames] is written as a run
-//     of consecutive frames; f32 or f16 (round to nearest even) at the store;
+//     of consecutive frames (one-frame tiles above 4096 points: a warp per
+//     band, lanes over its taps, the weights copied into the transform's
+//     buffer once the power row is complete); f32 or f16 (round to nearest
+//     even) at the store;
 //  5. log plans store log10(max(mel, 1e-10)) and publish each tile's maximum
 //     into a per-tile slot; a second kernel (the clamp epilogue shared with
 //     the STFT path) turns slots into clip maxima and rescales in place.
