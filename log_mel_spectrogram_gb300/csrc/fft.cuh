@@ -120,6 +120,43 @@ struct Dft<5> {
   }
 };
 
+template <>
+struct Dft<16> {
+  // 16 = 4 x 4: inputs j = 4a + b, outputs l = c + 4d.  Four 4-point DFTs
+  // over a, the factors exp(-2 pi i b c / 16), four 4-point DFTs over b.
+  __device__ __forceinline__ static void run(float2 (&u)[16]) {
+    constexpr float c1 = 0.92387953251128674f;  // cos(pi / 8)
+    constexpr float s1 = 0.38268343236508977f;  // sin(pi / 8)
+    constexpr float h = 0.70710678118654752f;   // sqrt(1/2)
+    float2 v[4][4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float2 t[4] = {u[b], u[4 + b], u[8 + b], u[12 + b]};
+      Dft<4>::run(t);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[b][c] = t[c];
+    }
+    // exp(-2 pi i m / 16) for m = b c: 1 = (c1, -s1), 2 = (h, -h), 3 = (s1, -c1),
+    // 4 = -i, 6 = (-h, -h), 9 = (-c1, s1)
+    v[1][1] = cmul(v[1][1], make_float2(c1, -s1));
+    v[1][2] = cmul(v[1][2], make_float2(h, -h));
+    v[1][3] = cmul(v[1][3], make_float2(s1, -c1));
+    v[2][1] = cmul(v[2][1], make_float2(h, -h));
+    v[2][2] = mul_neg_i(v[2][2]);
+    v[2][3] = cmul(v[2][3], make_float2(-h, -h));
+    v[3][1] = cmul(v[3][1], make_float2(s1, -c1));
+    v[3][2] = cmul(v[3][2], make_float2(-h, -h));
+    v[3][3] = cmul(v[3][3], make_float2(-c1, s1));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float2 t[4] = {v[0][c], v[1][c], v[2][c], v[3][c]};
+      Dft<4>::run(t);
+#pragma unroll
+      for (int d = 0; d < 4; ++d) u[c + 4 * d] = t[d];
+    }
+  }
+};
+
 // Radix of the pass that follows span P: 5 while M/P has a factor 5, then 8
 // while possible, then the leftover 4 or 2.
 template <int M, int P>
@@ -207,13 +244,35 @@ __device__ __forceinline__ bool run(float2 *a, float2 *b, const float2 *W) {
   }
 }
 
+// Radix of the in-place pass that follows span P: 16 for the first pass of
+// the in-place sizes (M >= 4096; it needs no twiddle factors, so its 16
+// points fit the registers of two 512-thread CTAs per SM), then the rule of
+// next_radix.  One pass fewer than radix 8 at M = 8192, and no pass with span
+// 8, whose butterflies fall two lanes to a bank.
+template <int M, int P>
+__host__ __device__ constexpr int ip_radix() {
+  return (P == 1 && M >= 4096 && M % 16 == 0) ? 16 : next_radix<M, P>();
+}
+
+// Offset of the in-place pass with span Q in the twiddle table (the rows of
+// rows_offset, for the passes of ip_radix).
+template <int M, int Q, int P = 1>
+__host__ __device__ constexpr int ip_rows_offset() {
+  if constexpr (P >= Q) {
+    return 0;
+  } else {
+    constexpr int R = ip_radix<M, P>();
+    return (P > 1 ? P * row_stride<R>() : 0) + ip_rows_offset<M, Q, P * R>();
+  }
+}
+
 // In-place form (decimation in time) for transforms too large for two
 // buffers: the input goes to the digit-reversed position dit_pos(n), and the
 // pass of radix R after span P applies butterfly (g, k), k < P, to the
 // elements g R P + k + j P (j < R), multiplying element j by
-// exp(-2 pi i j k / (P R)) -- the same factors, and table rows, as the
-// Stockham pass -- and writing output l back to g R P + k + l P.  After the
-// last pass the result is in natural order.
+// exp(-2 pi i j k / (P R)) -- the same factors, and the same row layout, as
+// the Stockham pass, for the radices of ip_radix -- and writing output l back
+// to g R P + k + l P.  After the last pass the result is in natural order.
 //
 // Position of input n: the first pass transforms the R1 inputs n' + j M/R1
 // (j < R1) of group n' < M/R1, which sit at R1 dit_pos<M/R1>(n') + j.
@@ -222,7 +281,7 @@ __device__ __forceinline__ int dit_pos(int n) {
   if constexpr (M == 1) {
     return 0;
   } else {
-    constexpr int R = next_radix<M, 1>();
+    constexpr int R = ip_radix<M, 1>();
     constexpr int S = M / R;
     return dit_pos<S>(n % S) * R + n / S;
   }
@@ -243,7 +302,7 @@ __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict
 #pragma unroll
     for (int r = 0; r < ROUNDS; ++r) {
       const int t = static_cast<int>(threadIdx.x) + r * NT;
-      const float2 *row = W + rows_offset<M, P>() + (t % P) * row_stride<R>();
+      const float2 *row = W + ip_rows_offset<M, P>() + (t % P) * row_stride<R>();
 #pragma unroll
       for (int j = 1; j < R; ++j) tw[r][j] = __ldg(row + j - 1);
     }
@@ -261,7 +320,7 @@ __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict
 #pragma unroll
       for (int j = 1; j < R; ++j) u[j] = cmul(u[j], tw[r][j]);
     } else if constexpr (P > 1) {
-      const float2 *row = W + rows_offset<M, P>() + k * row_stride<R>();
+      const float2 *row = W + ip_rows_offset<M, P>() + k * row_stride<R>();
 #pragma unroll
       for (int j = 1; j < R; ++j) u[j] = cmul(u[j], __ldg(row + j - 1));
     }
@@ -271,11 +330,11 @@ __device__ __forceinline__ void pass_inplace(float2 *x, const float2 *__restrict
   }
 }
 
-// Every pass, in place; a block barrier follows each.
+// Every pass from span P on, in place; a block barrier follows each.
 template <int M, int NT, int P = 1>
 __device__ __forceinline__ void run_inplace(float2 *x, const float2 *W) {
   if constexpr (P < M) {
-    constexpr int R = next_radix<M, P>();
+    constexpr int R = ip_radix<M, P>();
     pass_inplace<M, R, P, NT>(x, W);
     __syncthreads();
     run_inplace<M, NT, P * R>(x, W);

@@ -158,12 +158,13 @@ __device__ __forceinline__ float load_sample(const WaveArgs &a, int64_t b, int64
 // Above 4096 points one frame's two Stockham buffers and the twiddle table
 // (199 KB at 16384) leave room for a single CTA per SM.  Those sizes
 // transform in place instead (one buffer laid out with fft::LayoutIP, the
-// twiddle rows read through L1, a separate power row, samples gathered
+// twiddle rows read through L1, a separate power row, samples loaded
 // without staging), which fits two 512-thread CTAs per SM.  32 clips of
 // 160000 samples, hop n_fft / 4, L2 flushed, us per call: 8192: 155.6 with
 // one 1024-thread Stockham CTA, 145.4 in place with one padding level,
 // 141.1 with LayoutIP's two; 16384: 137.2 Stockham, 147.5 in place with one
-// level, 133.1 with two.
+// level, 133.1 with two.  (With direct framing, the filterbank image, and
+// the radix-16 first pass fused with the framing: 94.7 and 99.9.)
 constexpr bool in_place_nfft(int n_fft) { return n_fft >= 8192; }
 
 template <int NFFT>
@@ -263,30 +264,39 @@ __device__ __forceinline__ float2 pair_point(int v) {
 }
 
 // Framing of an interior frame for the in-place transform, its sample pairs
-// aligned: each thread loads PB sample pairs and their window pairs at a
-// time, all in flight together, and stores each windowed point n at its
-// digit-reversed position.  src points at the frame's first sample pair.
+// aligned, fused with the transform's first pass (radix 16, span 1, no
+// twiddle factors): thread g < M/16 loads the 16 points g + j M/16 (sample
+// pairs and window pairs, 8 of each in flight at a time), windows them, runs
+// the 16-point DFT in registers and stores output l at 16 dit_pos<M/16>(g) + l,
+// where the pass would have written it.  src points at the frame's first
+// sample pair.
 template <int M, int NT, typename Pair>
-__device__ __forceinline__ void frame_in_place(const Pair *src, const float2 *win2, float2 *buf) {
-  constexpr int PER = M / NT, PB = 8;
-  static_assert(M % NT == 0 && PER % PB == 0, "points per thread");
-#pragma unroll 1
-  for (int c = 0; c < PER; c += PB) {
-    Pair x[PB];
-    float2 w[PB];
+__device__ __forceinline__ void frame_first_pass(const Pair *src, const float2 *win2, float2 *buf) {
+  constexpr int S = M / 16;
+  static_assert(fft::ip_radix<M, 1>() == 16 && S <= NT, "one first-pass butterfly per thread");
+  const int g = static_cast<int>(threadIdx.x);
+  if (S < NT && g >= S) return;
+  float2 u[16];
 #pragma unroll
-    for (int j = 0; j < PB; ++j) {
-      const int n = static_cast<int>(threadIdx.x) + (c + j) * NT;
+  for (int c = 0; c < 16; c += 8) {
+    Pair x[8];
+    float2 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int n = g + (c + j) * S;
       x[j] = __ldg(src + n);
       w[j] = __ldg(win2 + n);
     }
 #pragma unroll
-    for (int j = 0; j < PB; ++j) {
-      const int n = static_cast<int>(threadIdx.x) + (c + j) * NT;
+    for (int j = 0; j < 8; ++j) {
       const float2 v = pair_point(x[j]);
-      buf[fft::LayoutIP<M>::at(fft::dit_pos<M>(n))] = make_float2(v.x * w[j].x, v.y * w[j].y);
+      u[c + j] = make_float2(v.x * w[j].x, v.y * w[j].y);
     }
   }
+  fft::Dft<16>::run(u);
+  const int base = 16 * fft::dit_pos<S>(g);
+#pragma unroll
+  for (int l = 0; l < 16; ++l) buf[fft::LayoutIP<M>::at(base + l)] = u[l];
 }
 
 template <int NFFT>
@@ -447,16 +457,18 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     // Power-of-two sizes fuse the framing into the first FFT pass; at 400
     // points the fused radix-5 pass measured slower than framing on its own.
     const bool fused = paired && C::kFuseFirst;
-    bool gathered = false;  // in place: the frame is already in the buffer
+    bool gathered = false;  // in place: the frame is in the buffer, its first pass done
     if constexpr (C::kInPlace) {
       const int64_t p0 = b * a.T + s_first;  // the frame's first sample
       if (interior && ((reinterpret_cast<uintptr_t>(a.wave) & (a.in_i16 ? 3u : 7u)) == 0) && (p0 & 1) == 0 &&
           LM_IN_BOUNDS(p0 + NFFT - 1, a.B * a.T, a.err)) {
         const float2 *win2 = reinterpret_cast<const float2 *>(win);
         if (a.in_i16)
-          frame_in_place<M, NT>(reinterpret_cast<const int *>(static_cast<const int16_t *>(a.wave) + p0), win2, bufA);
+          frame_first_pass<M, NT>(reinterpret_cast<const int *>(static_cast<const int16_t *>(a.wave) + p0), win2,
+                                  bufA);
         else
-          frame_in_place<M, NT>(reinterpret_cast<const float2 *>(static_cast<const float *>(a.wave) + p0), win2, bufA);
+          frame_first_pass<M, NT>(reinterpret_cast<const float2 *>(static_cast<const float *>(a.wave) + p0), win2,
+                                  bufA);
         gathered = true;
       }
     }
@@ -593,7 +605,13 @@ __global__ void __launch_bounds__(WaveCfg<NFFT>::NT, WaveCfg<NFFT>::kMinBlocks) 
     // for aligned staged tiles, whose result is then in bufB)
     bool in_b;
     if constexpr (C::kInPlace) {
-      fft::run_inplace<M, NT>(bufA, a.tw_m);
+      // (frames gathered point by point still need the first pass)
+      constexpr int R0 = fft::ip_radix<M, 1>();
+      if (!gathered) {
+        fft::pass_inplace<M, R0, 1, NT>(bufA, a.tw_m);
+        __syncthreads();
+      }
+      fft::run_inplace<M, NT, R0>(bufA, a.tw_m);
       in_b = false;
     } else if constexpr (C::kFuseFirst) {
       if (fused) {
@@ -890,7 +908,12 @@ void build_tables(const lm_mel_params &p, HostTables *t) {
     size_t off = 0;
     for (int P = 1; P < M;) {
       const int q = M / P;
-      const int R = q % 5 == 0 ? 5 : q % 8 == 0 ? 8 : q % 4 == 0 ? 4 : 2;
+      // (the in-place sizes open with a radix-16 pass: fft::ip_radix)
+      const int R = (P == 1 && in_place_nfft(N) && M % 16 == 0) ? 16
+                    : q % 5 == 0                                 ? 5
+                    : q % 8 == 0                                 ? 8
+                    : q % 4 == 0                                 ? 4
+                                                                 : 2;
       if (P > 1) {
         const int stride = R == 5 ? 5 : R - 1;
         for (int k = 0; k < P; ++k) {
