@@ -187,8 +187,10 @@ struct WaveCfg {
   // hop n_fft / 4, 128 bands, L2 flushed, us per call with 256 / 512 / 1024
   // threads: 2048: 84.0 / 124.9 / 147.5; 4096: 105.5 / 94.2 / 106.5; 8192:
   // 303.1 / 188.4 / 155.6; 16384: 313.3 / 190.5 / 138.2.  8192 and 16384 now
-  // run in place, two 512-thread CTAs per SM (see in_place_nfft).
-  static constexpr int NT = (kInPlace || NFFT == 4096) ? 512 : 256;
+  // run in place (see in_place_nfft): 16384 with two 512-thread CTAs per SM,
+  // 8192 with four of 256 threads, whose 50 KB of shared memory allow it
+  // (86.5 us against 94.3 with two of 512).
+  static constexpr int NT = (NFFT == 4096 || NFFT == 16384) ? 512 : 256;
   static_assert(NT % 32 == 0 && NT % TF == 0, "thread count");
   // Up to 4096 every table sits in shared memory; beyond, only the FFT
   // twiddles do and the window, untangle twiddles and filterbank are read
@@ -198,7 +200,8 @@ struct WaveCfg {
   // capped to match so they do not lower the occupancy further.  400 points
   // gets no minimum (0): the compiler's own choice there is 64 registers,
   // while an explicit 4 made it spill and 1 let it take 104.
-  static constexpr int kMinBlocks = NFFT == 400 ? 0 : (NFFT <= 512 ? 4 : (NFFT <= 1024 || kInPlace ? 2 : 1));
+  static constexpr int kMinBlocks =
+      NFFT == 400 ? 0 : (NFFT <= 512 || NFFT == 8192 ? 4 : (NFFT <= 1024 || kInPlace ? 2 : 1));
   static constexpr bool kFuseFirst = (M & (M - 1)) == 0;
   // The power tile (TF rows of NFP floats) lives in whichever FFT buffer does
   // not hold the transform's result; it needs at most half of it.
